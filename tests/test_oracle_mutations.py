@@ -1,0 +1,187 @@
+"""Plant plausible mistakes in the oracle (on the CPU) and check that the pins
+catch every one of them: a dropped term, a wrong sign or index, a transposed
+or swapped operand, a wrong digit or bit order, a wrong plane offset."""
+import numpy as np
+import pytest
+
+import oracle
+import oracle.ternary as T
+import pins
+
+
+def _patch(monkeypatch, name, fn):
+    monkeypatch.setattr(T, name, fn)
+    if hasattr(oracle, name):
+        monkeypatch.setattr(oracle, name, fn)
+
+
+def _orig(name):
+    return getattr(T, name)
+
+
+def m_pq2_msb_first(mp):
+    def dec(base_g):
+        b = base_g.astype(np.int64)
+        f = [((b >> (6 - 2 * i)) & 3) for i in range(4)]
+        return np.stack(f, -1).reshape(base_g.shape[:-1] + (128,)) - 1
+    _patch(mp, "_decode_pq2", dec)
+
+
+def m_pq2_twos_complement(mp):
+    def dec(base_g):
+        b = base_g.astype(np.int64)
+        f = [((b >> (2 * i)) & 3) for i in range(4)]
+        c = np.stack(f, -1).reshape(base_g.shape[:-1] + (128,))
+        return np.where(c >= 2, c - 4, c)
+    _patch(mp, "_decode_pq2", dec)
+
+
+def m_pq2_no_offset(mp):
+    orig = _orig("_decode_pq2")
+    _patch(mp, "_decode_pq2", lambda b: orig(b) + 1)
+
+
+def m_ptq1_big_endian(mp):
+    def dec(base_g, high_g):
+        b = base_g.astype(np.int64)
+        h = high_g.astype(np.int64)
+        lead = base_g.shape[:-1]
+        lo = np.stack([(b // 3 ** (4 - i)) % 3 for i in range(5)], -1).reshape(lead + (120,))
+        hi = np.stack([(h // 3 ** (3 - i)) % 3 for i in range(4)], -1).reshape(lead + (8,))
+        return np.concatenate([lo, hi], -1) - 1
+    _patch(mp, "_decode_ptq1", dec)
+
+
+def m_ptq1_high_first(mp):
+    orig = _orig("_decode_ptq1")
+    def dec(base_g, high_g):
+        v = orig(base_g, high_g)
+        return np.concatenate([v[..., 120:], v[..., :120]], -1)
+    _patch(mp, "_decode_ptq1", dec)
+
+
+def m_forward_no_normalisation(mp):
+    orig = _orig("hadamard_forward")
+    _patch(mp, "hadamard_forward", lambda x, s: orig(x, s) * 32.0)
+
+
+def m_forward_signs_after(mp):
+    _patch(mp, "hadamard_forward", _orig("hadamard_inverse"))
+
+
+def m_inverse_signs_before(mp):
+    _patch(mp, "hadamard_inverse", _orig("hadamard_forward"))
+
+
+def m_signs_not_global(mp):
+    orig = _orig("hadamard_forward")
+    def fw(x, s):
+        s = np.asarray(s, dtype=np.float64).reshape(-1)
+        return orig(x, np.tile(s[:1024], s.size // 1024) if s.size % 1024 == 0 else s)
+    _patch(mp, "hadamard_forward", fw)
+
+
+def m_sequency_order(mp):
+    orig = _orig("hadamard_matrix")
+    def H(size=1024):
+        h = orig(size)
+        order = np.argsort((np.abs(np.diff(h, axis=1)) > 0).sum(axis=1), kind="stable")
+        return h[order]
+    _patch(mp, "hadamard_matrix", H)
+
+
+def m_scale_offset_in_high_plane(mp):
+    orig = _orig("row_split_geometry")
+    def geo(fmt, n, k):
+        g = orig(fmt, n, k)
+        return g._replace(scale_offset=g.base_bytes)
+    _patch(mp, "row_split_geometry", geo)
+
+
+def m_high_offset_unaligned(mp):
+    orig = _orig("row_split_geometry")
+    def geo(fmt, n, k):
+        g = orig(fmt, n, k)
+        d = g.high_offset - g.base_bytes
+        return g._replace(high_offset=g.base_bytes, scale_offset=g.scale_offset - d,
+                          payload_bytes=g.payload_bytes - d)
+    _patch(mp, "row_split_geometry", geo)
+
+
+def m_kpad_not_aligned(mp):
+    orig = _orig("row_split_geometry")
+    def geo(fmt, n, k):
+        g = orig(fmt, n, k)
+        return g._replace(k_pad=k)
+    _patch(mp, "row_split_geometry", geo)
+
+
+def m_scale_wrong_group(mp):
+    orig = _orig("dequantize")
+    def deq(fmt, payload, n, k, rows=None):
+        w = orig(fmt, payload, n, k, rows)
+        return np.roll(w.reshape(w.shape[0], -1, 128), 1, axis=1).reshape(w.shape) if k % 128 == 0 else w
+    _patch(mp, "dequantize", deq)
+
+
+def m_scale_dropped(mp):
+    orig = _orig("dequantize")
+    def deq(fmt, payload, n, k, rows=None):
+        w = orig(fmt, payload, n, k, rows)
+        return np.sign(w)
+    _patch(mp, "dequantize", deq)
+
+
+def m_transform_dropped(mp):
+    def mm(fmt, payload, n, k, x, signs=None, rows=None):
+        x = np.atleast_2d(np.asarray(x, dtype=np.float64))
+        return x @ T.dequantize(fmt, payload, n, k, rows).T
+    _patch(mp, "ternary_matmul", mm)
+
+
+def m_rows_reversed(mp):
+    orig = _orig("ternary_matmul")
+    _patch(mp, "ternary_matmul", lambda *a, **kw: orig(*a, **kw)[:, ::-1])
+
+
+def m_embed_forward(mp):
+    def emb(fmt, payload, n, k, ids, signs):
+        return T.hadamard_forward(T.dequantize(fmt, payload, n, k, ids), signs)
+    _patch(mp, "embed_rows", emb)
+
+
+def m_blocks_scale_after(mp):
+    monkeypatch_slices = dict(T.BLOCK_PLANE_SLICES)
+    monkeypatch_slices["PQ2_0_G128"] = ((0, 32), None, (32, 34))
+    mp.setattr(T, "BLOCK_PLANE_SLICES", monkeypatch_slices)
+
+
+def m_pack_pad_minus_one(mp):
+    orig = _orig("pack_planes")
+    def pk(fmt, values, scales):
+        values = np.asarray(values)
+        n, k = values.shape
+        kp = -(-k // 128) * 128
+        if kp == k:
+            return orig(fmt, values, scales)
+        full = np.full((n, kp), -1, np.int8)
+        full[:, :k] = values
+        p = orig(fmt, full, scales)
+        return p
+    _patch(mp, "pack_planes", pk)
+
+
+MUTATIONS = [v for k, v in sorted(globals().items()) if k.startswith("m_")]
+
+
+@pytest.mark.parametrize("mutation", MUTATIONS, ids=lambda f: f.__name__)
+def test_mutation_is_caught(mutation, monkeypatch):
+    mutation(monkeypatch)
+    caught = []
+    for pin in pins.ALL_PINS:
+        try:
+            pin()
+        except Exception as exc:  # an assertion or a shape/value error both count
+            caught.append((pin.__name__, type(exc).__name__))
+            break
+    assert caught, f"no pin catches {mutation.__name__}"
