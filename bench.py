@@ -1,0 +1,382 @@
+"""Benchmark of the fused Hadamard-rotated ternary GEMV on GB300.
+
+Default workload: FFN gate/up decode projection, PQ2_0_G128 n=17408 k=5120,
+M=1 bf16 activation, seed 1 (synthetic inputs with the pages' distributions).
+One step = one call of ninfer_ternary_matmul (rotate + decode + GEMV) on one
+activation row. Inputs are resident in HBM; L2 reuse is defeated by cycling a
+pool of weight-payload copies whose total size is more than 3x the L2 cache.
+Steps are captured in CUDA graphs and timed with CUDA events on the launching
+stream.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload gateup|down|down_m8|head|head_m8|tiny]
+  python bench.py --impl reference ...   (the fp64 CPU oracle on the host cores)
+
+Prints one JSON line (rank 0).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "fused ternary GEMV weight GB/s & % of HBM roofline at 17408x5120; tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def algorithmic_bytes(w, M: int) -> dict:
+    """Bytes the method must move per call: packed planes + activations + signs + fp32 output."""
+    groups = -(-w.k // 128)
+    per_group = 34 if w.fmt == "PQ2_0_G128" else 28
+    weights = w.n * groups * per_group
+    xb = M * w.k * (4 if w.x_dtype == "f32" else 2)
+    sb = w.k * 2
+    yb = M * w.n * 4
+    return {"weights": weights, "x": xb, "signs": sb, "y": yb, "total": weights + xb + sb + yb}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            p = json.load(fh)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def profile_traffic(kernel_tag: str, workload: str, source_files):
+    """Per-launch DRAM bytes from the committed ncu summary for this kernel and
+    workload, or None when absent or when the kernel sources changed since."""
+    path = os.path.join(ROOT, "profiles", f"{kernel_tag}_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    txt = open(path, encoding="utf-8").read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    h = re.search(r"source_sha256:\s*([0-9a-f]{64})", txt)
+    if not m or not h or h.group(1) != sources_sha256(source_files):
+        return None
+    return float(m.group(1))
+
+
+def sources_sha256(files) -> str:
+    d = hashlib.sha256()
+    for f in sorted(files):
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            d.update(fh.read())
+    return d.hexdigest()
+
+
+GEMV_SOURCES = ["bit_gemv_gb300/csrc/gemm_simple.cu", "bit_gemv_gb300/csrc/hadamard.cu",
+                "bit_gemv_gb300/csrc/matmul.cu", "bit_gemv_gb300/csrc/device.cuh",
+                "bit_gemv_gb300/csrc/plane.cuh"]
+KERNEL_TAG = "gemv"
+
+
+# ------------------------------------------------------------------ clocks ---
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+
+    def start(self):
+        os.makedirs(os.path.dirname(self.path), exist_ok=True)
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        loaded = [s for s in sm if s >= 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------- our arm ---
+def run_ours(args, rank: int, world: int, local_rank: int):
+    import torch
+
+    import bit_gemv_gb300 as nt
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = synth.WORKLOADS[args.workload]
+    c = synth.make_case(w)
+    n, k, M = w.n, w.k, w.M
+    nbytes = algorithmic_bytes(w, M)
+    payload_host = nt.ninfer_ternary_pack(w.fmt, c.values, c.scales)
+    del c.values
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    pool = max(2, -(-3 * l2 // payload_host.size))
+    payloads = [torch.from_numpy(payload_host).to(dev) for _ in range(pool)]
+    signs = torch.from_numpy(c.signs.view(np.int16)).to(dev)
+    if w.x_dtype == "bf16":
+        x_host = torch.from_numpy(c.x_raw.view(np.int16)).view(torch.bfloat16)
+    else:
+        x_host = torch.from_numpy(c.x)
+    x = x_host.to(dev)
+    y = torch.empty((M, n), dtype=torch.float32, device=dev)
+    ws_bytes = nt.ninfer_ternary_matmul_workspace(w.fmt, n, k, M, True)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(dev)
+
+    def step(i):
+        nt.ninfer_ternary_matmul(w.fmt, payloads[i % pool], n, k, x, signs, y=y, workspace=ws)
+
+    # e2e buffers: pinned host activations in, pinned host result out
+    x_pin = [x_host.clone().pin_memory() for _ in range(pool)]
+    y_pin = [torch.empty((M, n), dtype=torch.float32).pin_memory() for _ in range(pool)]
+
+    def step_e2e(i):
+        x.copy_(x_pin[i % pool], non_blocking=True)
+        step(i)
+        y_pin[i % pool].copy_(y, non_blocking=True)
+
+    per_graph = min(args.steps, 1000)
+
+    def capture(fn, count, offset=0):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(count):
+                    fn(offset + i)
+        return g
+
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 1)):     # eager warm-up (module load, first launches)
+            step(i)
+    stream.synchronize()
+    full, rem = divmod(args.steps, per_graph)
+    g_main = capture(step, per_graph)
+    g_rem = capture(step, rem, per_graph * full) if rem else None
+    g_e2e = capture(step_e2e, per_graph)
+    g_e2e_rem = capture(step_e2e, rem, per_graph * full) if rem else None
+
+    def timed(graph, graph_rem, warm_graph_replays):
+        with torch.cuda.stream(stream):
+            for _ in range(warm_graph_replays):
+                graph.replay()
+        stream.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(full):
+                graph.replay()
+            if graph_rem is not None:
+                graph_rem.replay()
+            e1.record(stream)
+        e1.synchronize()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([ms], device=dev, dtype=torch.float64)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            ms = float(t.item())
+            torch.distributed.barrier()
+        return ms
+
+    warm_replays = max(1, -(-args.warmup // per_graph))
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    ms_total = timed(g_main, g_rem, warm_replays)
+    clock_info = clocks.stop()
+    ms_e2e = timed(g_e2e, g_e2e_rem, warm_replays)
+
+    # final output check against the first warm-up result (same inputs -> same bits)
+    torch.cuda.synchronize()
+    ms_step = ms_total / args.steps
+    s_step = ms_step / 1e3
+    value = world * nbytes["weights"] / s_step / 1e9
+    achieved = nbytes["total"] / s_step / 1e9
+    peak, peak_kind = measured_peaks()
+    e2e_s = ms_e2e / args.steps / 1e3
+    traffic = profile_traffic(KERNEL_TAG, args.workload, GEMV_SOURCES)
+    res = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 6),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "format": w.fmt, "n": n, "k": k, "M": M, "x_dtype": w.x_dtype,
+                   "seed": w.seed, "rotate": True,
+                   "l2": f"rotating pool of {pool} payload copies ({pool * payload_host.size / 1e6:.0f} MB > 3x L2 "
+                         f"{l2 / 1e6:.0f} MB)",
+                   "parallelism": f"replicas x{world}"},
+        "tokens_per_s": round(world * M / s_step, 1),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "peak_source": f"{peak_kind} hbm_gbs (copy)", "frac_of_8000_nominal": round(achieved / 8000, 4)},
+        "e2e": {"value": round(world * nbytes["weights"] / e2e_s / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": int(x_host.numel() * x_host.element_size()),
+                "d2h_bytes_per_step": int(M * n * 4), "ms_per_step": round(ms_e2e / args.steps, 6)},
+        "clocks": clock_info,
+        "gpu_launches": args.steps * kernels_per_step(),
+    }
+    return res
+
+
+def kernels_per_step() -> int:
+    return 2          # forward transform + tiled GEMV
+
+
+# ------------------------------------------------------------ CPU oracle ---
+def cpu_oracle_sample(workload: str, rows: int, reps: int) -> dict:
+    """Time the fp64 oracle on `rows` rows of the workload (single thread)."""
+    import oracle
+
+    w = synth.WORKLOADS[workload]
+    c = synth.make_case(w, n=rows)
+    payload = oracle.pack_planes(w.fmt, c.values, c.scales)
+    D = synth.bf16_bits_to_f32(c.signs)
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle.ternary_matmul(w.fmt, payload, rows, w.k, c.x, D)
+    dt = (time.perf_counter() - t0) / reps
+    groups = -(-w.k // 128)
+    wbytes = rows * groups * (34 if w.fmt == "PQ2_0_G128" else 28)
+    return {"seconds_per_call": dt, "weight_bytes": wbytes, "rows": rows}
+
+
+def run_cpu_child(workload: str, rows: int, reps: int) -> dict:
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    out = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-child", workload, str(rows), str(reps)],
+                         capture_output=True, text=True, env=env, timeout=900)
+    if out.returncode != 0:
+        raise RuntimeError(out.stderr[-2000:])
+    return json.loads(out.stdout.strip().splitlines()[-1])
+
+
+def cpu_baseline(workload: str) -> dict:
+    w = synth.WORKLOADS[workload]
+    rows = min(w.n, 17408)
+    r = run_cpu_child(workload, rows, 2)
+    gbs = r["weight_bytes"] / r["seconds_per_call"] / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{rows} of {w.n} rows of the {workload} workload, 2 calls, fp64 numpy, 1 thread",
+            "seconds_per_call": round(r["seconds_per_call"], 4),
+            "tokens_per_s_full_matrix": round(w.M / (r["seconds_per_call"] * w.n / rows), 4)}
+
+
+def run_reference(args, rank: int, world: int):
+    if rank != 0:
+        return None
+    w = synth.WORKLOADS[args.workload]
+    # size each step's row sample so that warm-up + timed steps take ~2 minutes
+    cal = run_cpu_child(args.workload, min(w.n, 256), 1)
+    per_row = cal["seconds_per_call"] / min(w.n, 256)
+    rows = int(max(1, min(w.n, 120.0 / (args.steps + args.warmup) / per_row)))
+    run_cpu_child(args.workload, rows, args.warmup)
+    r = run_cpu_child(args.workload, rows, max(args.steps, 1))
+    gbs = r["weight_bytes"] / r["seconds_per_call"] / 1e9
+    sample = f"each step: {rows} of {w.n} rows of the {args.workload} workload, fp64 numpy oracle, 1 thread"
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(r["seconds_per_call"] * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "format": w.fmt, "n": w.n, "k": w.k, "M": w.M, "x_dtype": w.x_dtype,
+                   "seed": w.seed, "rotate": True},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    if len(sys.argv) > 1 and sys.argv[1] == "--cpu-child":
+        print(json.dumps(cpu_oracle_sample(sys.argv[2], int(sys.argv[3]), int(sys.argv[4]))))
+        return
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="gateup", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+        if res is not None:
+            print(json.dumps(res))
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    res = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline(args.workload)
+        print(json.dumps(res))
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

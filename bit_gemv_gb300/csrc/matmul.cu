@@ -1,0 +1,69 @@
+// ninfer_ternary_matmul: argument checks, workspace sizing and dispatch.
+#include <cuda_runtime.h>
+
+#include "common.h"
+#include "device.cuh"
+#include "plane.cuh"
+
+namespace ninfer {
+int gemm_simple_launch(const PlaneView &p, uint64_t n, uint64_t k, const void *a, int a_dtype, uint64_t M, void *y,
+                       int y_dtype, cudaStream_t stream);
+}
+
+using namespace ninfer;
+
+static uint64_t workspace_bytes_for(uint64_t M, uint64_t k, bool rotate) {
+    return rotate ? M * k * sizeof(float) : 0;   // rotated activations, fp32
+}
+
+extern "C" int ninfer_ternary_matmul_workspace(int fmt, uint64_t n, uint64_t k, uint64_t M, int rotate,
+                                               uint64_t *bytes) {
+    ninfer_row_split_geometry g;
+    int st = geometry(fmt, n, k, &g);
+    if (st) return st;
+    if (!bytes) return fail(NINFER_ERR_INVALID_ARGUMENT, "workspace: NULL output");
+    if (M == 0) return fail(NINFER_ERR_SHAPE, "workspace: M must be positive");
+    uint64_t mk;
+    if (!mul_ok(M, k, &mk) || mk > (UINT64_MAX / 8)) return fail(NINFER_ERR_OVERFLOW, "workspace size overflows");
+    *bytes = workspace_bytes_for(M, k, rotate != 0);
+    return NINFER_OK;
+}
+
+extern "C" int ninfer_ternary_matmul(int fmt, const uint8_t *payload, uint64_t payload_bytes, uint64_t n, uint64_t k,
+                                     const void *x, int x_dtype, const uint16_t *signs_bf16, void *y, int y_dtype,
+                                     uint64_t M, void *workspace, uint64_t workspace_bytes, ninfer_stream stream) {
+    ninfer_row_split_geometry g;
+    int st = geometry(fmt, n, k, &g);
+    if (st) return st;
+    if (!payload || !x || !y) return fail(NINFER_ERR_INVALID_ARGUMENT, "matmul: NULL payload, x or y");
+    if (M == 0) return fail(NINFER_ERR_SHAPE, "matmul: M must be positive");
+    if (!dtype_valid(x_dtype)) return fail(NINFER_ERR_INVALID_ARGUMENT, "matmul: x dtype %d unsupported", x_dtype);
+    if (y_dtype != NINFER_F32 && y_dtype != NINFER_BF16)
+        return fail(NINFER_ERR_INVALID_ARGUMENT, "matmul: y dtype must be f32 or bf16");
+    if (payload_bytes != g.payload_bytes)
+        return fail(NINFER_ERR_SIZE_MISMATCH, "payload stores %llu bytes; layout requires %llu",
+                    (unsigned long long)payload_bytes, (unsigned long long)g.payload_bytes);
+    if (!aligned(payload, 256)) return fail(NINFER_ERR_ALIGNMENT, "matmul: payload must be 256-byte aligned");
+    if (!aligned(x, 16) || !aligned(y, 16)) return fail(NINFER_ERR_ALIGNMENT, "matmul: x and y must be 16-byte aligned");
+    const bool rotate = signs_bf16 != nullptr;
+    if (rotate && k % 1024)
+        return fail(NINFER_ERR_SHAPE, "matmul: k=%llu is not a multiple of 1024; the rotated input needs whole blocks",
+                    (unsigned long long)k);
+    if (rotate && !aligned(signs_bf16, 16)) return fail(NINFER_ERR_ALIGNMENT, "matmul: signs must be 16-byte aligned");
+    const uint64_t need = workspace_bytes_for(M, k, rotate);
+    if (need && (!workspace || workspace_bytes < need))
+        return fail(NINFER_ERR_SIZE_MISMATCH, "matmul: workspace of %llu bytes needed, %llu given",
+                    (unsigned long long)need, (unsigned long long)workspace_bytes);
+    if (need && !aligned(workspace, 16)) return fail(NINFER_ERR_ALIGNMENT, "matmul: workspace must be 16-byte aligned");
+    cudaStream_t s = (cudaStream_t)stream;
+    const PlaneView p = make_view(payload, g, fmt);
+    const void *a = x;
+    int a_dtype = x_dtype;
+    if (rotate) {
+        st = ninfer_hadamard_fwd(x, x_dtype, workspace, NINFER_F32, signs_bf16, M, k, stream);
+        if (st) return st;
+        a = workspace;
+        a_dtype = NINFER_F32;
+    }
+    return gemm_simple_launch(p, n, k, a, a_dtype, M, y, y_dtype, s);
+}

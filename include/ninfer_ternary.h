@@ -1,0 +1,242 @@
+/*
+ * ninfer_ternary.h -- C ABI of the GB300 (sm_103a) Hadamard-rotated ternary
+ * projection library (libninfer_ternary.so).
+ *
+ * The library computes y = W . T(x): activations x (M x k) are rotated by the
+ * signed block Walsh-Hadamard transform T(x) = H(D.x)/sqrt(1024) per 1024-wide
+ * block, and multiplied by ternary weights W (n x k) stored in the row-split
+ * PQ2_0_G128 / PTQ1_0_G128 plane layout. It also provides the inverse transform
+ * for embedding rows, the host-side plane geometry and plane packers.
+ *
+ * Sources (web pages; cited by title and section):
+ *   [FMT]  "bonsai三元GGUF模型转ninfer模型01" -- ninfer ternary artifact format
+ *          page: §2 ternary numeric formats, §3 row-split plane geometry,
+ *          §4 block <-> plane conversion, §6 constants.
+ *   [GGUF] "GGUF 完整讲解" -- §4.3 the Q2_0 dequantisation (2-bit field order,
+ *          offset code -> value).
+ *   [V3]   NInfer "artifact-container.md" -- §6.1 numeric formats, §6.2 layouts
+ *          (256-byte object alignment), §8 the hadamard_signs auxiliary,
+ *          §11.3 / §12.6 error ownership ("refuse rather than run wrong").
+ *   [TS]   "从 TensorSharp 视角解读 Ternary Bonsai 2 27B" -- §4.2 transform
+ *          contract, §4.4 where the transforms apply.
+ *
+ * Conventions shared by every entry point
+ *   - Sizes are uint64_t element or byte counts; data is little-endian.
+ *   - Every function returns an ninfer_status. NINFER_OK is 0. On any other
+ *     status nothing was launched or written, and ninfer_last_error() returns a
+ *     thread-local message naming the argument at fault.
+ *   - Host pointers ("host") are read/written synchronously. Device pointers
+ *     ("device") must be device (or managed) memory the caller allocated and
+ *     owns; the library never frees or retains them, and performs all device
+ *     work asynchronously on the given stream (a cudaStream_t; NULL = the
+ *     legacy default stream). Device pointers must be 16-byte aligned; packed
+ *     weight payloads 256-byte aligned (the plane alignment of [FMT] §1 and
+ *     [V3] §6.2).
+ *   - The library allocates no device memory in any call. Kernels never trap
+ *     or assert; device-side input problems are reported through an optional
+ *     caller-owned status word.
+ */
+#ifndef NINFER_TERNARY_H
+#define NINFER_TERNARY_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define NINFER_TERNARY_ABI_VERSION 1
+
+/* Numeric formats ([FMT] §2, GGUF type ids from [FMT] §6 / [TS] §4.1). */
+typedef enum {
+    NINFER_PQ2_0_G128 = 142,  /* 32 base bytes + 2 scale bytes per 128 weights */
+    NINFER_PTQ1_0_G128 = 143  /* 24 base + 2 high + 2 scale bytes per 128 weights */
+} ninfer_format;
+
+/* Element types of activations / outputs. */
+typedef enum {
+    NINFER_F32 = 0,
+    NINFER_BF16 = 1,
+    NINFER_F16 = 2
+} ninfer_dtype;
+
+typedef enum {
+    NINFER_OK = 0,
+    NINFER_ERR_INVALID_ARGUMENT = 1, /* null pointer, zero size, bad enum value */
+    NINFER_ERR_UNKNOWN_FORMAT = 2,   /* format id is not 142 / 143 */
+    NINFER_ERR_SHAPE = 3,            /* shape violates a rule (e.g. k % 1024 with signs) */
+    NINFER_ERR_SIZE_MISMATCH = 4,    /* buffer size != the size the layout requires */
+    NINFER_ERR_ALIGNMENT = 5,        /* pointer not aligned as required */
+    NINFER_ERR_INVALID_CODE = 6,     /* packed bytes hold no ternary value */
+    NINFER_ERR_CUDA = 7,             /* a CUDA runtime call failed (message has it) */
+    NINFER_ERR_OVERFLOW = 8          /* a size does not fit in 64 bits */
+} ninfer_status;
+
+/* cudaStream_t without including CUDA headers. */
+typedef struct CUstream_st *ninfer_stream;
+
+/*
+ * RowSplitGeometry: the 16 fields of row_split_geometry(format, shape), in the
+ * page's order ([FMT] §3):
+ *   k_pad = align_up(k, 128); groups_per_row = k_pad / 128;
+ *   *_row_bytes = groups_per_row * per-group bytes (scale: 2, one binary16);
+ *   base_offset = 0; high_offset = align_up(base_bytes, 256) (computed even
+ *   when high_bytes == 0, so PQ2_0 has scale_offset == high_offset);
+ *   scale_offset = high_offset + align_up(high_bytes, 256);
+ *   payload_bytes = scale_offset + scale_bytes;
+ *   plane sizes are n * the per-row sizes.
+ * Planes are row-major [row][group][bytes].
+ */
+typedef struct {
+    uint64_t n, k, k_pad, groups_per_row;
+    uint64_t base_bytes_per_group, high_bytes_per_group;
+    uint64_t base_row_bytes, high_row_bytes, scale_row_bytes;
+    uint64_t base_offset, base_bytes;
+    uint64_t high_offset, high_bytes;
+    uint64_t scale_offset, scale_bytes;
+    uint64_t payload_bytes;
+} ninfer_row_split_geometry;
+
+/* Thread-local description of the last non-OK status returned on this thread. */
+const char *ninfer_last_error(void);
+/* Static name of a status value ("NINFER_OK", ...). */
+const char *ninfer_status_name(int status);
+/* NINFER_TERNARY_ABI_VERSION of the loaded library. */
+int ninfer_abi_version(void);
+
+/*
+ * ninfer_ternary_geometry -- [FMT] §3 row_split_geometry.
+ *   fmt: ninfer_format; n, k: output rows and input width, both > 0.
+ *   out: host struct, written on success.
+ * Errors: UNKNOWN_FORMAT, SHAPE (n or k == 0), OVERFLOW, INVALID_ARGUMENT (out NULL).
+ */
+int ninfer_ternary_geometry(int fmt, uint64_t n, uint64_t k,
+                            ninfer_row_split_geometry *out);
+
+/*
+ * ninfer_ternary_pack -- ternary values + group scales -> row-split payload (host).
+ *   values: host int8[n * k], row-major, each -1, 0 or +1.
+ *   scales_f16: host uint16[n * groups_per_row], binary16 bit patterns, one per
+ *     128-weight group ([FMT] §3: "one binary16 per group").
+ *   payload: host uint8[payload_bytes] written completely (pad bytes included).
+ * Encoding (value v, code c = v + 1):
+ *   PQ2_0_G128: group byte j holds weights 4j..4j+3, weight i in bits
+ *     2*(i % 4) (least significant field first) -- the Q2_0 layout of
+ *     [GGUF] §4.3, where code c decodes to c - 1.
+ *   PTQ1_0_G128: base byte b (0..23) = sum_{i<5} c[5b+i] * 3^i, high byte h
+ *     (0..1) = sum_{i<4} c[120+4h+i] * 3^i (little-endian base-3 digits; the
+ *     pages fix 24 + 2 bytes per 128 weights but no digit order).
+ *   Pad weights (columns k..k_pad-1) encode value 0.
+ * Errors: UNKNOWN_FORMAT, SHAPE, INVALID_ARGUMENT, SIZE_MISMATCH (payload_bytes
+ *   != geometry.payload_bytes), INVALID_CODE (a value outside {-1,0,+1}).
+ */
+int ninfer_ternary_pack(int fmt, uint64_t n, uint64_t k, const int8_t *values,
+                        const uint16_t *scales_f16, uint8_t *payload,
+                        uint64_t payload_bytes);
+
+/*
+ * ninfer_ternary_unpack -- exact inverse of ninfer_ternary_pack (host).
+ *   values: host int8[n * k] out; scales_f16: host uint16[n * groups_per_row] out.
+ * Errors: as pack, plus INVALID_CODE when a PQ2_0 field holds code 3 or a
+ *   PTQ1_0 base byte is >= 243 / high byte >= 81 (no ternary value packs to it).
+ */
+int ninfer_ternary_unpack(int fmt, uint64_t n, uint64_t k, const uint8_t *payload,
+                          uint64_t payload_bytes, int8_t *values,
+                          uint16_t *scales_f16);
+
+/*
+ * ninfer_blocks_to_planes / ninfer_planes_to_blocks -- [FMT] §3-§4: the ggml
+ * stream of single-group blocks (row-major, groups_per_row blocks per row)
+ * <-> the row-split payload. Block layouts: PQ2_0 34 bytes [scale 2][base 32];
+ * PTQ1_0 28 bytes [base 24][high 2][scale 2]. The two are exact inverses: bytes
+ * are moved, never changed. blocks_bytes must be n * groups_per_row * 34 (28).
+ * Host, synchronous. Errors: UNKNOWN_FORMAT, SHAPE, INVALID_ARGUMENT, SIZE_MISMATCH.
+ */
+int ninfer_blocks_to_planes(int fmt, uint64_t n, uint64_t k, const uint8_t *blocks,
+                            uint64_t blocks_bytes, uint8_t *payload,
+                            uint64_t payload_bytes);
+int ninfer_planes_to_blocks(int fmt, uint64_t n, uint64_t k, const uint8_t *payload,
+                            uint64_t payload_bytes, uint8_t *blocks,
+                            uint64_t blocks_bytes);
+
+/*
+ * ninfer_hadamard_fwd -- [V3] §8 hadamard_signs, [TS] §4.2 forward transform:
+ *   for every row m and 1024-block b: y_b = H (D_b * x_b) / sqrt(1024), with H
+ *   the unnormalised Sylvester Hadamard matrix in natural order
+ *   (H[i][j] = (-1)^popcount(i & j)) and D_b the block's slice of the sign vector.
+ * ninfer_hadamard_inv -- [TS] §4.2 inverse (embedding rows): y_b = D_b * (H x_b) / 32.
+ *   x: device, M x K row-major of x_dtype; y: device, M x K of y_dtype
+ *     (may alias x exactly for in-place use when the dtypes match).
+ *   signs_bf16: device bfloat16[K], each +1 or -1 (other values give
+ *     unspecified results; they are not checked on the device).
+ *   K must be a multiple of 1024 ([V3] §8: "K ... is a multiple of 1024").
+ *   Computed in fp32; y rounded to y_dtype.
+ * Errors: INVALID_ARGUMENT, SHAPE (K % 1024 != 0), ALIGNMENT, CUDA.
+ */
+int ninfer_hadamard_fwd(const void *x, int x_dtype, void *y, int y_dtype,
+                        const uint16_t *signs_bf16, uint64_t M, uint64_t K,
+                        ninfer_stream stream);
+int ninfer_hadamard_inv(const void *x, int x_dtype, void *y, int y_dtype,
+                        const uint16_t *signs_bf16, uint64_t M, uint64_t K,
+                        ninfer_stream stream);
+
+/*
+ * ninfer_ternary_matmul_workspace -- bytes of device workspace that
+ * ninfer_ternary_matmul needs for this problem (0 when none). Host only.
+ */
+int ninfer_ternary_matmul_workspace(int fmt, uint64_t n, uint64_t k, uint64_t M,
+                                    int rotate, uint64_t *bytes);
+
+/*
+ * ninfer_ternary_matmul -- the rotated ternary projection:
+ *   y[m][r] = sum_c W[r][c] * xr[m][c],   W[r][c] = value(code[r][c]) * scale[r][c/128],
+ *   xr = forward transform of x (as ninfer_hadamard_fwd) when signs_bf16 != NULL,
+ *   xr = x when signs_bf16 == NULL (unrotated use).
+ * ([V3] §8: the matrix multiplies hadamard_transform(input, signs) instead of
+ * the raw input; [TS] §4.4: forward transform before every low-bit projection
+ * and before the output head; value mapping as ninfer_ternary_pack.)
+ *   payload: device, the row-split payload of an n x k matrix, exactly
+ *     payload_bytes == geometry.payload_bytes, 256-byte aligned.
+ *   x: device M x k row-major of x_dtype (f32, bf16 or f16), 16-byte aligned,
+ *     row stride k elements.
+ *   signs_bf16: device bfloat16[k] (+-1) or NULL; non-NULL requires k % 1024 == 0.
+ *   y: device M x n row-major of y_dtype (f32 or bf16).
+ *   workspace: device scratch of at least ninfer_ternary_matmul_workspace()
+ *     bytes (NULL allowed when that is 0); its contents are not preserved.
+ *   M >= 1. Decode shapes (M <= 8) run the fused rotate + decode + GEMV
+ *   kernels; larger M run the prefill path.
+ * Arithmetic: transform in fp32; the rotated activations enter the contraction
+ * as a three-term e4m3 expansion per 1024-block (relative error <= 2^-12 per
+ * element before accumulation); ternary x activation products are exact and
+ * accumulate in fp32. Max relative error vs exact (infinity norm over y) is
+ * well under 1e-3 for the decode path.
+ * Errors: INVALID_ARGUMENT, UNKNOWN_FORMAT, SHAPE, SIZE_MISMATCH, ALIGNMENT, CUDA.
+ */
+int ninfer_ternary_matmul(int fmt, const uint8_t *payload, uint64_t payload_bytes,
+                          uint64_t n, uint64_t k, const void *x, int x_dtype,
+                          const uint16_t *signs_bf16, void *y, int y_dtype,
+                          uint64_t M, void *workspace, uint64_t workspace_bytes,
+                          ninfer_stream stream);
+
+/*
+ * ninfer_ternary_embed -- embedding rows ([TS] §4.4: token id -> low-bit
+ * embedding row -> inverse signed Hadamard transform; [V3] §7.3: a row range of
+ * a row-split matrix spans intervals of the base, high and scale planes):
+ *   out[i][c] = inverse transform of (W[ids[i]][:]) , i < count.
+ *   payload: device row-split payload of the n x k embedding matrix.
+ *   ids: device int32[count]; an id outside [0, n) writes a zero row and sets
+ *     bit 0 of *status_dev (if status_dev != NULL; never cleared by the library).
+ *   signs_bf16: device bfloat16[k] (+-1), k % 1024 == 0; NULL skips the transform.
+ *   out: device count x k of out_dtype (f32 or bf16).
+ * Errors: INVALID_ARGUMENT, UNKNOWN_FORMAT, SHAPE, SIZE_MISMATCH, ALIGNMENT, CUDA.
+ */
+int ninfer_ternary_embed(int fmt, const uint8_t *payload, uint64_t payload_bytes,
+                         uint64_t n, uint64_t k, const int32_t *ids, uint64_t count,
+                         const uint16_t *signs_bf16, void *out, int out_dtype,
+                         int32_t *status_dev, ninfer_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NINFER_TERNARY_H */

@@ -1,0 +1,189 @@
+"""CUDA path vs the CPU oracle, element by element, through the C ABI.
+
+Small shapes span several tiles and ragged tails and compare every output;
+the full-size workloads compare all outputs where the oracle finishes in
+seconds and sampled rows otherwise. Tolerance (infinity-norm relative error,
+max|y - y_ref| / max|y_ref|): 1e-3 for the decode projection, the transform
+and the embedding; 2e-2 for the 16-bit tensor-core prefill path.
+"""
+import numpy as np
+import pytest
+import torch
+
+import bit_gemv_gb300 as nt
+import oracle
+import synth
+from gpu_util import DEV, dev_signs, dev_u8, dev_x, oracle_matmul_rows, run_matmul, signs_values
+
+pytestmark = pytest.mark.gpu
+
+TOL_DECODE = 1e-3
+TOL_PREFILL = 2e-2
+
+
+# ---------------------------------------------------------------- transform ---
+@pytest.mark.parametrize("x_dtype", [torch.float32, torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("y_dtype", [torch.float32, torch.bfloat16])
+def test_hadamard_forward_inverse(x_dtype, y_dtype):
+    rng = np.random.default_rng(10)
+    M, K = 5, 3072
+    x = torch.from_numpy(rng.standard_normal((M, K)).astype(np.float32)).to(DEV).to(x_dtype)
+    sbits = synth.sign_vector(rng, K)
+    s = dev_signs(sbits)
+    D = synth.bf16_bits_to_f32(sbits)
+    xv = x.float().cpu().numpy().astype(np.float64)
+    fw = nt.ninfer_hadamard_fwd(x, s, out_dtype=y_dtype)
+    iv = nt.ninfer_hadamard_inv(x, s, out_dtype=y_dtype)
+    torch.cuda.synchronize()
+    tol = 1e-5 if y_dtype == torch.float32 else 4e-3
+    assert oracle.max_rel_error(fw.float().cpu().numpy(), oracle.hadamard_forward(xv, D)) <= tol
+    assert oracle.max_rel_error(iv.float().cpu().numpy(), oracle.hadamard_inverse(xv, D)) <= tol
+
+
+def test_hadamard_in_place_and_roundtrip():
+    rng = np.random.default_rng(11)
+    M, K = 3, 17408
+    x0 = rng.standard_normal((M, K)).astype(np.float32)
+    sbits = synth.sign_vector(rng, K)
+    s = dev_signs(sbits)
+    x = torch.from_numpy(x0).to(DEV)
+    nt.ninfer_hadamard_fwd(x, s, out=x)            # in place
+    ref = oracle.hadamard_forward(x0, synth.bf16_bits_to_f32(sbits))
+    assert oracle.max_rel_error(x.cpu().numpy(), ref) <= 1e-5
+    nt.ninfer_hadamard_inv(x, s, out=x)
+    assert oracle.max_rel_error(x.cpu().numpy(), x0) <= 1e-5
+
+
+# ------------------------------------------------------------------ matmul ---
+def test_matmul_tiny_workload():
+    c = synth.make_case("tiny")
+    y = run_matmul("PQ2_0_G128", c)
+    ref = oracle_matmul_rows("PQ2_0_G128", c, np.arange(c.workload.n))
+    assert oracle.max_rel_error(y, ref) <= TOL_DECODE
+
+
+@pytest.mark.parametrize("fmt", ["PQ2_0_G128", "PTQ1_0_G128"])
+@pytest.mark.parametrize("n,k,M", [(300, 2048, 1), (300, 2048, 8), (77, 3072, 3), (1, 1024, 1), (17, 5120, 2),
+                                   (1000, 1024, 5)])
+def test_matmul_small_shapes(fmt, n, k, M):
+    c = synth.make_case("gateup", n=n, k=k, M=M, seed=n * 7 + k + M)
+    y = run_matmul(fmt, c)
+    ref = oracle_matmul_rows(fmt, c, np.arange(n))
+    assert oracle.max_rel_error(y, ref) <= TOL_DECODE
+
+
+@pytest.mark.parametrize("fmt", ["PQ2_0_G128", "PTQ1_0_G128"])
+def test_matmul_unrotated_padded_k(fmt):
+    """No hadamard_signs (raw input) and k % 128 != 0: the pad columns of the
+    last group must not contribute."""
+    c = synth.make_case("gateup", n=129, k=300, M=2, seed=5)
+    y = run_matmul(fmt, c, rotate=False)
+    ref = oracle_matmul_rows(fmt, c, np.arange(129), rotate=False)
+    assert oracle.max_rel_error(y, ref) <= TOL_DECODE
+
+
+def test_matmul_bf16_output():
+    c = synth.make_case("gateup", n=512, k=5120, M=1, seed=9)
+    y = run_matmul("PQ2_0_G128", c, y_dtype=torch.bfloat16)
+    ref = oracle_matmul_rows("PQ2_0_G128", c, np.arange(512))
+    assert oracle.max_rel_error(y, ref) <= 4e-3       # bf16 output rounding
+
+
+@pytest.mark.slow
+def test_matmul_gateup_full():
+    c = synth.make_case("gateup")
+    y = run_matmul("PQ2_0_G128", c)
+    ref = oracle_matmul_rows("PQ2_0_G128", c, np.arange(c.workload.n))
+    assert oracle.max_rel_error(y, ref) <= TOL_DECODE
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("M", [1, 8])
+def test_matmul_down_full(M):
+    c = synth.make_case("down", M=M)
+    y = run_matmul("PTQ1_0_G128", c)
+    ref = oracle_matmul_rows("PTQ1_0_G128", c, np.arange(c.workload.n))
+    assert oracle.max_rel_error(y, ref) <= TOL_DECODE
+
+
+@pytest.fixture(scope="module")
+def head_case():
+    c = synth.make_case("head", M=8, with_ids=True)
+    payload = dev_u8(nt.ninfer_ternary_pack("PQ2_0_G128", c.values, c.scales))
+    return c, payload
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("M", [1, 8])
+def test_matmul_head_sampled(head_case, M):
+    c, payload = head_case
+    sub = synth.Case(c.workload, c.values, c.scales, c.signs, c.x[:M], c.x_raw[:M])
+    y = run_matmul("PQ2_0_G128", sub, payload_dev=payload)
+    rng = np.random.default_rng(123)
+    rows = np.unique(np.concatenate([[0, 1, c.workload.n - 1], rng.integers(0, c.workload.n, 3000)]))
+    ref = oracle_matmul_rows("PQ2_0_G128", sub, rows)
+    assert oracle.max_rel_error(y[:, rows], ref) <= TOL_DECODE
+    assert np.all(np.isfinite(y))
+
+
+@pytest.mark.slow
+def test_embed_head_rows(head_case):
+    c, payload = head_case
+    n, k = c.values.shape
+    ids = torch.from_numpy(c.ids).to(DEV)
+    out = nt.ninfer_ternary_embed("PQ2_0_G128", payload, n, k, ids, dev_signs(c.signs))
+    torch.cuda.synchronize()
+    sub = oracle.pack_planes("PQ2_0_G128", c.values[c.ids], c.scales[c.ids])
+    ref = oracle.embed_rows("PQ2_0_G128", sub, c.ids.size, k, np.arange(c.ids.size), signs_values(c))
+    assert oracle.max_rel_error(out.cpu().numpy(), ref) <= TOL_DECODE
+
+
+@pytest.mark.slow
+def test_matmul_prefill_sampled():
+    c = synth.make_case("prefill")
+    y = run_matmul("PQ2_0_G128", c)
+    rng = np.random.default_rng(7)
+    rows = np.unique(np.concatenate([[0, c.workload.n - 1], rng.integers(0, c.workload.n, 256)]))
+    ref = oracle_matmul_rows("PQ2_0_G128", c, rows)
+    assert oracle.max_rel_error(y[:, rows], ref) <= TOL_PREFILL
+
+
+# --------------------------------------------------------------- embedding ---
+@pytest.mark.parametrize("fmt", ["PQ2_0_G128", "PTQ1_0_G128"])
+def test_embed_small(fmt):
+    c = synth.make_case("gateup", n=500, k=3072, M=1, seed=21)
+    payload = dev_u8(nt.ninfer_ternary_pack(fmt, c.values, c.scales))
+    ids_np = np.array([0, 499, 7, 7, 250], np.int32)
+    out = nt.ninfer_ternary_embed(fmt, payload, 500, 3072, torch.from_numpy(ids_np).to(DEV), dev_signs(c.signs))
+    torch.cuda.synchronize()
+    ref = oracle.embed_rows(fmt, oracle.pack_planes(fmt, c.values, c.scales), 500, 3072, ids_np, signs_values(c))
+    assert oracle.max_rel_error(out.cpu().numpy(), ref) <= TOL_DECODE
+
+
+def test_embed_out_of_range_ids_flagged():
+    c = synth.make_case("gateup", n=64, k=1024, M=1, seed=22)
+    payload = dev_u8(nt.ninfer_ternary_pack("PQ2_0_G128", c.values, c.scales))
+    ids = torch.tensor([3, -1, 64, 5], dtype=torch.int32, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = nt.ninfer_ternary_embed("PQ2_0_G128", payload, 64, 1024, ids, dev_signs(c.signs), status=status)
+    torch.cuda.synchronize()
+    o = out.cpu().numpy()
+    assert status.item() == 1
+    assert np.all(o[1] == 0) and np.all(o[2] == 0)
+    ref = oracle.embed_rows("PQ2_0_G128", oracle.pack_planes("PQ2_0_G128", c.values, c.scales), 64, 1024, [3, 5],
+                            signs_values(c))
+    assert oracle.max_rel_error(o[[0, 3]], ref) <= TOL_DECODE
+    status.zero_()
+    nt.ninfer_ternary_embed("PQ2_0_G128", payload, 64, 1024, ids[[0, 3]].contiguous(), dev_signs(c.signs), status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+
+
+def test_embed_unrotated():
+    c = synth.make_case("gateup", n=40, k=300, M=1, seed=23)
+    payload = dev_u8(nt.ninfer_ternary_pack("PTQ1_0_G128", c.values, c.scales))
+    ids = torch.tensor([1, 39], dtype=torch.int32, device=DEV)
+    out = nt.ninfer_ternary_embed("PTQ1_0_G128", payload, 40, 300, ids)
+    torch.cuda.synchronize()
+    W = oracle.dequantize("PTQ1_0_G128", oracle.pack_planes("PTQ1_0_G128", c.values, c.scales), 40, 300, [1, 39])
+    assert np.array_equal(out.cpu().numpy().astype(np.float64), W)
