@@ -80,9 +80,8 @@ def sources_sha256(files) -> str:
     return d.hexdigest()
 
 
-GEMV_SOURCES = ["bit_gemv_gb300/csrc/gemm_simple.cu", "bit_gemv_gb300/csrc/hadamard.cu",
-                "bit_gemv_gb300/csrc/matmul.cu", "bit_gemv_gb300/csrc/device.cuh",
-                "bit_gemv_gb300/csrc/plane.cuh"]
+GEMV_SOURCES = ["bit_gemv_gb300/csrc/gemv_pq2.cu", "bit_gemv_gb300/csrc/async.cuh",
+                "bit_gemv_gb300/csrc/device.cuh", "bit_gemv_gb300/csrc/gemv.h"]
 KERNEL_TAG = "gemv"
 
 
@@ -255,7 +254,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f32",
+        "dtype": "e4m3x3*ternary->f32",
         "data": "synthetic",
         "config": {"workload": args.workload, "format": w.fmt, "n": n, "k": k, "M": M, "x_dtype": w.x_dtype,
                    "seed": w.seed, "rotate": True,
@@ -276,7 +275,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
 
 
 def kernels_per_step() -> int:
-    return 2          # forward transform + tiled GEMV
+    return 1          # one fused rotate + decode + GEMV kernel
 
 
 # ------------------------------------------------------------ CPU oracle ---

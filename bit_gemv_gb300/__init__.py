@@ -61,6 +61,8 @@ _sig = {
     "ninfer_ternary_matmul_workspace": (_int, [_int, _u64, _u64, _u64, _int, C.POINTER(_u64)]),
     "ninfer_ternary_matmul": (_int, [_int, _vp, _u64, _u64, _u64, _vp, _int, _vp, _vp, _int, _u64, _vp, _u64, _vp]),
     "ninfer_ternary_embed": (_int, [_int, _vp, _u64, _u64, _u64, _vp, _u64, _vp, _vp, _int, _vp, _vp]),
+    "ninfer_device_errors": (_int, [C.POINTER(C.c_uint32), _int]),
+    "ninfer_set_prefetch_before_dependency": (_int, [_int]),
 }
 for _name, (_res, _args) in _sig.items():
     _f = getattr(_lib, _name)
@@ -130,6 +132,16 @@ def ninfer_planes_to_blocks(fmt, n: int, k: int, payload: np.ndarray) -> np.ndar
     out = np.empty(n * g.groups_per_row * nb, dtype=np.uint8)
     _check(_lib.ninfer_planes_to_blocks(_fmt(fmt), n, k, _np_ptr(payload), payload.size, _np_ptr(out), out.size))
     return out
+
+
+def ninfer_device_errors(clear: bool = True) -> int:
+    v = C.c_uint32()
+    _check(_lib.ninfer_device_errors(C.byref(v), int(bool(clear))))
+    return v.value
+
+
+def ninfer_set_prefetch_before_dependency(enable: bool) -> None:
+    _check(_lib.ninfer_set_prefetch_before_dependency(int(bool(enable))))
 
 
 # ---------------------------------------------------------------- device ---

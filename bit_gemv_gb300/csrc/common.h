@@ -2,6 +2,7 @@
 // handling, overflow-checked size arithmetic and the plane geometry.
 #pragma once
 
+#include <algorithm>
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>

@@ -3,17 +3,67 @@
 
 #include "common.h"
 #include "device.cuh"
+#include "gemv.h"
 #include "plane.cuh"
 
 namespace ninfer {
 int gemm_simple_launch(const PlaneView &p, uint64_t n, uint64_t k, const void *a, int a_dtype, uint64_t M, void *y,
                        int y_dtype, cudaStream_t stream);
+
+int device_info(DeviceInfo *out) {
+    static DeviceInfo cache[64];
+    static bool have[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(NINFER_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev >= 0 && dev < 64 && have[dev]) {
+        *out = cache[dev];
+        return NINFER_OK;
+    }
+    DeviceInfo d{};
+    e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess) return fail(NINFER_ERR_CUDA, "device attributes: %s", cudaGetErrorString(e));
+    if (dev >= 0 && dev < 64) {
+        cache[dev] = d;
+        have[dev] = true;
+    }
+    *out = d;
+    return NINFER_OK;
 }
+
+static bool g_pdl = true;
+}  // namespace ninfer
 
 using namespace ninfer;
 
-static uint64_t workspace_bytes_for(uint64_t M, uint64_t k, bool rotate) {
-    return rotate ? M * k * sizeof(float) : 0;   // rotated activations, fp32
+namespace {
+enum class Path { kFusedPq2, kTiled };
+
+struct MatmulPlan {
+    Path path;
+    GemvPlan gemv;
+    uint64_t workspace;
+};
+
+int plan_matmul(int fmt, const ninfer_row_split_geometry &g, uint64_t M, bool rotate, MatmulPlan *mp) {
+    DeviceInfo d;
+    int st = device_info(&d);
+    if (st) return st;
+    mp->workspace = 0;
+    if (fmt == NINFER_PQ2_0_G128 && gemv_pq2_plan(g, M, rotate, d.sms, d.smem_optin, &mp->gemv)) {
+        mp->path = Path::kFusedPq2;
+        return NINFER_OK;
+    }
+    mp->path = Path::kTiled;
+    mp->workspace = rotate ? M * g.k * sizeof(float) : 0;   // rotated activations, fp32
+    return NINFER_OK;
+}
+}  // namespace
+
+extern "C" int ninfer_set_prefetch_before_dependency(int enable) {
+    g_pdl = enable != 0;
+    return NINFER_OK;
 }
 
 extern "C" int ninfer_ternary_matmul_workspace(int fmt, uint64_t n, uint64_t k, uint64_t M, int rotate,
@@ -25,7 +75,10 @@ extern "C" int ninfer_ternary_matmul_workspace(int fmt, uint64_t n, uint64_t k, 
     if (M == 0) return fail(NINFER_ERR_SHAPE, "workspace: M must be positive");
     uint64_t mk;
     if (!mul_ok(M, k, &mk) || mk > (UINT64_MAX / 8)) return fail(NINFER_ERR_OVERFLOW, "workspace size overflows");
-    *bytes = workspace_bytes_for(M, k, rotate != 0);
+    MatmulPlan mp;
+    st = plan_matmul(fmt, g, M, rotate != 0, &mp);
+    if (st) return st;
+    *bytes = mp.workspace;
     return NINFER_OK;
 }
 
@@ -50,12 +103,17 @@ extern "C" int ninfer_ternary_matmul(int fmt, const uint8_t *payload, uint64_t p
         return fail(NINFER_ERR_SHAPE, "matmul: k=%llu is not a multiple of 1024; the rotated input needs whole blocks",
                     (unsigned long long)k);
     if (rotate && !aligned(signs_bf16, 16)) return fail(NINFER_ERR_ALIGNMENT, "matmul: signs must be 16-byte aligned");
-    const uint64_t need = workspace_bytes_for(M, k, rotate);
+    MatmulPlan mp;
+    st = plan_matmul(fmt, g, M, rotate, &mp);
+    if (st) return st;
+    const uint64_t need = mp.workspace;
     if (need && (!workspace || workspace_bytes < need))
         return fail(NINFER_ERR_SIZE_MISMATCH, "matmul: workspace of %llu bytes needed, %llu given",
                     (unsigned long long)need, (unsigned long long)workspace_bytes);
     if (need && !aligned(workspace, 16)) return fail(NINFER_ERR_ALIGNMENT, "matmul: workspace must be 16-byte aligned");
     cudaStream_t s = (cudaStream_t)stream;
+    if (mp.path == Path::kFusedPq2)
+        return gemv_pq2_launch(mp.gemv, payload, g, x, x_dtype, signs_bf16, y, y_dtype, M, s, g_pdl);
     const PlaneView p = make_view(payload, g, fmt);
     const void *a = x;
     int a_dtype = x_dtype;

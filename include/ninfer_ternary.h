@@ -235,6 +235,27 @@ int ninfer_ternary_embed(int fmt, const uint8_t *payload, uint64_t payload_bytes
                          const uint16_t *signs_bf16, void *out, int out_dtype,
                          int32_t *status_dev, ninfer_stream stream);
 
+/*
+ * ninfer_device_errors -- reads the library's device error word on the current
+ * device into *out and clears it when clear != 0. Bit 0 (value 1): a kernel
+ * gave up waiting for its own asynchronous weight copies (a bounded wait of
+ * about two seconds ran out); that call's output is incomplete. Kernels never
+ * trap; this word is how such a failure is reported. Host, synchronous.
+ * Errors: INVALID_ARGUMENT (out NULL), CUDA.
+ */
+int ninfer_device_errors(uint32_t *out, int clear);
+
+/*
+ * ninfer_set_prefetch_before_dependency -- process-wide switch, default 1.
+ * With 1, decode projections (ninfer_ternary_matmul with M <= 8) are launched
+ * with programmatic dependent launch: they begin streaming the weight payload
+ * while the preceding work on the stream is still finishing, and touch the
+ * activations, signs and output only after it has completed. Set 0 when the
+ * work immediately preceding a call writes that call's weight payload.
+ * Always returns NINFER_OK.
+ */
+int ninfer_set_prefetch_before_dependency(int enable);
+
 #ifdef __cplusplus
 }
 #endif

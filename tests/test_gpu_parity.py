@@ -187,3 +187,8 @@ def test_embed_unrotated():
     torch.cuda.synchronize()
     W = oracle.dequantize("PTQ1_0_G128", oracle.pack_planes("PTQ1_0_G128", c.values, c.scales), 40, 300, [1, 39])
     assert np.array_equal(out.cpu().numpy().astype(np.float64), W)
+
+
+def test_no_device_errors_after_suite():
+    torch.cuda.synchronize()
+    assert nt.ninfer_device_errors(clear=True) == 0
