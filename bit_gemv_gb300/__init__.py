@@ -63,7 +63,9 @@ _sig = {
     "ninfer_ternary_embed": (_int, [_int, _vp, _u64, _u64, _u64, _vp, _u64, _vp, _vp, _int, _vp, _vp]),
     "ninfer_device_errors": (_int, [C.POINTER(C.c_uint32), _int]),
     "ninfer_set_prefetch_before_dependency": (_int, [_int]),
+    "ninfer_ternary_matmul_noalloc": (_int, [_int, _vp, _u64, _u64, _u64, _vp, _int, _vp, _vp, _int, _u64, _vp]),
 }
+NOALLOC_SCRATCH_BYTES = 4 * 1024 * 1024
 for _name, (_res, _args) in _sig.items():
     _f = getattr(_lib, _name)
     _f.restype = _res
@@ -208,6 +210,20 @@ def ninfer_ternary_matmul(fmt, payload, n: int, k: int, x, signs=None, y=None, y
         _fmt(fmt), _dev(payload, "payload"), payload.numel(), n, k, _dev(x2, "x"), _dt(x2.dtype),
         _dev(signs, "signs") if signs is not None else None, _dev(y, "y"), _dt(y.dtype), M,
         ws_ptr, ws_bytes, _stream(x)))
+    return y
+
+
+def ninfer_ternary_matmul_noalloc(fmt, payload, n: int, k: int, x, signs=None, y=None, y_dtype=None):
+    """As ninfer_ternary_matmul, for callers that cannot allocate device memory:
+    the workspace comes from the library's fixed device array."""
+    torch = _torch()
+    x2 = x.reshape(-1, k)
+    M = x2.shape[0]
+    if y is None:
+        y = torch.empty((M, n), dtype=y_dtype or torch.float32, device=x.device)
+    _check(_lib.ninfer_ternary_matmul_noalloc(
+        _fmt(fmt), _dev(payload, "payload"), payload.numel(), n, k, _dev(x2, "x"), _dt(x2.dtype),
+        _dev(signs, "signs") if signs is not None else None, _dev(y, "y"), _dt(y.dtype), M, _stream(x)))
     return y
 
 

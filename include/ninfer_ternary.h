@@ -256,6 +256,41 @@ int ninfer_device_errors(uint32_t *out, int clear);
  */
 int ninfer_set_prefetch_before_dependency(int enable);
 
+/*
+ * ninfer_ternary_matmul_noalloc -- ninfer_ternary_matmul for callers that
+ * cannot allocate device memory. No counterpart on the source pages: it is a
+ * convenience of this library.
+ *
+ * Who needs it: code that may not call cudaMalloc or any allocator around the
+ * projection -- for instance a plug-in whose host hands it only the input and
+ * output buffers, or a runtime with no device allocator of its own. Such a
+ * caller cannot provide the workspace ninfer_ternary_matmul asks for on the
+ * paths that stage rotated activations.
+ *
+ * What it does: exactly ninfer_ternary_matmul (same arguments minus the
+ * workspace, same results), with the workspace taken from a fixed array of
+ * NINFER_NOALLOC_SCRATCH_BYTES bytes that the library keeps in device memory.
+ * Every GPU that loads the library holds that array until the process exits.
+ * The call itself allocates nothing.
+ *   - Limit: a problem whose ninfer_ternary_matmul_workspace() exceeds
+ *     NINFER_NOALLOC_SCRATCH_BYTES is rejected with NINFER_ERR_SIZE_MISMATCH
+ *     (use ninfer_ternary_matmul with your own workspace instead).
+ *   - Set-up: the first call on a device (with that device current) looks up
+ *     the array's device address once; make that first call before any stream
+ *     capture.
+ *   - Sharing: all calls on a device share the one array and it keeps the last
+ *     call's contents (every call overwrites what it reads, so no clearing is
+ *     needed). Calls that may overlap on the GPU -- on different streams, or
+ *     from different host threads without ordering -- race on the array; order
+ *     them on one stream.
+ * Errors: as ninfer_ternary_matmul, plus SIZE_MISMATCH for the limit above.
+ */
+#define NINFER_NOALLOC_SCRATCH_BYTES (4u * 1024u * 1024u)
+int ninfer_ternary_matmul_noalloc(int fmt, const uint8_t *payload, uint64_t payload_bytes,
+                                  uint64_t n, uint64_t k, const void *x, int x_dtype,
+                                  const uint16_t *signs_bf16, void *y, int y_dtype,
+                                  uint64_t M, ninfer_stream stream);
+
 #ifdef __cplusplus
 }
 #endif
