@@ -80,7 +80,8 @@ def sources_sha256(files) -> str:
     return d.hexdigest()
 
 
-GEMV_SOURCES = ["bit_gemv_gb300/csrc/gemv_pq2.cu", "bit_gemv_gb300/csrc/async.cuh",
+GEMV_SOURCES = ["bit_gemv_gb300/csrc/gemv_pq2_int.cu", "bit_gemv_gb300/csrc/act_prep.cu",
+                "bit_gemv_gb300/csrc/gemv_common.cu", "bit_gemv_gb300/csrc/async.cuh",
                 "bit_gemv_gb300/csrc/device.cuh", "bit_gemv_gb300/csrc/gemv.h"]
 KERNEL_TAG = "gemv"
 
@@ -254,7 +255,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "e4m3x3*ternary->f32",
+        "dtype": "int16*ternary->int32->f32",
         "data": "synthetic",
         "config": {"workload": args.workload, "format": w.fmt, "n": n, "k": k, "M": M, "x_dtype": w.x_dtype,
                    "seed": w.seed, "rotate": True,
@@ -275,7 +276,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
 
 
 def kernels_per_step() -> int:
-    return 1          # one fused rotate + decode + GEMV kernel
+    return 2          # activation rotate/quantise + decode GEMV
 
 
 # ------------------------------------------------------------ CPU oracle ---

@@ -1,0 +1,83 @@
+// Pieces shared by the fused decode kernels: the library's device error word
+// and tensor-map encoding for row-range views of a plane.
+#include <cstring>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "common.h"
+#include "gemv.h"
+
+namespace ninfer {
+
+// Error word shared by all kernels of the library (bit flags from async.cuh).
+__device__ uint32_t g_device_error = 0;
+
+int device_error_word(uint32_t **out) {
+    static uint32_t *cache[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(NINFER_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev >= 0 && dev < 64 && cache[dev]) {
+        *out = cache[dev];
+        return NINFER_OK;
+    }
+    void *ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_device_error);
+    if (e != cudaSuccess) return fail(NINFER_ERR_CUDA, "error word address: %s", cudaGetErrorString(e));
+    if (dev >= 0 && dev < 64) cache[dev] = static_cast<uint32_t *>(ptr);
+    *out = static_cast<uint32_t *>(ptr);
+    return NINFER_OK;
+}
+
+namespace {
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+int encode_fn(EncodeTiledFn *out) {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !ptr)
+            return fail(NINFER_ERR_CUDA, "cuTensorMapEncodeTiled unavailable (%s)", cudaGetErrorString(e));
+        fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    *out = fn;
+    return NINFER_OK;
+}
+}  // namespace
+
+int encode_rows(CUtensorMap *map, const uint8_t *addr, uint64_t row_bytes, uint64_t rows, uint64_t ctas,
+                uint32_t box_bytes, uint32_t box_rows, bool swizzle128) {
+    EncodeTiledFn fn;
+    int st = encode_fn(&fn);
+    if (st) return st;
+    std::memset(map, 0, sizeof *map);
+    const cuuint32_t rank = ctas > 1 ? 3 : 2;
+    const cuuint64_t dims[3] = {row_bytes, rows, ctas};
+    const cuuint64_t strides[2] = {row_bytes, row_bytes * rows};
+    const cuuint32_t box[3] = {box_bytes, box_rows, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, rank, const_cast<uint8_t *>(addr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(NINFER_ERR_CUDA, "tensor map encode failed (CUresult %d)", (int)r);
+    return NINFER_OK;
+}
+
+}  // namespace ninfer
+
+extern "C" int ninfer_device_errors(uint32_t *out, int clear) {
+    if (!out) return ninfer::fail(NINFER_ERR_INVALID_ARGUMENT, "device_errors: NULL output");
+    cudaError_t e = cudaMemcpyFromSymbol(out, ninfer::g_device_error, sizeof(uint32_t));
+    if (e != cudaSuccess) return ninfer::fail(NINFER_ERR_CUDA, "device_errors: %s", cudaGetErrorString(e));
+    if (clear) {
+        const uint32_t zero = 0;
+        e = cudaMemcpyToSymbol(ninfer::g_device_error, &zero, sizeof(uint32_t));
+        if (e != cudaSuccess) return ninfer::fail(NINFER_ERR_CUDA, "device_errors: %s", cudaGetErrorString(e));
+    }
+    return NINFER_OK;
+}

@@ -1,4 +1,4 @@
-// Fused rotate + decode + GEMV for PQ2_0_G128 weights, M <= 8 activation rows.
+// Fused rotate + decode + GEMV for PQ2_0_G128 weights, 2 <= M <= 8 activation rows.
 //
 // What it computes (the decode projection):
 //   y[m][r] = sum_g scale[r][g] * sum_{j<128} (code[r][128g+j] - 1) * xr[m][128g+j],
@@ -26,9 +26,9 @@
 //  * The e4m3 tensor core sums sum_j c_j * t_q(xr_j) exactly into fp32; per
 //    group, y += scale * (F * P - O) with F = 2^(9-E-4q) and O the group's
 //    sum of B terms (the "-1" of the offset code), still fp32.
-// The integer pipe (LOP3, 64 lanes/clk/SM on GB300) would cap a one-op-per-
-// weight CUDA-core decode below the HBM rate; four weights per LOP3 keeps the
-// kernel bandwidth-bound.
+// One activation row runs on the integer pipes instead (gemv_pq2_int.cu); with
+// several rows one decoded A fragment serves all of them, which the integer
+// path cannot share.
 #include <cstring>
 
 #include <cuda.h>
@@ -41,26 +41,6 @@
 #include "gemv.h"
 
 namespace ninfer {
-
-// Error word shared by all kernels of the library (bit flags from async.cuh).
-__device__ uint32_t g_device_error = 0;
-
-int device_error_word(uint32_t **out) {
-    static uint32_t *cache[64];
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return fail(NINFER_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
-    if (dev >= 0 && dev < 64 && cache[dev]) {
-        *out = cache[dev];
-        return NINFER_OK;
-    }
-    void *ptr = nullptr;
-    e = cudaGetSymbolAddress(&ptr, g_device_error);
-    if (e != cudaSuccess) return fail(NINFER_ERR_CUDA, "error word address: %s", cudaGetErrorString(e));
-    if (dev >= 0 && dev < 64) cache[dev] = static_cast<uint32_t *>(ptr);
-    *out = static_cast<uint32_t *>(ptr);
-    return NINFER_OK;
-}
 
 namespace {
 
@@ -456,208 +436,12 @@ __global__ void __launch_bounds__(NT == 1 ? 512 : 256, 1) gemv_pq2_kernel(const 
     }
 }
 
-// ---------------------------------------------------------------------------
-// M = 1: integer dot products on the CUDA cores.
-//
-// The rotated activation of each 1024-block becomes 16-bit fixed point,
-// x16 = rint(xr * 2^E) with E chosen per block so max |x16| is in
-// [2^14, 2^15): 15 significant bits relative to the block's largest element.
-// For a 16-weight word of a row, masking with 0x03 << 2p per byte leaves the
-// four codes of position p as bytes (scaled by 4^p); dp2a multiplies two of
-// them by two int16 activations and accumulates exactly in int32. Per group:
-//   sum_j c_j x16_j = acc0 + acc1/4 + acc2/16 + acc3/64   (exact shifts)
-//   y += scale * 2^-E * (that - sum_j x16_j)               (value = code - 1)
-// One lane owns one row of the 32-row tile; the four warps of a slot split
-// the groups in quarters.
-// ---------------------------------------------------------------------------
-struct ActM1 {
-    uint32_t off_act;   // [word][8 u32]: lo_p = (x[16w+p], x[16w+4+p]), hi_p = (x[16w+8+p], x[16w+12+p])
-    uint32_t off_gs;    // [group] {float 2^-E, int sum x16}
-};
-
-__device__ __forceinline__ int dp2a_lo(uint32_t a, uint32_t b, int c) {
-    int d;
-    asm("dp2a.lo.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-    return d;
-}
-__device__ __forceinline__ int dp2a_hi(uint32_t a, uint32_t b, int c) {
-    int d;
-    asm("dp2a.hi.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-    return d;
-}
-
-// Rotate block b of the (single) activation row into 16-bit fixed point.
-__device__ __forceinline__ void prep_block_m1(const Params &p, uint8_t *smem, const ActM1 &L, uint32_t b, int lane) {
-    float v[32];    // v[8*i + e] = element 256*i + 8*lane + e of the block
-    const bool full = (b + 1) * 1024 <= p.k;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const uint32_t c = b * 1024 + 256 * i + 8 * lane;
-        float t8[8];
-        if (full) {
-            load8(p.x, c, p.x_dtype, t8);
-        } else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) t8[e] = c + e < p.k ? load1(p.x, c + e, p.x_dtype) : 0.f;
-        }
-        if (p.signs) {
-            float d8[8];
-            load_signs8(p.signs, c, d8);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) t8[e] *= d8[e];
-        }
-#pragma unroll
-        for (int e = 0; e < 8; ++e) v[8 * i + e] = t8[e];
-    }
-    if (p.signs) {
-        wht1024_warp(v, lane);
-#pragma unroll
-        for (int r = 0; r < 32; ++r) v[r] *= 0.03125f;
-    }
-    float mx = 0.f;
-#pragma unroll
-    for (int r = 0; r < 32; ++r) mx = fmaxf(mx, fabsf(v[r]));
-#pragma unroll
-    for (int s = 16; s > 0; s >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, s));
-    int E = 0;
-    if (mx > 0.f) E = 14 - ilogbf(mx);     // mx * 2^E in [2^14, 2^15)
-    E = max(-100, min(100, E));
-    const float up = ldexpf(1.f, E);
-    int gsum[4];
-    uint32_t *act = reinterpret_cast<uint32_t *>(smem + L.off_act);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        int q[8];
-        int s = 0;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            q[e] = max(-32767, min(32767, __float2int_rn(v[8 * i + e] * up)));
-            s += q[e];
-        }
-        gsum[i] = s;
-        // this lane holds elements 8*lane .. +7 of row i, i.e. half (lane & 1)
-        // of 16-element word (b*64 + 16*i + lane/2)
-        const uint32_t word = b * 64 + 16 * i + (lane >> 1);
-        uint4 pk;
-        pk.x = (uint32_t)(q[0] & 0xffff) | ((uint32_t)q[4] << 16);
-        pk.y = (uint32_t)(q[1] & 0xffff) | ((uint32_t)q[5] << 16);
-        pk.z = (uint32_t)(q[2] & 0xffff) | ((uint32_t)q[6] << 16);
-        pk.w = (uint32_t)(q[3] & 0xffff) | ((uint32_t)q[7] << 16);
-        *reinterpret_cast<uint4 *>(act + word * 8 + (lane & 1) * 4) = pk;   // [lo_0..3 | hi_0..3]
-    }
-    // group sums: group (b*8 + 2*i + lane/16) gathers lanes 16*(lane/16) .. +15 of row i
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int s = 8; s > 0; s >>= 1) gsum[i] += __shfl_xor_sync(0xffffffffu, gsum[i], s);
-    if ((lane & 15) == 0) {
-        float2 *gs = reinterpret_cast<float2 *>(smem + L.off_gs);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t G = b * 8 + 2 * i + (lane >> 4);
-            if (G < p.groups) gs[G] = make_float2(ldexpf(1.f, -E), __int_as_float(gsum[i]));
-        }
-    }
-}
-
-__global__ void __launch_bounds__(512, 1) gemv_pq2_m1_kernel(const __grid_constant__ Params p) {
-    extern __shared__ __align__(1024) uint8_t smem[];
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int nwarps = blockDim.x >> 5;
-    const uint64_t r_begin = (uint64_t)blockIdx.x * p.rows_per_cta;
-    const uint64_t r_end = r_begin + p.rows_per_cta < p.n ? r_begin + p.rows_per_cta : p.n;
-    const bool last_cta = blockIdx.x == gridDim.x - 1;
-    const uint32_t ntile = (uint32_t)((r_end - r_begin + kTile - 1) / kTile);
-    const uint32_t bar0 = smem_u32(smem + p.off_bar);
-    const uint32_t slot = warp >> 2, quarter = warp & 3;
-    ActM1 L;
-    L.off_act = p.off_b;
-    L.off_gs = p.off_fo;
-    if (tid == 32) prefetch_tmap(last_cta ? &p.tmap_last : &p.tmap_main);
-    if (tid == 0) {
-        for (uint32_t s = 0; s < p.nslots; ++s) mbar_init(bar0 + 8 * s, 1);
-        fence_mbar_init();
-    }
-    __syncthreads();
-    if (quarter == 0 && slot < ntile) issue_tile(p, smem, r_begin, r_end, slot, slot, lane, last_cta);
-    pdl_launch_dependents();
-    {   // words of a partial last block read as zero activations
-        uint4 *z = reinterpret_cast<uint4 *>(smem + p.off_b);
-        const uint32_t nz = (p.off_red - p.off_b) / 16;
-        for (uint32_t i = tid; i < nz; i += blockDim.x) z[i] = make_uint4(0, 0, 0, 0);
-    }
-    pdl_wait();
-    __syncthreads();
-    const uint32_t nblk = (p.k + 1023) / 1024;
-    for (uint32_t b = warp; b < nblk; b += nwarps) prep_block_m1(p, smem, L, b, lane);
-    __syncthreads();
-
-    const uint32_t g_lo = quarter * p.groups / 4, g_hi = (quarter + 1) * p.groups / 4;
-    const uint32_t slot_addr = smem_u32(smem) + slot * p.slot_bytes;
-    const uint32_t act_addr = smem_u32(smem + L.off_act);
-    const float2 *gs = reinterpret_cast<const float2 *>(smem + L.off_gs);
-    float *red = reinterpret_cast<float *>(smem + p.off_red) + slot * (2 * 3 * kTile);
-    // lane = tile row; its 16-byte chunk c of box x sits at x*4096 + row*128 + ((c ^ row%8) * 16)
-    const uint32_t row_addr = slot_addr + lane * 128;
-    const uint32_t sw = lane & 7;
-    uint32_t phase = 0;
-    for (uint32_t tile = slot; tile < ntile; tile += p.nslots) {
-        const uint64_t row0 = r_begin + (uint64_t)tile * kTile;
-        const uint32_t nrows = r_end - row0 < (uint64_t)kTile ? (uint32_t)(r_end - row0) : (uint32_t)kTile;
-        const bool ready = mbar_wait(bar0 + 8 * slot, phase, p.err);
-        phase ^= 1;
-        const uint32_t s_delta = (uint32_t)(reinterpret_cast<uintptr_t>(p.scale + row0 * p.scale_row) & 15);
-        const uint32_t sc_addr = slot_addr + p.nbox * 4096u + s_delta + lane * p.scale_row;
-        float y = 0.f;
-        for (uint32_t G = g_lo; ready && G < g_hi; ++G) {
-            int acc0 = 0, acc1 = 0, acc2 = 0, acc3 = 0;
-#pragma unroll
-            for (int hc = 0; hc < 2; ++hc) {            // two 64-weight chunks per group
-                const uint32_t c16 = G * 2 + hc;         // 16-byte chunk index within the row
-                const uint4 wq = lds128u(row_addr + (c16 >> 3) * 4096u + (((c16 & 7) ^ sw) << 4));
-                const uint32_t wv[4] = {wq.x, wq.y, wq.z, wq.w};
-#pragma unroll
-                for (int wi = 0; wi < 4; ++wi) {
-                    const uint32_t word = G * 8 + hc * 4 + wi;
-                    const uint4 lo = lds128u(act_addr + word * 32);
-                    const uint4 hi = lds128u(act_addr + word * 32 + 16);
-                    const uint32_t c0 = wv[wi] & 0x03030303u, c1 = wv[wi] & 0x0C0C0C0Cu;
-                    const uint32_t c2 = wv[wi] & 0x30303030u, c3 = wv[wi] & 0xC0C0C0C0u;
-                    acc0 = dp2a_hi(hi.x, c0, dp2a_lo(lo.x, c0, acc0));
-                    acc1 = dp2a_hi(hi.y, c1, dp2a_lo(lo.y, c1, acc1));
-                    acc2 = dp2a_hi(hi.z, c2, dp2a_lo(lo.z, c2, acc2));
-                    acc3 = dp2a_hi(hi.w, c3, dp2a_lo(lo.w, c3, acc3));
-                }
-            }
-            const float2 f = gs[G];
-            const int tot = acc0 + (acc1 >> 2) + (acc2 >> 4) + (acc3 >> 6) - __float_as_int(f.y);
-            const float sc = __half2float(__ushort_as_half((unsigned short)lds16(sc_addr + 2 * G)));
-            y = fmaf(sc * f.x, (float)tot, y);
-        }
-        float *rbuf = red + ((tile / p.nslots) & 1) * (3 * kTile);
-        if (quarter) rbuf[(quarter - 1) * kTile + lane] = y;
-        named_barrier(1 + slot, 128);
-        if (!ready) {
-            mbar_wait(bar0 + 8 * slot, phase ^ 1, p.err);
-            return;
-        }
-        if (!quarter) {
-            if ((uint32_t)lane < nrows)
-                store1(p.y, row0 + lane, p.y_dtype, y + rbuf[lane] + rbuf[kTile + lane] + rbuf[2 * kTile + lane]);
-            if (tile + p.nslots < ntile) {
-                fence_proxy_async();
-                issue_tile(p, smem, r_begin, r_end, slot, tile + p.nslots, lane, last_cta);
-            }
-        }
-    }
-}
-
 }  // namespace
 
 bool gemv_pq2_plan(const ninfer_row_split_geometry &g, uint64_t M, bool rotate, int sms, int smem_limit,
                    GemvPlan *plan) {
     *plan = GemvPlan{};
-    if (M < 1 || M > 8) return false;
+    if (M < 2 || M > 8) return false;
     if (rotate && g.k % 1024) return false;
     if (g.payload_bytes % 16 || g.base_row_bytes % 16) return false;
     if (g.k > (1u << 24) || g.groups_per_row > (1u << 16) || g.n > (1ull << 31)) return false;
@@ -666,11 +450,8 @@ bool gemv_pq2_plan(const ninfer_row_split_geometry &g, uint64_t M, bool rotate, 
     const uint32_t nbox = (uint32_t)((g.base_row_bytes + 127) / 128);
     const uint32_t scale_area = ((kTile * (uint32_t)g.scale_row_bytes + 16 + 15) / 16) * 16;
     const uint32_t slot_bytes = ((nbox * 4096u + scale_area + 1023) / 1024) * 1024;
-    // M = 1: int16 activations [word][8 u32] + per-group {2^-E, sum}; else the
-    // e4m3 B fragments + per-group factors
-    const bool m1 = M == 1;
-    const uint32_t b_bytes = m1 ? groups * 8 * 32 : groups * NT * 1024;
-    const uint32_t fo_bytes = m1 ? groups * 8 : groups * NT * 64;
+    const uint32_t b_bytes = groups * NT * 1024;
+    const uint32_t fo_bytes = groups * NT * 64;
     const uint32_t red_bytes = kMaxSlots * 2 * 3 * kTile * (uint32_t)M * 4;
     const uint32_t bar_bytes = 64;
     // rows per CTA: ceil(n / grid) for all CTAs but the last
@@ -687,7 +468,7 @@ bool gemv_pq2_plan(const ninfer_row_split_geometry &g, uint64_t M, bool rotate, 
     plan->grid = (uint32_t)grid;
     plan->rows_per_cta = (uint32_t)R;
     plan->nbox = nbox;
-    plan->nt = m1 ? 0 : NT;
+    plan->nt = NT;
     plan->nslots = nslots;
     plan->slot_bytes = slot_bytes;
     plan->off_b = nslots * slot_bytes;
@@ -698,43 +479,6 @@ bool gemv_pq2_plan(const ninfer_row_split_geometry &g, uint64_t M, bool rotate, 
     return true;
 }
 
-namespace {
-using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-int encode_fn(EncodeTiledFn *out) {
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q);
-        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !ptr)
-            return fail(NINFER_ERR_CUDA, "cuTensorMapEncodeTiled unavailable (%s)", cudaGetErrorString(e));
-        fn = reinterpret_cast<EncodeTiledFn>(ptr);
-    }
-    *out = fn;
-    return NINFER_OK;
-}
-
-// Base rows [row0, row0 + rows * ctas) of width row_bytes as a byte tensor
-// {row_bytes, rows, ctas} (3-D when ctas > 1), boxes of 128 bytes x 32 rows.
-int encode_rows(CUtensorMap *map, const uint8_t *addr, uint64_t row_bytes, uint64_t rows, uint64_t ctas) {
-    EncodeTiledFn fn;
-    int st = encode_fn(&fn);
-    if (st) return st;
-    const cuuint32_t rank = ctas > 1 ? 3 : 2;
-    const cuuint64_t dims[3] = {row_bytes, rows, ctas};
-    const cuuint64_t strides[2] = {row_bytes, row_bytes * rows};
-    const cuuint32_t box[3] = {128, (cuuint32_t)kTile, 1};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, rank, const_cast<uint8_t *>(addr), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return fail(NINFER_ERR_CUDA, "tensor map encode failed (CUresult %d)", (int)r);
-    return NINFER_OK;
-}
-}  // namespace
 
 int gemv_pq2_launch(const GemvPlan &plan, const uint8_t *payload, const ninfer_row_split_geometry &g, const void *x,
                     int x_dtype, const uint16_t *signs, void *y, int y_dtype, uint64_t M, cudaStream_t stream,
@@ -766,15 +510,12 @@ int gemv_pq2_launch(const GemvPlan &plan, const uint8_t *payload, const ninfer_r
     if (st) return st;
     const uint64_t R = plan.rows_per_cta, G = plan.grid;
     if (G > 1) {
-        st = encode_rows(&p.tmap_main, p.base, g.base_row_bytes, R, G - 1);
+        st = encode_rows(&p.tmap_main, p.base, g.base_row_bytes, R, G - 1, 128, kTile, true);
         if (st) return st;
     }
-    st = encode_rows(&p.tmap_last, p.base + (G - 1) * R * g.base_row_bytes, g.base_row_bytes, g.n - (G - 1) * R, 1);
+    st = encode_rows(&p.tmap_last, p.base + (G - 1) * R * g.base_row_bytes, g.base_row_bytes, g.n - (G - 1) * R, 1, 128, kTile, true);
     if (st) return st;
-    void (*kern)(const Params) = plan.nt == 0   ? gemv_pq2_m1_kernel
-                                 : plan.nt == 1 ? gemv_pq2_kernel<1>
-                                 : plan.nt == 2 ? gemv_pq2_kernel<2>
-                                                : gemv_pq2_kernel<3>;
+    void (*kern)(const Params) = plan.nt == 1 ? gemv_pq2_kernel<1> : plan.nt == 2 ? gemv_pq2_kernel<2> : gemv_pq2_kernel<3>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.smem);
     if (e != cudaSuccess) return fail(NINFER_ERR_CUDA, "gemv: smem attribute: %s", cudaGetErrorString(e));
     cudaLaunchConfig_t cfg = {};
@@ -794,14 +535,3 @@ int gemv_pq2_launch(const GemvPlan &plan, const uint8_t *payload, const ninfer_r
 
 }  // namespace ninfer
 
-extern "C" int ninfer_device_errors(uint32_t *out, int clear) {
-    if (!out) return ninfer::fail(NINFER_ERR_INVALID_ARGUMENT, "device_errors: NULL output");
-    cudaError_t e = cudaMemcpyFromSymbol(out, ninfer::g_device_error, sizeof(uint32_t));
-    if (e != cudaSuccess) return ninfer::fail(NINFER_ERR_CUDA, "device_errors: %s", cudaGetErrorString(e));
-    if (clear) {
-        const uint32_t zero = 0;
-        e = cudaMemcpyToSymbol(ninfer::g_device_error, &zero, sizeof(uint32_t));
-        if (e != cudaSuccess) return ninfer::fail(NINFER_ERR_CUDA, "device_errors: %s", cudaGetErrorString(e));
-    }
-    return NINFER_OK;
-}

@@ -38,11 +38,12 @@ static bool g_pdl = true;
 using namespace ninfer;
 
 namespace {
-enum class Path { kFusedPq2, kTiled };
+enum class Path { kIntPq2, kFusedPq2, kTiled };
 
 struct MatmulPlan {
     Path path;
     GemvPlan gemv;
+    IntPlan gint;
     uint64_t workspace;
 };
 
@@ -51,6 +52,11 @@ int plan_matmul(int fmt, const ninfer_row_split_geometry &g, uint64_t M, bool ro
     int st = device_info(&d);
     if (st) return st;
     mp->workspace = 0;
+    if (fmt == NINFER_PQ2_0_G128 && gemv_pq2_int_plan(g, M, rotate, d.sms, d.smem_optin, &mp->gint)) {
+        mp->path = Path::kIntPq2;
+        mp->workspace = mp->gint.workspace;     // the prepared activation
+        return NINFER_OK;
+    }
     if (fmt == NINFER_PQ2_0_G128 && gemv_pq2_plan(g, M, rotate, d.sms, d.smem_optin, &mp->gemv)) {
         mp->path = Path::kFusedPq2;
         return NINFER_OK;
@@ -112,6 +118,8 @@ extern "C" int ninfer_ternary_matmul(int fmt, const uint8_t *payload, uint64_t p
                     (unsigned long long)need, (unsigned long long)workspace_bytes);
     if (need && !aligned(workspace, 16)) return fail(NINFER_ERR_ALIGNMENT, "matmul: workspace must be 16-byte aligned");
     cudaStream_t s = (cudaStream_t)stream;
+    if (mp.path == Path::kIntPq2)
+        return gemv_pq2_int_launch(mp.gint, payload, g, x, x_dtype, signs_bf16, y, y_dtype, workspace, s, g_pdl);
     if (mp.path == Path::kFusedPq2)
         return gemv_pq2_launch(mp.gemv, payload, g, x, x_dtype, signs_bf16, y, y_dtype, M, s, g_pdl);
     const PlaneView p = make_view(payload, g, fmt);

@@ -64,7 +64,7 @@ def test_matmul_tiny_workload():
 
 @pytest.mark.parametrize("fmt", ["PQ2_0_G128", "PTQ1_0_G128"])
 @pytest.mark.parametrize("n,k,M", [(300, 2048, 1), (300, 2048, 8), (77, 3072, 3), (1, 1024, 1), (17, 5120, 2),
-                                   (1000, 1024, 5)])
+                                   (1000, 1024, 5), (31, 2048, 1), (517, 5120, 1), (50001, 1024, 1)])
 def test_matmul_small_shapes(fmt, n, k, M):
     c = synth.make_case("gateup", n=n, k=k, M=M, seed=n * 7 + k + M)
     y = run_matmul(fmt, c)
