@@ -80,8 +80,7 @@ def sources_sha256(files) -> str:
     return d.hexdigest()
 
 
-GEMV_SOURCES = ["bit_gemv_gb300/csrc/gemv_pq2_int.cu", "bit_gemv_gb300/csrc/act_prep.cu",
-                "bit_gemv_gb300/csrc/gemv_common.cu", "bit_gemv_gb300/csrc/async.cuh",
+GEMV_SOURCES = ["bit_gemv_gb300/csrc/gemv_pq2_int.cu", "bit_gemv_gb300/csrc/gemv_common.cu", "bit_gemv_gb300/csrc/async.cuh",
                 "bit_gemv_gb300/csrc/device.cuh", "bit_gemv_gb300/csrc/gemv.h"]
 KERNEL_TAG = "gemv"
 
@@ -270,13 +269,15 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                 "h2d_bytes_per_step": int(x_host.numel() * x_host.element_size()),
                 "d2h_bytes_per_step": int(M * n * 4), "ms_per_step": round(ms_e2e / args.steps, 6)},
         "clocks": clock_info,
-        "gpu_launches": args.steps * kernels_per_step(),
+        "gpu_launches": args.steps * kernels_per_step(w),
     }
     return res
 
 
-def kernels_per_step() -> int:
-    return 2          # activation rotate/quantise + decode GEMV
+def kernels_per_step(w) -> int:
+    """Kernels one projection launches: the PQ2_0 decode kernels (M <= 8) rotate
+    x themselves; the general path runs the transform and then the tiled GEMM."""
+    return 1 if (w.fmt == "PQ2_0_G128" and w.M <= 8) else 2
 
 
 # ------------------------------------------------------------ CPU oracle ---

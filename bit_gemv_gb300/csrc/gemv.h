@@ -29,24 +29,17 @@ int device_error_word(uint32_t **out);
 int encode_rows(CUtensorMap *map, const uint8_t *addr, uint64_t row_bytes, uint64_t rows, uint64_t ctas,
                 uint32_t box_bytes, uint32_t box_rows, bool swizzle128);
 
-// Activation preparation for the integer decode kernels (act_prep.cu): per row
-// of x, rotated 16-bit fixed-point operand words + per-group {2^-E, sum}.
-uint64_t act_prep_int16_row_bytes(uint64_t k_pad);
-int act_prep_int16_launch(const void *x, int x_dtype, const uint16_t *signs, uint64_t k, uint64_t k_pad, uint64_t M,
-                          uint32_t copies, uint8_t *out, cudaStream_t stream, bool pdl);
-
-// M = 1 integer kernel (PQ2_0_G128).
+// M = 1 integer kernel (PQ2_0_G128), rotation fused in.
 struct IntPlan {
     bool ok;
-    uint32_t grid, rows_per_cta, nbox, nslots, pre_issue;
-    uint32_t off_ring, off_act, off_part, off_bar, off_cnt, act_bytes, smem;
+    uint32_t grid, rows_per_cta, nitem, nslots, pre_issue;
+    uint32_t off_ring, off_act, off_part, off_bar, off_cnt, smem;
     uint64_t workspace;
 };
 bool gemv_pq2_int_plan(const ninfer_row_split_geometry &g, uint64_t M, bool rotate, int sms, int smem_limit,
                        IntPlan *plan);
 int gemv_pq2_int_launch(const IntPlan &plan, const uint8_t *payload, const ninfer_row_split_geometry &g, const void *x,
-                        int x_dtype, const uint16_t *signs, void *y, int y_dtype, void *workspace, cudaStream_t stream,
-                        bool pdl);
+                        int x_dtype, const uint16_t *signs, void *y, int y_dtype, cudaStream_t stream, bool pdl);
 
 bool gemv_pq2_plan(const ninfer_row_split_geometry &g, uint64_t M, bool rotate, int sms, int smem_limit,
                    GemvPlan *plan);

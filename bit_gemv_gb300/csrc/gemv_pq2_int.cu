@@ -1,35 +1,40 @@
 // Decode GEMV for PQ2_0_G128 weights and one activation row (M = 1), on the
-// CUDA cores' integer pipes.
+// CUDA cores' integer pipes, with the activation rotation fused in.
 //
 // What it computes:
 //   y[r] = sum_g scale[r][g] * sum_{j<128} (code[r][128g+j] - 1) * xr[128g+j]
-// with xr the forward-rotated activation ("artifact-container.md" §8
-// hadamard_signs; TensorSharp article §4.2), codes the 2-bit fields of the base
-// plane, least significant first, value = code - 1 ("GGUF 完整讲解" §4.3), and
-// one binary16 scale per 128-weight group at scale_offset
-// ("bonsai三元GGUF模型转ninfer模型01" §3).
+// with xr the forward-rotated activation, per 1024-block H (D * x) / 32
+// ("artifact-container.md" §8 hadamard_signs; TensorSharp article §4.2), codes
+// the 2-bit fields of the base plane, least significant first, value = code - 1
+// ("GGUF 完整讲解" §4.3), and one binary16 scale per 128-weight group at
+// scale_offset ("bonsai三元GGUF模型转ninfer模型01" §3).
 //
-// Arithmetic: the activation arrives prepared by act_prep.cu as 16-bit fixed
-// point per 1024-block (x16 = rint(xr * 2^E)). In a 32-bit word of codes (16
+// Arithmetic: every CTA rotates x itself (one warp per 1024-block: sign
+// multiply, the 1024-point butterfly, block maximum) and keeps it in shared
+// memory as 16-bit fixed point, x16 = rint(xr * 2^E) with E per block so that
+// max |x16| < 2^14, laid out as dp2a operands. In a 32-bit word of codes (16
 // weights, four per byte) the mask 0x03 << 2p per byte leaves the four codes of
 // position p as bytes (times 4^p); dp2a multiplies two of them by two int16
 // activations and accumulates exactly in int32. Per group:
 //   sum_j c_j x16_j = acc0 + acc1/4 + acc2/16 + acc3/64        (exact shifts)
 //   y += scale * 2^-E * (that - sum_j x16_j)                     (value = code - 1)
-// GB300 issues LOP3 and dp2a at 64 lanes/clk/SM each (partly co-issuing);
-// with two rows per lane the loop sustains ~100 weights/clk/SM, above the
-// HBM rate of ~70-80 weights/clk/SM, while legacy mma.sync with changing
-// operands reaches only ~55.
+// dp2a issues on the FMA-heavy pipe and the masks on the ALU pipe, so the two
+// overlap; legacy mma.sync with changing operands is slower on GB300.
 //
-// Data movement: two CTAs per SM, each owning a contiguous row range. Weights
-// stream through a ring of item slots; an item is 64 rows x 4 groups: two
-// 128-byte-swizzled tensor boxes of 32 rows x 128 bytes (a 3-D map view keeps
-// them inside the CTA's rows) plus the two matching boxes of scales (32 rows x
-// 16 bytes). Each item completes on its own mbarrier. The last of the four
-// warps reading an item re-arms its slot with the item nslots further on. A
-// few items are requested before the programmatic-dependent-launch wait
-// (weights are read-only parameters); the prepared activation follows as one
-// bulk copy right after the wait, ahead of the rest of the ring.
+// Data movement: one CTA per SM owns a contiguous row range, in tiles of 128
+// rows. Weights stream through a ring of item slots; an item is 128 rows x 8
+// groups: two 128-byte-swizzled tensor boxes of 128 rows x 128 bytes (a 3-D
+// map view keeps them inside the CTA's rows) and one box of the rows' 8 scales
+// (128 rows x 16 bytes), completing on the slot's mbarrier. Warps w and w + 8
+// take words 0-3 and 4-7 of group w of every item, lane l rows l, l+32, l+64,
+// l+96 of the tile, so each activation word read from shared memory serves
+// four rows. A few items are
+// requested before the programmatic-dependent-launch wait (weights and signs
+// are read-only parameters, so the stream overlaps the previous kernel's
+// tail); x is requested right after the wait and the rest of the ring behind
+// it, so the latency-critical read does not queue behind the whole slice. The
+// last of the sixteen warps reading an item re-arms its slot with the item
+// nslots further on.
 #include <cstring>
 
 #include <cuda.h>
@@ -43,23 +48,24 @@
 namespace ninfer {
 namespace {
 
-constexpr int kThreads = 256;     // 8 warps; two CTAs per SM
-constexpr int kWarps = 8;
-constexpr int kRows = 64;         // rows per tile: two 32-row boxes, two rows per lane
-constexpr uint32_t kItemBytes = 2 * 4096 + 2 * 512;
-constexpr uint32_t kMaxSlots = 12;
-constexpr uint32_t kActCopies = 8;     // prepared-activation copies, read by CTA % 8
+constexpr int kThreads = 512;     // 16 warps, two per group of an item; one CTA per SM
+constexpr int kWarps = 16;
+constexpr int kRows = 128;        // rows per tile, four per lane
+constexpr uint32_t kBoxBytes = 128 * kRows;              // one 128-byte column of the tile
+constexpr uint32_t kItemBytes = 2 * kBoxBytes + 16 * kRows;
+constexpr uint32_t kMaxSlots = 8;
+constexpr uint32_t kRotWarps = 8;     // warps that rotate x (one 1024-block at a time each)
 
 struct IntParams {
     CUtensorMap wmap_main, wmap_last;   // base rows: {row bytes, R rows, CTA} / last CTA {row bytes, rows}
     CUtensorMap smap_main, smap_last;   // scale rows, same views
-    const uint8_t *act;                 // prepared activation (act_prep.cu layout), kActCopies copies
-    uint64_t act_copy_stride;
+    const void *x;
+    const uint16_t *signs;              // bf16 +-1 per element, or null (no rotation)
     void *y;
     uint64_t n;
-    uint32_t groups, nbox, rows_per_cta;
-    int y_dtype;
-    uint32_t nslots, pre_issue, act_bytes;
+    uint32_t k, groups, nblk, nitem, rows_per_cta;     // nitem: items per tile, ceil(groups / 8)
+    int x_dtype, y_dtype;
+    uint32_t nslots, pre_issue;
     uint32_t off_ring, off_act, off_part, off_bar, off_cnt;
     uint32_t *err;
 };
@@ -75,37 +81,147 @@ __device__ __forceinline__ int dp2a_hi(uint32_t a, uint32_t b, int c) {
     return d;
 }
 
-// Item i = tile * nbox + column: its two weight boxes and two scale boxes into
-// ring slot i % nslots (one thread).
+// Item i = tile * nitem + j (groups 8j .. 8j + 7 of the tile's rows): its two
+// weight boxes and its scale box into ring slot i % nslots (one thread).
 __device__ __forceinline__ void issue_item(const IntParams &p, uint8_t *smem, uint32_t item, bool last_cta) {
-    const uint32_t tile = item / p.nbox, col = item % p.nbox, slot = item % p.nslots;
+    const uint32_t tile = item / p.nitem, j = item % p.nitem, slot = item % p.nslots;
     const uint32_t dst = smem_u32(smem + p.off_ring) + slot * kItemBytes;
     const uint32_t bar = smem_u32(smem + p.off_bar) + 8 * slot;
     mbar_arrive_expect_tx(bar, kItemBytes);
-    const int x = (int)(col * 128), xs = (int)((col >> 1) * 16), y0 = (int)(tile * kRows);
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        if (last_cta) {
-            tma_load_2d(dst + h * 4096, &p.wmap_last, x, y0 + 32 * h, bar);
-            tma_load_2d(dst + 8192 + h * 512, &p.smap_last, xs, y0 + 32 * h, bar);
-        } else {
-            tma_load_3d(dst + h * 4096, &p.wmap_main, x, y0 + 32 * h, (int)blockIdx.x, bar);
-            tma_load_3d(dst + 8192 + h * 512, &p.smap_main, xs, y0 + 32 * h, (int)blockIdx.x, bar);
-        }
+    const int y0 = (int)(tile * kRows), xs = (int)(j * 16);
+    if (last_cta) {
+        tma_load_2d(dst, &p.wmap_last, (int)(j * 256), y0, bar);
+        tma_load_2d(dst + kBoxBytes, &p.wmap_last, (int)(j * 256 + 128), y0, bar);
+        tma_load_2d(dst + 2 * kBoxBytes, &p.smap_last, xs, y0, bar);
+    } else {
+        tma_load_3d(dst, &p.wmap_main, (int)(j * 256), y0, (int)blockIdx.x, bar);
+        tma_load_3d(dst + kBoxBytes, &p.wmap_main, (int)(j * 256 + 128), y0, (int)blockIdx.x, bar);
+        tma_load_3d(dst + 2 * kBoxBytes, &p.smap_main, xs, y0, (int)blockIdx.x, bar);
     }
 }
 
-__global__ void __launch_bounds__(kThreads, 2) gemv_pq2_int_kernel(const __grid_constant__ IntParams p) {
+// Activation preparation, one warp per 1024-block, 32 elements per lane. Pass
+// 1: lane l holds elements 32l + r and butterflies index bits 0-4 in registers.
+// A transpose through a padded 32 x 33 float tile (conflict-free both ways)
+// gives lane c the elements 32j + c, and pass 2 butterflies bits 5-9. The
+// quantised values go through the same scratch as int16 in natural order, so
+// that each lane can read 16-byte runs of eight consecutive elements for the
+// operand words.
+constexpr uint32_t kRotScratch = 32 * 33 * 4;      // bytes per rotating warp
+
+__device__ __forceinline__ void butterfly32(float (&v)[32]) {
+#pragma unroll
+    for (int bit = 0; bit < 5; ++bit)
+#pragma unroll
+        for (int r = 0; r < 32; ++r) {
+            if (r & (1 << bit)) continue;
+            const float a0 = v[r], a1 = v[r | (1 << bit)];
+            v[r] = a0 + a1;
+            v[r | (1 << bit)] = a0 - a1;
+        }
+}
+
+// x (times the signs) of block b: lane l gets elements 32l .. 32l + 31 (zero past k).
+__device__ __forceinline__ void load_block(const IntParams &p, uint32_t b, int lane, float (&v)[32]) {
+    const uint64_t e0 = (uint64_t)b * 1024 + 32 * lane;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float t[8];
+        const uint64_t idx = e0 + 8 * i;
+        if (idx + 8 <= p.k) {
+            load8(p.x, idx, p.x_dtype, t);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) t[e] = idx + e < p.k ? load1(p.x, idx + e, p.x_dtype) : 0.f;
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[8 * i + e] = t[e];
+    }
+}
+
+__device__ __forceinline__ void load_block_signs(const IntParams &p, uint32_t b, int lane, float (&d)[32]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float t[8];
+        load_signs8(p.signs, (uint64_t)b * 1024 + 32 * lane + 8 * i, t);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) d[8 * i + e] = t[e];
+    }
+}
+
+// Rotates and quantises block b (x in v, signs in d) and writes its dp2a
+// operand words and group entries to shared memory:
+//   act[word][4h + p] = (x16[16 word + 8h + p], x16[16 word + 8h + 4 + p]),
+//   gs[group] = {2^-E, sum of the group's x16 (as int bits)},
+// x16 = rint(xr * 2^E), E per block so that max |x16| < 2^14.
+__device__ __forceinline__ void prepare_block(const IntParams &p, uint8_t *act_s, uint32_t b, int lane,
+                                              float (&v)[32], const float (&d)[32], float *tile) {
+    const bool rotate = p.signs != nullptr;
+    if (rotate) {
+#pragma unroll
+        for (int r = 0; r < 32; ++r) v[r] *= d[r];
+        butterfly32(v);                       // index bits 0-4
+    }
+#pragma unroll
+    for (int r = 0; r < 32; ++r) tile[r * 33 + lane] = v[r];     // element 32 lane + r
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = tile[lane * 33 + j];     // element 32 j + lane
+    if (rotate) butterfly32(v);               // index bits 5-9; v = 32 * xr
+    float mx = 0.f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) mx = fmaxf(mx, fabsf(v[j]));
+#pragma unroll
+    for (int s = 16; s > 0; s >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, s));
+    int ev = 0;                               // max |v * 2^ev| < 2^14
+    if (mx > 0.f) ev = 13 - ilogbf(mx);
+    ev = max(-100, min(100, ev));
+    const float up = ldexpf(1.f, ev);
+    const int E = rotate ? ev + 5 : ev;       // x16 = xr * 2^E (xr = v / 32 when rotated)
+    __syncwarp();                             // every lane has read the tile
+    int16_t *qs = reinterpret_cast<int16_t *>(tile);
+#pragma unroll
+    for (int j = 0; j < 32; ++j)              // adding 1.5 * 2^23 rounds to nearest, ties to even
+        qs[32 * j + lane] = (int16_t)(__float_as_int(fmaf(v[j], up, 12582912.0f)) - 0x4B400000);
+    __syncwarp();
+    // 128 runs of eight elements; lane takes runs lane + 32i (operand word run/2, half run&1)
+    uint4 *act = reinterpret_cast<uint4 *>(act_s);
+    float2 *gs = reinterpret_cast<float2 *>(act_s + (uint64_t)p.groups * 256);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int run = lane + 32 * i;
+        const uint4 raw = reinterpret_cast<const uint4 *>(qs)[run];
+        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};     // x16 pairs (2e, 2e+1)
+        // entry p = (x16[p], x16[4 + p]) of the run
+        uint4 pk;
+        pk.x = __byte_perm(w[0], w[2], 0x5410);
+        pk.y = __byte_perm(w[0], w[2], 0x7632);
+        pk.z = __byte_perm(w[1], w[3], 0x5410);
+        pk.w = __byte_perm(w[1], w[3], 0x7632);
+        const uint32_t word = b * 64 + (run >> 1);
+        if (word < p.groups * 8) act[word * 2 + (run & 1)] = pk;
+        int sum = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) sum += (int)(int16_t)(w[q] & 0xffff) + (int)(int16_t)(w[q] >> 16);
+#pragma unroll
+        for (int sh = 8; sh > 0; sh >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, sh);
+        const uint32_t G = b * 8 + (run >> 4);     // 16 runs per group of 128
+        if ((lane & 15) == 0 && G < p.groups) gs[G] = make_float2(ldexpf(1.f, -E), __int_as_float(sum));
+    }
+    __syncwarp();                             // qs is read before the next block reuses the tile
+}
+
+__global__ void __launch_bounds__(kThreads, 1) gemv_pq2_int_kernel(const __grid_constant__ IntParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint64_t r_begin = (uint64_t)blockIdx.x * p.rows_per_cta;
     const uint64_t r_end = r_begin + p.rows_per_cta < p.n ? r_begin + p.rows_per_cta : p.n;
     const bool last_cta = blockIdx.x == gridDim.x - 1;
     const uint32_t ntile = (uint32_t)((r_end - r_begin + kRows - 1) / kRows);
-    const uint32_t nitems = ntile * p.nbox;
+    const uint32_t nitems = ntile * p.nitem;
     const uint32_t bar0 = smem_u32(smem + p.off_bar);
-    const uint32_t act_bar = bar0 + 8 * kMaxSlots;
     uint32_t *cnt = reinterpret_cast<uint32_t *>(smem + p.off_cnt);
+    uint32_t *issued = cnt + kMaxSlots, *failed = cnt + kMaxSlots + 1;
 
     if (tid == 0) {
         prefetch_tmap(last_cta ? &p.wmap_last : &p.wmap_main);
@@ -114,90 +230,114 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_pq2_int_kernel(const __grid_
             mbar_init(bar0 + 8 * s, 1);
             cnt[s] = 0;
         }
-        mbar_init(act_bar, 1);
+        *failed = 0;
         fence_mbar_init();
     }
     __syncthreads();
     const uint32_t ring_to = p.nslots < nitems ? p.nslots : nitems;
+    const uint32_t pre = p.pre_issue < ring_to ? p.pre_issue : ring_to;
     if (tid == 0) {
-        // weights are read-only parameters: start their stream before waiting
-        // on the preceding kernels
-        for (uint32_t i = 0; i < p.pre_issue && i < ring_to; ++i) issue_item(p, smem, i, last_cta);
+        // weights are read-only parameters: a few items before the dependency wait
+        for (uint32_t i = 0; i < pre; ++i) issue_item(p, smem, i, last_cta);
     }
+    // rotation: warp w < nrot takes blocks w, w + nrot, ...
+    const uint32_t nrot = p.nblk < kRotWarps ? p.nblk : kRotWarps;
+    float d[32];
+    if (p.signs && (uint32_t)warp < nrot) load_block_signs(p, warp, lane, d);     // also read-only
     pdl_launch_dependents();
-    pdl_wait();          // the prepared activation comes from the preceding kernel
-    if (tid == 0) {
-        mbar_arrive_expect_tx(act_bar, p.act_bytes);
-        bulk_g2s(smem_u32(smem + p.off_act), p.act + (blockIdx.x % kActCopies) * p.act_copy_stride, p.act_bytes,
-                 act_bar);
-        for (uint32_t i = p.pre_issue; i < ring_to; ++i) issue_item(p, smem, i, last_cta);
-    }
-    bool ok = mbar_wait(act_bar, 0, p.err);
+    pdl_wait();          // x may come from the preceding kernel
 
-    const uint32_t gi = warp & 3, par = warp >> 2;
-    const uint32_t ring = smem_u32(smem + p.off_ring), act_addr = smem_u32(smem + p.off_act);
-    const float2 *gs = reinterpret_cast<const float2 *>(smem + p.off_act + p.groups * 256);
+    float v[32];
+    if ((uint32_t)warp < nrot) load_block(p, warp, lane, v);
+    __syncthreads();     // every warp's x request is out: the rest of the ring queues behind them
+    if (tid == 0) {
+        for (uint32_t i = pre; i < ring_to; ++i) issue_item(p, smem, i, last_cta);
+        *issued = ring_to;
+    }
+    uint8_t *act_s = smem + p.off_act;
+    if ((uint32_t)warp < nrot) {
+        float *tile = reinterpret_cast<float *>(smem + p.off_part + warp * kRotScratch);
+        for (uint32_t b = warp; b < p.nblk; b += nrot) {
+            if (b != (uint32_t)warp) {
+                if (p.signs) load_block_signs(p, b, lane, d);
+                load_block(p, b, lane, v);
+            }
+            prepare_block(p, act_s, b, lane, v, d, tile);
+        }
+    }
+    __syncthreads();
+
+    bool ok = true;
+    // group gw of the item = 16-byte chunks 2gi, 2gi+1 of column h's 128-byte
+    // line; this warp reads chunk 2gi + half (words 4 half .. 4 half + 3), swizzled by row % 8
+    const uint32_t gw = warp & 7, half = warp >> 3, h = gw >> 2, gi = gw & 3;
+    const uint32_t ch = ((2 * gi + half) ^ (lane & 7)) << 4;
+    const float2 *gs = reinterpret_cast<const float2 *>(act_s + p.groups * 256);
     float *part = reinterpret_cast<float *>(smem + p.off_part);
-    const uint32_t sw = (uint32_t)(lane & 7);
     for (uint32_t tile = 0; tile < ntile; ++tile) {
-        float y0 = 0.f, y1 = 0.f;      // rows lane and lane + 32 of the tile
-        for (uint32_t col = par; col < p.nbox; col += 2) {
-            const uint32_t item = tile * p.nbox + col, slot = item % p.nslots;
+        float y[4] = {0.f, 0.f, 0.f, 0.f};      // rows lane + 32q of the tile
+        for (uint32_t j = 0; j < p.nitem; ++j) {
+            const uint32_t item = tile * p.nitem + j, slot = item % p.nslots;
             ok = ok && mbar_wait(bar0 + 8 * slot, (item / p.nslots) & 1, p.err);
-            const uint32_t G = col * 4 + gi;
+            const uint32_t G = j * 8 + gw;
             if (ok && G < p.groups) {
-                const uint32_t sa = ring + slot * kItemBytes;
-                const uint32_t r0 = sa + lane * 128, r1 = r0 + 4096;
-                // group G = 16-byte chunks 2gi, 2gi+1 of the box line, swizzled by row % 8
-                const uint32_t ch0 = ((2 * gi) ^ sw) << 4, ch1 = ((2 * gi + 1) ^ sw) << 4;
-                const uint4 a0 = lds128u(r0 + ch0), a1 = lds128u(r0 + ch1);
-                const uint4 b0 = lds128u(r1 + ch0), b1 = lds128u(r1 + ch1);
-                const uint32_t wa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-                const uint32_t wb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-                int u0 = 0, u1 = 0, u2 = 0, u3 = 0, v0 = 0, v1 = 0, v2 = 0, v3 = 0;
+                const uint8_t *sa = smem + p.off_ring + slot * kItemBytes;
+                const uint8_t *wr = sa + h * kBoxBytes + lane * 128 + ch;
+                uint32_t w[4][4];
 #pragma unroll
-                for (int wi = 0; wi < 8; ++wi) {
-                    const uint32_t aw = act_addr + (G * 8 + wi) * 32;
-                    const uint4 lo = lds128u(aw), hi = lds128u(aw + 16);
-                    const uint32_t ca = wa[wi], cb = wb[wi];
-                    u0 = dp2a_hi(hi.x, ca & 0x03030303u, dp2a_lo(lo.x, ca & 0x03030303u, u0));
-                    u1 = dp2a_hi(hi.y, ca & 0x0C0C0C0Cu, dp2a_lo(lo.y, ca & 0x0C0C0C0Cu, u1));
-                    u2 = dp2a_hi(hi.z, ca & 0x30303030u, dp2a_lo(lo.z, ca & 0x30303030u, u2));
-                    u3 = dp2a_hi(hi.w, ca & 0xC0C0C0C0u, dp2a_lo(lo.w, ca & 0xC0C0C0C0u, u3));
-                    v0 = dp2a_hi(hi.x, cb & 0x03030303u, dp2a_lo(lo.x, cb & 0x03030303u, v0));
-                    v1 = dp2a_hi(hi.y, cb & 0x0C0C0C0Cu, dp2a_lo(lo.y, cb & 0x0C0C0C0Cu, v1));
-                    v2 = dp2a_hi(hi.z, cb & 0x30303030u, dp2a_lo(lo.z, cb & 0x30303030u, v2));
-                    v3 = dp2a_hi(hi.w, cb & 0xC0C0C0C0u, dp2a_lo(lo.w, cb & 0xC0C0C0C0u, v3));
+                for (int q = 0; q < 4; ++q) {
+                    const uint4 a = *reinterpret_cast<const uint4 *>(wr + q * 4096);
+                    w[q][0] = a.x; w[q][1] = a.y; w[q][2] = a.z; w[q][3] = a.w;
+                }
+                const uint4 *aw = reinterpret_cast<const uint4 *>(act_s + (uint64_t)G * 256 + half * 128);
+                int acc[4][4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) acc[q][t] = 0;
+#pragma unroll
+                for (int wi = 0; wi < 4; ++wi) {
+                    const uint4 lo = aw[2 * wi], hi = aw[2 * wi + 1];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint32_t c = w[q][wi];
+                        acc[q][0] = dp2a_hi(hi.x, c & 0x03030303u, dp2a_lo(lo.x, c & 0x03030303u, acc[q][0]));
+                        acc[q][1] = dp2a_hi(hi.y, c & 0x0C0C0C0Cu, dp2a_lo(lo.y, c & 0x0C0C0C0Cu, acc[q][1]));
+                        acc[q][2] = dp2a_hi(hi.z, c & 0x30303030u, dp2a_lo(lo.z, c & 0x30303030u, acc[q][2]));
+                        acc[q][3] = dp2a_hi(hi.w, c & 0xC0C0C0C0u, dp2a_lo(lo.w, c & 0xC0C0C0C0u, acc[q][3]));
+                    }
                 }
                 const float2 f = gs[G];
-                const int off = __float_as_int(f.y);
-                const int t0 = u0 + (u1 >> 2) + (u2 >> 4) + (u3 >> 6) - off;
-                const int t1 = v0 + (v1 >> 2) + (v2 >> 4) + (v3 >> 6) - off;
-                // scale box: row r at r * 16 bytes holds groups 8 * (col / 2) .. + 7
-                const uint32_t so = 2 * (4 * (col & 1) + gi);
-                const float s0 = __half2float(__ushort_as_half((unsigned short)lds16(sa + 8192 + lane * 16 + so)));
-                const float s1 = __half2float(__ushort_as_half((unsigned short)lds16(sa + 8192 + 512 + lane * 16 + so)));
-                y0 = fmaf(s0 * f.x, (float)t0, y0);
-                y1 = fmaf(s1 * f.x, (float)t1, y1);
+                const int off = half ? 0 : __float_as_int(f.y);     // the group's sum of x16, once
+                // scale box: row r at r * 16 bytes holds the item's 8 scales
+                const uint8_t *sc = sa + 2 * kBoxBytes + lane * 16 + 2 * gw;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int t = acc[q][0] + (acc[q][1] >> 2) + (acc[q][2] >> 4) + (acc[q][3] >> 6) - off;
+                    const float s = __half2float(*reinterpret_cast<const __half *>(sc + q * 512));
+                    y[q] = fmaf(s * f.x, (float)t, y[q]);
+                }
             }
-            // release the slot; the fourth reader re-arms it with item + nslots
+            // release the slot; the last of the sixteen readers re-arms it with item + nslots
             __syncwarp();
             if (lane == 0) {
+                if (!ok) *failed = 1;
                 __threadfence_block();
                 const uint32_t seen = atomicAdd(&cnt[slot], 1u);
-                if (seen == 3) {
+                if (seen == kWarps - 1) {
                     cnt[slot] = 0;
-                    if (ok && item + p.nslots < nitems) {
+                    if (ok && !*(volatile uint32_t *)failed && item + p.nslots < nitems) {
                         fence_proxy_async();
                         issue_item(p, smem, item + p.nslots, last_cta);
+                        atomicAdd(issued, 1u);
                     }
                 }
             }
         }
-        part[warp * kRows + lane] = y0;
-        part[warp * kRows + 32 + lane] = y1;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) part[warp * kRows + 32 * q + lane] = y[q];
         __syncthreads();
-        if (warp < 2) {
+        if (warp < kRows / 32) {
             const uint32_t rl = warp * 32 + lane;
             const uint64_t r = r_begin + (uint64_t)tile * kRows + rl;
             float acc = 0.f;
@@ -206,6 +346,13 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_pq2_int_kernel(const __grid_
             if (r < r_end) store1(p.y, r, p.y_dtype, acc);
         }
         __syncthreads();
+    }
+    // after a timed-out wait: let the copies still in flight land (at most one
+    // per slot, the last one issued into it) before the CTA's memory is freed
+    if (tid == 0 && *(volatile uint32_t *)failed) {
+        const uint32_t n_issued = *(volatile uint32_t *)issued;
+        for (uint32_t i = n_issued > p.nslots ? n_issued - p.nslots : 0; i < n_issued; ++i)
+            mbar_wait(bar0 + 8 * (i % p.nslots), (i / p.nslots) & 1, p.err, 200000000ll);
     }
 }
 
@@ -216,79 +363,75 @@ bool gemv_pq2_int_plan(const ninfer_row_split_geometry &g, uint64_t M, bool rota
     *plan = IntPlan{};
     if (M != 1) return false;
     if (rotate && g.k % 1024) return false;
-    // scale rows must be whole 16-byte units for the scale boxes
+    // scale rows must be whole 16-byte units (8 groups) for the scale boxes
     if (g.scale_row_bytes % 16 || g.base_row_bytes % 16 || g.payload_bytes % 16) return false;
     if (g.k > (1u << 24) || g.n > (1ull << 31)) return false;
     const uint32_t groups = (uint32_t)g.groups_per_row;
-    const uint32_t nbox = (uint32_t)((g.base_row_bytes + 127) / 128);
     const uint32_t act_bytes = ((groups * 264 + 15) / 16) * 16;
-    const uint32_t part_bytes = kWarps * kRows * 4;
-    const uint32_t bar_bytes = (kMaxSlots + 1) * 8;
-    const uint32_t fixed = act_bytes + part_bytes + bar_bytes + kMaxSlots * 4;
-    // two CTAs per SM share its 228 KB (each CTA also reserves 1 KB)
-    const int per_cta = (228 * 1024) / 2 - 1024;
-    const int limit = std::min(smem_limit, per_cta);
-    if ((int)fixed + 2 * (int)kItemBytes > limit) return false;
-    const uint32_t nslots = std::min<uint32_t>(kMaxSlots, (uint32_t)((limit - (int)fixed) / (int)kItemBytes));
-    // two CTAs per SM with ~n / (2 * SMs) rows each (tiles of 64 rows, the last
-    // one partly out of the CTA's range and never read from HBM)
-    const uint64_t grid0 = std::max<uint64_t>(1, std::min<uint64_t>(2ull * (uint64_t)sms, g.n / 32));
+    // tile partial sums, and before them the rotation's scratch (one 32 x 33 tile per rotating warp)
+    const uint32_t nrot = std::min<uint32_t>((uint32_t)((g.k + 1023) / 1024), kRotWarps);
+    const uint32_t part_bytes = std::max<uint32_t>(kWarps * kRows * 4, nrot * kRotScratch);
+    const uint32_t bar_bytes = kMaxSlots * 8;
+    const uint32_t cnt_bytes = (kMaxSlots + 4) * 4;
+    const uint32_t fixed = act_bytes + part_bytes + bar_bytes + cnt_bytes;
+    if ((int)fixed + 2 * (int)kItemBytes > smem_limit) return false;
+    const uint32_t nslots = std::min<uint32_t>(kMaxSlots, (uint32_t)((smem_limit - (int)fixed) / (int)kItemBytes));
+    // one CTA per SM with ~n / SMs rows each
+    const uint64_t grid0 = std::max<uint64_t>(1, std::min<uint64_t>((uint64_t)sms, g.n / 64));
     const uint64_t R = (g.n + grid0 - 1) / grid0;
     const uint64_t grid = (g.n + R - 1) / R;
     plan->ok = true;
     plan->grid = (uint32_t)grid;
     plan->rows_per_cta = (uint32_t)R;
-    plan->nbox = nbox;
+    plan->nitem = (groups + 7) / 8;
     plan->nslots = nslots;
-    plan->pre_issue = nslots;      // the whole ring before the dependency wait
-    plan->act_bytes = act_bytes;
+    plan->pre_issue = std::min<uint32_t>(1, nslots);
     plan->off_ring = 0;
     plan->off_act = nslots * kItemBytes;
     plan->off_part = plan->off_act + act_bytes;
     plan->off_bar = plan->off_part + part_bytes;
     plan->off_cnt = plan->off_bar + bar_bytes;
-    plan->smem = plan->off_cnt + kMaxSlots * 4;
-    plan->workspace = act_prep_int16_row_bytes(g.k_pad) * kActCopies;
+    plan->smem = plan->off_cnt + cnt_bytes;
+    plan->workspace = 0;
     return true;
 }
 
 int gemv_pq2_int_launch(const IntPlan &plan, const uint8_t *payload, const ninfer_row_split_geometry &g, const void *x,
-                        int x_dtype, const uint16_t *signs, void *y, int y_dtype, void *workspace, cudaStream_t stream,
-                        bool pdl) {
-    int st = act_prep_int16_launch(x, x_dtype, signs, g.k, g.k_pad, 1, kActCopies, static_cast<uint8_t *>(workspace),
-                                   stream, pdl);
-    if (st) return st;
+                        int x_dtype, const uint16_t *signs, void *y, int y_dtype, cudaStream_t stream, bool pdl) {
     IntParams p;
     std::memset(&p, 0, sizeof p);
     const uint8_t *base = payload + g.base_offset, *scale = payload + g.scale_offset;
-    p.act = static_cast<const uint8_t *>(workspace);
-    p.act_copy_stride = act_prep_int16_row_bytes(g.k_pad);
+    p.x = x;
+    p.signs = signs;
     p.y = y;
     p.n = g.n;
+    p.k = (uint32_t)g.k;
     p.groups = (uint32_t)g.groups_per_row;
-    p.nbox = plan.nbox;
+    p.nblk = (uint32_t)((g.k + 1023) / 1024);
+    p.nitem = plan.nitem;
     p.rows_per_cta = plan.rows_per_cta;
+    p.x_dtype = x_dtype;
     p.y_dtype = y_dtype;
     p.nslots = plan.nslots;
     p.pre_issue = plan.pre_issue;
-    p.act_bytes = plan.act_bytes;
     p.off_ring = plan.off_ring;
     p.off_act = plan.off_act;
     p.off_part = plan.off_part;
     p.off_bar = plan.off_bar;
     p.off_cnt = plan.off_cnt;
-    st = device_error_word(&p.err);
+    int st = device_error_word(&p.err);
     if (st) return st;
     const uint64_t R = plan.rows_per_cta, G = plan.grid, last_rows = g.n - (G - 1) * R;
     if (G > 1) {
-        st = encode_rows(&p.wmap_main, base, g.base_row_bytes, R, G - 1, 128, 32, true);
-        if (!st) st = encode_rows(&p.smap_main, scale, g.scale_row_bytes, R, G - 1, 16, 32, false);
+        st = encode_rows(&p.wmap_main, base, g.base_row_bytes, R, G - 1, 128, kRows, true);
+        if (!st) st = encode_rows(&p.smap_main, scale, g.scale_row_bytes, R, G - 1, 16, kRows, false);
         if (st) return st;
     }
-    st = encode_rows(&p.wmap_last, base + (G - 1) * R * g.base_row_bytes, g.base_row_bytes, last_rows, 1, 128, 32, true);
+    st = encode_rows(&p.wmap_last, base + (G - 1) * R * g.base_row_bytes, g.base_row_bytes, last_rows, 1, 128, kRows,
+                     true);
     if (!st)
-        st = encode_rows(&p.smap_last, scale + (G - 1) * R * g.scale_row_bytes, g.scale_row_bytes, last_rows, 1, 16, 32,
-                         false);
+        st = encode_rows(&p.smap_last, scale + (G - 1) * R * g.scale_row_bytes, g.scale_row_bytes, last_rows, 1, 16,
+                         kRows, false);
     if (st) return st;
     cudaError_t e = cudaFuncSetAttribute(gemv_pq2_int_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.smem);
     if (e != cudaSuccess) return fail(NINFER_ERR_CUDA, "gemv: smem attribute: %s", cudaGetErrorString(e));

@@ -54,7 +54,7 @@ int plan_matmul(int fmt, const ninfer_row_split_geometry &g, uint64_t M, bool ro
     mp->workspace = 0;
     if (fmt == NINFER_PQ2_0_G128 && gemv_pq2_int_plan(g, M, rotate, d.sms, d.smem_optin, &mp->gint)) {
         mp->path = Path::kIntPq2;
-        mp->workspace = mp->gint.workspace;     // the prepared activation
+        mp->workspace = mp->gint.workspace;     // none: each CTA rotates x itself
         return NINFER_OK;
     }
     if (fmt == NINFER_PQ2_0_G128 && gemv_pq2_plan(g, M, rotate, d.sms, d.smem_optin, &mp->gemv)) {
@@ -119,7 +119,7 @@ extern "C" int ninfer_ternary_matmul(int fmt, const uint8_t *payload, uint64_t p
     if (need && !aligned(workspace, 16)) return fail(NINFER_ERR_ALIGNMENT, "matmul: workspace must be 16-byte aligned");
     cudaStream_t s = (cudaStream_t)stream;
     if (mp.path == Path::kIntPq2)
-        return gemv_pq2_int_launch(mp.gint, payload, g, x, x_dtype, signs_bf16, y, y_dtype, workspace, s, g_pdl);
+        return gemv_pq2_int_launch(mp.gint, payload, g, x, x_dtype, signs_bf16, y, y_dtype, s, g_pdl);
     if (mp.path == Path::kFusedPq2)
         return gemv_pq2_launch(mp.gemv, payload, g, x, x_dtype, signs_bf16, y, y_dtype, M, s, g_pdl);
     const PlaneView p = make_view(payload, g, fmt);
