@@ -10,7 +10,7 @@ namespace ninfer {
 
 // Bits of the library's device error word (read and cleared by
 // ninfer_device_errors()); kernels receive its address as a parameter.
-enum : uint32_t { kErrBarrierTimeout = 1u };
+enum : uint32_t { kErrBarrierTimeout = 1u, kErrSmemAlign = 2u };
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -30,6 +30,10 @@ __device__ __forceinline__ void fence_proxy_async() {
 
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
 // global -> shared bulk copy completing on an mbarrier (dst, src, size 16-byte aligned).

@@ -1,0 +1,352 @@
+// Prefill projection for PQ2_0_G128 (M > 8 activation rows) on the 5th-generation
+// tensor cores: tcgen05.mma kind::f16, fp32 accumulators in tensor memory.
+//
+// What it computes:
+//   y[m][r] = sum_c W[r][c] * xr[m][c],  W[r][c] = (code[r][c] - 1) * scale[r][c / 128]
+// with xr the forward-rotated activation (per 1024-block H (D * x) / 32,
+// "artifact-container.md" §8 hadamard_signs; TensorSharp article §4.2), codes the
+// 2-bit fields of the base plane, least significant first, value = code - 1
+// ("GGUF 完整讲解" §4.3), one binary16 scale per 128-weight group
+// ("bonsai三元GGUF模型转ninfer模型01" §3).
+//
+// Precision: xr is rounded to binary16 once; W = (code - 1) * scale is exact in
+// binary16 (a small integer times a binary16 value); products are exact and
+// accumulate in fp32.
+//
+// Two kernels:
+//  * tc_prep_kernel writes xr as binary16, one warp per (row, 1024-block). Inside
+//    every run of 16 elements it stores the order 0,8,1,9,...,7,15, which is the
+//    order in which one 32-bit word of codes decodes with one mask per pair
+//    (codes j and j+8 sit at bits 2j and 2j+16).
+//  * gemm_tc_kernel computes one 128 (tokens) x 128 (weight rows) output tile per
+//    CTA, two CTAs per SM, K in stages of 64:
+//      warp 0       TMA producer: xr tile (128 x 64 binary16, 128-byte swizzle),
+//                   the tile's 64 codes per weight row (16 bytes) and the 8
+//                   scales that cover them (16 bytes);
+//      warp 1       TMEM owner and MMA issuer (one thread): four K=16 MMAs per stage;
+//      warps 2..5   decode: thread t expands weight row t's 64 codes to binary16
+//                   (code - 1) * scale and writes them in the canonical K-major
+//                   128-byte-swizzled layout; after the K loop they read the
+//                   accumulators out of tensor memory and store y.
+//    Stages are handed over with mbarriers (TMA transaction counts, 128 decoder
+//    arrivals, and tcgen05.commit for "stage consumed"); every wait is bounded.
+#include <cstring>
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "async.cuh"
+#include "common.h"
+#include "device.cuh"
+#include "gemv.h"
+
+namespace ninfer {
+namespace {
+
+constexpr int kBM = 128, kBN = 128, kBK = 64;      // tokens, weight rows, k per stage
+constexpr int kStages = 3;
+constexpr uint32_t kABytes = kBM * kBK * 2;        // 16 KB of xr
+constexpr uint32_t kBBytes = kBN * kBK * 2;        // 16 KB of expanded weights
+constexpr uint32_t kCodeBytes = kBN * 16;          // 64 codes per weight row
+constexpr uint32_t kScaleBytes = kBN * 16;         // 8 scales per weight row
+constexpr uint32_t kStageBytes = kABytes + kBBytes + kCodeBytes + kScaleBytes;     // 36 KB, 1024-aligned
+constexpr uint32_t kBarBytes = 8 * (3 * kStages + 1);
+constexpr uint32_t kSmemBytes = ((kStages * kStageBytes + kBarBytes + 16 + 1023) / 1024) * 1024;
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 128;                // fp32 accumulators, one column per weight row
+
+struct TcParams {
+    CUtensorMap amap, cmap, smap;
+    void *y;
+    uint64_t M, n;
+    uint32_t nk;
+    int y_dtype;
+    uint32_t *err;
+};
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle (8-row atoms of
+// 1024 bytes), start address in 16-byte units.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | (1ull << 16) | ((uint64_t)(1024 >> 4) << 32) | (1ull << 46) |
+           (2ull << 61);
+}
+
+// Instruction descriptor of kind::f16: fp32 D, binary16 A and B, both K-major, M = 128, N = 128.
+constexpr uint32_t kIdesc = (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+
+__device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(tmem_d),
+        "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 32 consecutive fp32 accumulator columns of this warp's 32 TMEM lanes.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+          "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Codes j and j+8 of a 32-bit code word as a binary16 pair ((c - 1) * s):
+// OR-ing 0x6400 (1024.0) over a 2-bit code gives 1024 + c exactly.
+__device__ __forceinline__ uint32_t expand_pair(uint32_t w, int j, __half2 s2) {
+    uint32_t u = ((w >> (2 * j)) & 0x00030003u) | 0x64006400u;
+    __half2 h = *reinterpret_cast<__half2 *>(&u);
+    h = __hmul2(__hsub2(h, __float2half2_rn(1025.f)), s2);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+__global__ void __launch_bounds__(128) tc_prep_kernel(const void *__restrict__ x, int x_dtype,
+                                                      const uint16_t *__restrict__ signs, __half *__restrict__ out,
+                                                      uint64_t M, uint64_t K) {
+    const uint64_t nblk = K / 1024;
+    const uint64_t task = (uint64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
+    if (task >= M * nblk) return;
+    const int lane = threadIdx.x & 31;
+    const uint64_t m = task / nblk, b = task % nblk;
+    const uint64_t row = m * K, col0 = b * 1024;
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float t[8];
+        const uint64_t c = col0 + 256 * i + 8 * lane;
+        load8(x, row + c, x_dtype, t);
+        if (signs) {
+            float d[8];
+            load_signs8(signs, c, d);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) t[e] *= d[e];
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[8 * i + e] = t[e];
+    }
+    if (signs) {
+        wht1024_warp(v, lane);
+#pragma unroll
+        for (int r = 0; r < 32; ++r) v[r] *= 0.03125f;
+    }
+    // lane holds elements 8*lane + e of each 256-run: half h = lane & 1 of the
+    // 16-element run 16i + lane/2. Output order in the run: 0,8,1,9,...,7,15.
+    const int h = lane & 1;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float send[4], other[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) send[q] = h ? v[8 * i + q] : v[8 * i + 4 + q];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) other[q] = __shfl_xor_sync(0xffffffffu, send[q], 1);
+        uint32_t pk[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            // h = 0: (old q, old q + 8); h = 1: (old 4 + q, old 12 + q)
+            const float lo = h ? other[q] : v[8 * i + q];
+            const float hi = h ? v[8 * i + 4 + q] : other[q];
+            __half2 p2 = __floats2half2_rn(lo, hi);
+            pk[q] = *reinterpret_cast<uint32_t *>(&p2);
+        }
+        const uint64_t dst = row + col0 + 256 * i + 8 * lane;     // = run start + 8h
+        *reinterpret_cast<uint4 *>(out + dst) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 2) gemm_tc_kernel(const __grid_constant__ TcParams p) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t base = smem_u32(smem);
+    if (base & 1023) {         // the swizzled tiles need 1024-byte alignment: report, touch nothing
+        if (tid == 0) atomicOr(p.err, kErrSmemAlign);
+        return;
+    }
+    const uint32_t bar = base + kStages * kStageBytes;
+    const uint32_t accum_bar = bar + 8 * 3 * kStages;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kStages * kStageBytes + kBarBytes);
+    const uint64_t n0 = (uint64_t)blockIdx.x * kBN, m0 = (uint64_t)blockIdx.y * kBM;
+    // full_a[s]: xr, codes and scales landed; full_b[s]: weights expanded; empty[s]: stage consumed
+#define FULL_A(s) (bar + 8 * (s))
+#define FULL_B(s) (bar + 8 * (kStages + (s)))
+#define EMPTY(s) (bar + 8 * (2 * kStages + (s)))
+
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    if (tid == 0) {
+        prefetch_tmap(&p.amap);
+        prefetch_tmap(&p.cmap);
+        prefetch_tmap(&p.smap);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(FULL_A(s), 1);
+            mbar_init(FULL_B(s), 128);
+            mbar_init(EMPTY(s), 1);
+        }
+        mbar_init(accum_bar, 1);
+        fence_mbar_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            for (uint32_t kt = 0; kt < p.nk; ++kt) {
+                const uint32_t s = kt % kStages, round = kt / kStages;
+                if (round > 0 && !mbar_wait(EMPTY(s), (round - 1) & 1, p.err)) break;
+                const uint32_t st = base + s * kStageBytes;
+                mbar_arrive_expect_tx(FULL_A(s), kABytes + kCodeBytes + kScaleBytes);
+                tma_load_2d(st, &p.amap, (int)(kt * kBK), (int)m0, FULL_A(s));
+                tma_load_2d(st + kABytes + kBBytes, &p.cmap, (int)(kt * 16), (int)n0, FULL_A(s));
+                tma_load_2d(st + kABytes + kBBytes + kCodeBytes, &p.smap, (int)((kt / 16) * 16), (int)n0, FULL_A(s));
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            for (uint32_t kt = 0; kt < p.nk; ++kt) {
+                const uint32_t s = kt % kStages, par = (kt / kStages) & 1;
+                if (!mbar_wait(FULL_A(s), par, p.err) || !mbar_wait(FULL_B(s), par, p.err)) break;
+                tc_fence_after();
+                const uint32_t st = base + s * kStageBytes;
+                const uint64_t adesc = sw128_desc(st), bdesc = sw128_desc(st + kABytes);
+#pragma unroll
+                for (int kk = 0; kk < kBK / 16; ++kk)      // +32 bytes along K per MMA (16-byte units: +2)
+                    mma_f16(tmem, adesc + 2 * kk, bdesc + 2 * kk, (kt | kk) != 0);
+                mma_commit(EMPTY(s));
+            }
+            mma_commit(accum_bar);
+        }
+    } else {
+        const int t = tid - 64;     // weight row of the tile
+        for (uint32_t kt = 0; kt < p.nk; ++kt) {
+            const uint32_t s = kt % kStages, par = (kt / kStages) & 1;
+            if (!mbar_wait(FULL_A(s), par, p.err)) break;
+            uint8_t *st = smem + s * kStageBytes;
+            const uint4 cw = *reinterpret_cast<const uint4 *>(st + kABytes + kBBytes + t * 16);
+            const __half sc =
+                *reinterpret_cast<const __half *>(st + kABytes + kBBytes + kCodeBytes + t * 16 + 2 * ((kt / 2) % 8));
+            const __half2 s2 = __halves2half2(sc, sc);
+            uint8_t *brow = st + kABytes + t * 128;
+            const uint32_t w[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint4 o;
+                    o.x = expand_pair(w[i], 4 * hh + 0, s2);
+                    o.y = expand_pair(w[i], 4 * hh + 1, s2);
+                    o.z = expand_pair(w[i], 4 * hh + 2, s2);
+                    o.w = expand_pair(w[i], 4 * hh + 3, s2);
+                    *reinterpret_cast<uint4 *>(brow + ((((2 * i + hh) ^ (t & 7))) << 4)) = o;
+                }
+            fence_proxy_async();      // generic-proxy writes, read by the tensor core
+            mbar_arrive(FULL_B(s));
+        }
+        // epilogue: TMEM lanes 32q .. 32q + 31 are this warp's token rows
+        const bool done = __all_sync(0xffffffffu, mbar_wait(accum_bar, 0, p.err));
+        tc_fence_after();
+        const uint32_t q = warp & 3;
+        const uint64_t m = m0 + 32 * q + lane;
+        if (done) {
+#pragma unroll 1
+            for (int cb = 0; cb < kBN / 32; ++cb) {
+                float v[32];
+                tmem_ld32(tmem + ((32 * q) << 16) + 32 * cb, v);
+                const uint64_t nc = n0 + 32 * cb;
+                if (m >= p.M || nc >= p.n) continue;
+                const uint64_t off = m * p.n + nc;
+                const bool full = nc + 32 <= p.n;
+                if (p.y_dtype == NINFER_F32) {
+                    float *yp = static_cast<float *>(p.y) + off;
+                    if (full && (off % 4) == 0) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            reinterpret_cast<float4 *>(yp)[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                    } else {
+                        for (int i = 0; i < 32 && nc + i < p.n; ++i) yp[i] = v[i];
+                    }
+                } else {
+                    for (int i = 0; i < 32 && nc + i < p.n; ++i) store1(p.y, off + i, p.y_dtype, v[i]);
+                }
+            }
+        }
+    }
+#undef FULL_A
+#undef FULL_B
+#undef EMPTY
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+    }
+}
+
+}  // namespace
+
+bool gemm_tc_plan(const ninfer_row_split_geometry &g, uint64_t M, int smem_limit, TcPlan *plan) {
+    *plan = TcPlan{};
+    if (M < 9 || g.k % 1024 || g.k > (1u << 24)) return false;
+    if (g.scale_row_bytes % 16 || g.base_row_bytes % 16) return false;
+    if ((int)kSmemBytes > smem_limit) return false;
+    const uint64_t gm = (M + kBM - 1) / kBM, gn = (g.n + kBN - 1) / kBN;
+    if (gm > 65535 || gn > 0x7fffffffull) return false;
+    plan->ok = true;
+    plan->grid_n = (uint32_t)gn;
+    plan->grid_m = (uint32_t)gm;
+    plan->smem = kSmemBytes;
+    plan->workspace = M * g.k * 2;      // xr, binary16
+    return true;
+}
+
+int gemm_tc_launch(const TcPlan &plan, const uint8_t *payload, const ninfer_row_split_geometry &g, const void *x,
+                   int x_dtype, const uint16_t *signs, void *y, int y_dtype, uint64_t M, void *workspace,
+                   cudaStream_t stream) {
+    __half *xr = static_cast<__half *>(workspace);
+    const uint64_t tasks = M * (g.k / 1024), pgrid = (tasks + 3) / 4;
+    if (pgrid > 0x7fffffffull) return fail(NINFER_ERR_SHAPE, "prefill: too many rows");
+    tc_prep_kernel<<<(unsigned)pgrid, 128, 0, stream>>>(x, x_dtype, signs, xr, M, g.k);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(NINFER_ERR_CUDA, "prefill prep launch: %s", cudaGetErrorString(e));
+    TcParams p;
+    std::memset(&p, 0, sizeof p);
+    p.y = y;
+    p.M = M;
+    p.n = g.n;
+    p.nk = (uint32_t)(g.k / kBK);
+    p.y_dtype = y_dtype;
+    int st = device_error_word(&p.err);
+    if (st) return st;
+    st = encode_2d(&p.amap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, xr, g.k, M, g.k * 2, kBK, kBM, true);
+    if (!st) st = encode_rows(&p.cmap, payload + g.base_offset, g.base_row_bytes, g.n, 1, 16, kBN, false);
+    if (!st) st = encode_rows(&p.smap, payload + g.scale_offset, g.scale_row_bytes, g.n, 1, 16, kBN, false);
+    if (st) return st;
+    e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.smem);
+    if (e != cudaSuccess) return fail(NINFER_ERR_CUDA, "prefill: smem attribute: %s", cudaGetErrorString(e));
+    gemm_tc_kernel<<<dim3(plan.grid_n, plan.grid_m), kThreads, plan.smem, stream>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(NINFER_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
+    return NINFER_OK;
+}
+
+}  // namespace ninfer

@@ -29,6 +29,11 @@ int device_error_word(uint32_t **out);
 int encode_rows(CUtensorMap *map, const uint8_t *addr, uint64_t row_bytes, uint64_t rows, uint64_t ctas,
                 uint32_t box_bytes, uint32_t box_rows, bool swizzle128);
 
+// A 2-D tensor map over a row-major array: `inner` elements per row, `outer`
+// rows, rows `row_stride_bytes` apart; boxes of box_inner x box_outer.
+int encode_2d(CUtensorMap *map, CUtensorMapDataType dtype, uint32_t elem_bytes, const void *addr, uint64_t inner,
+              uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer, bool swizzle128);
+
 // M = 1 integer kernel (PQ2_0_G128), rotation fused in.
 struct IntPlan {
     bool ok;
@@ -46,5 +51,16 @@ bool gemv_pq2_plan(const ninfer_row_split_geometry &g, uint64_t M, bool rotate, 
 int gemv_pq2_launch(const GemvPlan &plan, const uint8_t *payload, const ninfer_row_split_geometry &g, const void *x,
                     int x_dtype, const uint16_t *signs, void *y, int y_dtype, uint64_t M, cudaStream_t stream,
                     bool pdl);
+
+// Prefill (M > 8) tensor-core path for PQ2_0_G128 (gemm_tc.cu).
+struct TcPlan {
+    bool ok;
+    uint32_t grid_n, grid_m, smem;
+    uint64_t workspace;
+};
+bool gemm_tc_plan(const ninfer_row_split_geometry &g, uint64_t M, int smem_limit, TcPlan *plan);
+int gemm_tc_launch(const TcPlan &plan, const uint8_t *payload, const ninfer_row_split_geometry &g, const void *x,
+                   int x_dtype, const uint16_t *signs, void *y, int y_dtype, uint64_t M, void *workspace,
+                   cudaStream_t stream);
 
 }  // namespace ninfer

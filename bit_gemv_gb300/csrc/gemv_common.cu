@@ -68,6 +68,24 @@ int encode_rows(CUtensorMap *map, const uint8_t *addr, uint64_t row_bytes, uint6
     return NINFER_OK;
 }
 
+int encode_2d(CUtensorMap *map, CUtensorMapDataType dtype, uint32_t elem_bytes, const void *addr, uint64_t inner,
+              uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer, bool swizzle128) {
+    EncodeTiledFn fn;
+    int st = encode_fn(&fn);
+    if (st) return st;
+    std::memset(map, 0, sizeof *map);
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {row_stride_bytes};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    (void)elem_bytes;
+    CUresult r = fn(map, dtype, 2, const_cast<void *>(addr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(NINFER_ERR_CUDA, "tensor map encode failed (CUresult %d)", (int)r);
+    return NINFER_OK;
+}
+
 }  // namespace ninfer
 
 extern "C" int ninfer_device_errors(uint32_t *out, int clear) {

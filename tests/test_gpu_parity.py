@@ -138,6 +138,24 @@ def test_embed_head_rows(head_case):
     assert oracle.max_rel_error(out.cpu().numpy(), ref) <= TOL_DECODE
 
 
+@pytest.mark.parametrize("preset,n,k,M", [("prefill", 300, 1024, 200), ("prefill", 129, 2048, 130),
+                                           ("tiny", 256, 1024, 17), ("prefill", 1000, 5120, 300)])
+def test_matmul_prefill_small(preset, n, k, M):
+    """Tensor-core prefill path: partial token and weight-row tiles, fp32 and
+    bf16 activations, every output compared."""
+    c = synth.make_case(preset, n=n, k=k, M=M, seed=n + k + M)
+    y = run_matmul("PQ2_0_G128", c)
+    ref = oracle_matmul_rows("PQ2_0_G128", c, np.arange(n))
+    assert oracle.max_rel_error(y, ref) <= TOL_PREFILL
+
+
+def test_matmul_prefill_unrotated_bf16_out():
+    c = synth.make_case("prefill", n=256, k=2048, M=64, seed=11)
+    y = run_matmul("PQ2_0_G128", c, rotate=False, y_dtype=torch.bfloat16)
+    ref = oracle_matmul_rows("PQ2_0_G128", c, np.arange(256), rotate=False)
+    assert oracle.max_rel_error(y, ref) <= TOL_PREFILL
+
+
 @pytest.mark.slow
 def test_matmul_prefill_sampled():
     c = synth.make_case("prefill")
