@@ -274,11 +274,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_pq2_int_kernel(const __grid_
     const uint32_t ch = ((2 * gi + half) ^ (lane & 7)) << 4;
     const float2 *gs = reinterpret_cast<const float2 *>(act_s + p.groups * 256);
     float *part = reinterpret_cast<float *>(smem + p.off_part);
+    const bool refill = nitems > p.nslots;    // otherwise the whole slice sits in the ring
+    uint32_t slot = 0, phase = 0, item = 0;
     for (uint32_t tile = 0; tile < ntile; ++tile) {
         float y[4] = {0.f, 0.f, 0.f, 0.f};      // rows lane + 32q of the tile
-        for (uint32_t j = 0; j < p.nitem; ++j) {
-            const uint32_t item = tile * p.nitem + j, slot = item % p.nslots;
-            ok = ok && mbar_wait(bar0 + 8 * slot, (item / p.nslots) & 1, p.err);
+        for (uint32_t j = 0; j < p.nitem; ++j, ++item) {
+            ok = ok && mbar_wait(bar0 + 8 * slot, phase, p.err);
             const uint32_t G = j * 8 + gw;
             if (ok && G < p.groups) {
                 const uint8_t *sa = smem + p.off_ring + slot * kItemBytes;
@@ -318,20 +319,29 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_pq2_int_kernel(const __grid_
                     y[q] = fmaf(s * f.x, (float)t, y[q]);
                 }
             }
-            // release the slot; the last of the sixteen readers re-arms it with item + nslots
-            __syncwarp();
-            if (lane == 0) {
-                if (!ok) *failed = 1;
-                __threadfence_block();
-                const uint32_t seen = atomicAdd(&cnt[slot], 1u);
-                if (seen == kWarps - 1) {
-                    cnt[slot] = 0;
-                    if (ok && !*(volatile uint32_t *)failed && item + p.nslots < nitems) {
-                        fence_proxy_async();
-                        issue_item(p, smem, item + p.nslots, last_cta);
-                        atomicAdd(issued, 1u);
+            if (refill) {
+                // release the slot; the last of the sixteen readers re-arms it with item + nslots
+                __syncwarp();
+                if (lane == 0) {
+                    if (!ok) *failed = 1;
+                    __threadfence_block();
+                    const uint32_t seen = atomicAdd(&cnt[slot], 1u);
+                    if (seen == kWarps - 1) {
+                        cnt[slot] = 0;
+                        if (ok && !*(volatile uint32_t *)failed && item + p.nslots < nitems) {
+                            fence_proxy_async();
+                            issue_item(p, smem, item + p.nslots, last_cta);
+                            atomicAdd(issued, 1u);
+                        }
                     }
                 }
+                __syncwarp();
+            } else if (!ok && lane == 0) {
+                *failed = 1;
+            }
+            if (++slot == p.nslots) {
+                slot = 0;
+                phase ^= 1u;
             }
         }
 #pragma unroll
