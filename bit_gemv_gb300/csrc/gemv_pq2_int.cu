@@ -54,7 +54,7 @@ constexpr int kRows = 128;        // rows per tile, four per lane
 constexpr uint32_t kBoxBytes = 128 * kRows;              // one 128-byte column of the tile
 constexpr uint32_t kItemBytes = 2 * kBoxBytes + 16 * kRows;
 constexpr uint32_t kMaxSlots = 8;
-constexpr uint32_t kRotWarps = 8;     // warps that rotate x (one 1024-block at a time each)
+constexpr uint32_t kRotPairs = 8;     // warp pairs that rotate x (one 1024-block at a time each)
 
 struct IntParams {
     CUtensorMap wmap_main, wmap_last;   // base rows: {row bytes, R rows, CTA} / last CTA {row bytes, rows}
@@ -100,20 +100,51 @@ __device__ __forceinline__ void issue_item(const IntParams &p, uint8_t *smem, ui
     }
 }
 
-// Activation preparation, one warp per 1024-block, 32 elements per lane. Pass
-// 1: lane l holds elements 32l + r and butterflies index bits 0-4 in registers.
-// A transpose through a padded 32 x 33 float tile (conflict-free both ways)
-// gives lane c the elements 32j + c, and pass 2 butterflies bits 5-9. The
-// quantised values go through the same scratch as int16 in natural order, so
-// that each lane can read 16-byte runs of eight consecutive elements for the
-// operand words.
-constexpr uint32_t kRotScratch = 32 * 33 * 4;      // bytes per rotating warp
+// Activation preparation, two warps (64 threads) per 1024-block, 16 elements
+// per thread, in three register passes over index bits 0-3, 4-7 and 8-9 with
+// transposes through a padded float tile between them (element e at e + e/16,
+// conflict-free for the first two layouts). The quantised values go through
+// the same scratch as int16 in natural order, so that each thread reads
+// 16-byte runs of eight consecutive elements for the operand words.
+constexpr uint32_t kRotScratch = (1024 + 64) * 4 + 16;     // bytes per rotating warp pair
 
-__device__ __forceinline__ void butterfly32(float (&v)[32]) {
+__device__ __forceinline__ int pad16(int e) { return e + (e >> 4); }
+
+// x (times the signs) of block b: thread t (0..63) gets elements 16t .. 16t + 15 (zero past k).
+__device__ __forceinline__ void load_run16(const IntParams &p, uint32_t b, int t, float (&v)[16]) {
+    const uint64_t e0 = (uint64_t)b * 1024 + 16 * t;
 #pragma unroll
-    for (int bit = 0; bit < 5; ++bit)
+    for (int i = 0; i < 2; ++i) {
+        float u[8];
+        const uint64_t idx = e0 + 8 * i;
+        if (idx + 8 <= p.k) {
+            load8(p.x, idx, p.x_dtype, u);
+        } else {
 #pragma unroll
-        for (int r = 0; r < 32; ++r) {
+            for (int e = 0; e < 8; ++e) u[e] = idx + e < p.k ? load1(p.x, idx + e, p.x_dtype) : 0.f;
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[8 * i + e] = u[e];
+    }
+}
+
+__device__ __forceinline__ void load_signs16(const IntParams &p, uint32_t b, int t, float (&d)[16]) {
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        float u[8];
+        load_signs8(p.signs, (uint64_t)b * 1024 + 16 * t + 8 * i, u);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) d[8 * i + e] = u[e];
+    }
+}
+
+// Butterflies over register index bits lo .. lo + nbits - 1 of 16 values.
+template <int kLo, int kBits>
+__device__ __forceinline__ void butterfly16(float (&v)[16]) {
+#pragma unroll
+    for (int bit = kLo; bit < kLo + kBits; ++bit)
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
             if (r & (1 << bit)) continue;
             const float a0 = v[r], a1 = v[r | (1 << bit)];
             v[r] = a0 + a1;
@@ -121,75 +152,68 @@ __device__ __forceinline__ void butterfly32(float (&v)[32]) {
         }
 }
 
-// x (times the signs) of block b: lane l gets elements 32l .. 32l + 31 (zero past k).
-__device__ __forceinline__ void load_block(const IntParams &p, uint32_t b, int lane, float (&v)[32]) {
-    const uint64_t e0 = (uint64_t)b * 1024 + 32 * lane;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        float t[8];
-        const uint64_t idx = e0 + 8 * i;
-        if (idx + 8 <= p.k) {
-            load8(p.x, idx, p.x_dtype, t);
-        } else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) t[e] = idx + e < p.k ? load1(p.x, idx + e, p.x_dtype) : 0.f;
-        }
-#pragma unroll
-        for (int e = 0; e < 8; ++e) v[8 * i + e] = t[e];
-    }
-}
-
-__device__ __forceinline__ void load_block_signs(const IntParams &p, uint32_t b, int lane, float (&d)[32]) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        float t[8];
-        load_signs8(p.signs, (uint64_t)b * 1024 + 32 * lane + 8 * i, t);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) d[8 * i + e] = t[e];
-    }
-}
-
 // Rotates and quantises block b (x in v, signs in d) and writes its dp2a
 // operand words and group entries to shared memory:
 //   act[word][4h + p] = (x16[16 word + 8h + p], x16[16 word + 8h + 4 + p]),
 //   gs[group] = {2^-E, sum of the group's x16 (as int bits)},
-// x16 = rint(xr * 2^E), E per block so that max |x16| < 2^14.
-__device__ __forceinline__ void prepare_block(const IntParams &p, uint8_t *act_s, uint32_t b, int lane,
-                                              float (&v)[32], const float (&d)[32], float *tile) {
+// x16 = rint(xr * 2^E), E per block so that max |x16| < 2^14. t = thread of
+// the pair (0..63), bar = the pair's named barrier.
+__device__ __forceinline__ void prepare_block(const IntParams &p, uint8_t *act_s, uint32_t b, int t, float (&v)[16],
+                                              const float (&d)[16], float *tile, uint32_t bar) {
     const bool rotate = p.signs != nullptr;
+    const int lane = t & 31;
+    float *pmax = tile + 1024 + 64;
     if (rotate) {
 #pragma unroll
-        for (int r = 0; r < 32; ++r) v[r] *= d[r];
-        butterfly32(v);                       // index bits 0-4
+        for (int r = 0; r < 16; ++r) v[r] *= d[r];
+        butterfly16<0, 4>(v);                                    // bits 0-3: elements 16t + r
+#pragma unroll
+        for (int r = 0; r < 16; ++r) tile[17 * t + r] = v[r];      // pad16(16t + r)
+        named_barrier(bar, 64);
+        // bits 4-7: thread t = (hi2, lo4) takes elements 256 hi2 + 16 r + lo4
+        const int hi2 = t >> 4, lo4 = t & 15;
+#pragma unroll
+        for (int r = 0; r < 16; ++r) v[r] = tile[272 * hi2 + 17 * r + lo4];
+        butterfly16<0, 4>(v);
+#pragma unroll
+        for (int r = 0; r < 16; ++r) tile[272 * hi2 + 17 * r + lo4] = v[r];
+        named_barrier(bar, 64);
+        // bits 8-9: thread t takes elements 256 a + 4t + c (a = r / 4, c = r % 4)
+#pragma unroll
+        for (int r = 0; r < 16; ++r) v[r] = tile[pad16(256 * (r >> 2) + 4 * t + (r & 3))];
+        butterfly16<2, 2>(v);                                    // register bits 2-3 = element bits 8-9
+#pragma unroll
+        for (int r = 0; r < 16; ++r) v[r] *= 0.03125f;
+    } else {
+#pragma unroll
+        for (int r = 0; r < 16; ++r) tile[17 * t + r] = v[r];
+        named_barrier(bar, 64);
+#pragma unroll
+        for (int r = 0; r < 16; ++r) v[r] = tile[pad16(256 * (r >> 2) + 4 * t + (r & 3))];
     }
-#pragma unroll
-    for (int r = 0; r < 32; ++r) tile[r * 33 + lane] = v[r];     // element 32 lane + r
-    __syncwarp();
-#pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] = tile[lane * 33 + j];     // element 32 j + lane
-    if (rotate) butterfly32(v);               // index bits 5-9; v = 32 * xr
     float mx = 0.f;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) mx = fmaxf(mx, fabsf(v[j]));
+    for (int r = 0; r < 16; ++r) mx = fmaxf(mx, fabsf(v[r]));
 #pragma unroll
     for (int s = 16; s > 0; s >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, s));
-    int ev = 0;                               // max |v * 2^ev| < 2^14
-    if (mx > 0.f) ev = 13 - ilogbf(mx);
-    ev = max(-100, min(100, ev));
-    const float up = ldexpf(1.f, ev);
-    const int E = rotate ? ev + 5 : ev;       // x16 = xr * 2^E (xr = v / 32 when rotated)
-    __syncwarp();                             // every lane has read the tile
+    if (lane == 0) pmax[t >> 5] = mx;
+    named_barrier(bar, 64);      // also: every thread has read its tile values
+    mx = fmaxf(pmax[0], pmax[1]);
+    int E = 0;
+    if (mx > 0.f) E = 13 - ilogbf(mx);     // max |x16| < 2^14
+    E = max(-100, min(100, E));
+    const float up = ldexpf(1.f, E);
     int16_t *qs = reinterpret_cast<int16_t *>(tile);
 #pragma unroll
-    for (int j = 0; j < 32; ++j)              // adding 1.5 * 2^23 rounds to nearest, ties to even
-        qs[32 * j + lane] = (int16_t)(__float_as_int(fmaf(v[j], up, 12582912.0f)) - 0x4B400000);
-    __syncwarp();
-    // 128 runs of eight elements; lane takes runs lane + 32i (operand word run/2, half run&1)
+    for (int r = 0; r < 16; ++r)           // adding 1.5 * 2^23 rounds to nearest, ties to even
+        qs[256 * (r >> 2) + 4 * t + (r & 3)] = (int16_t)(__float_as_int(fmaf(v[r], up, 12582912.0f)) - 0x4B400000);
+    named_barrier(bar, 64);
+    // 128 runs of eight elements; thread t takes runs t and t + 64 (operand word run/2, half run&1)
     uint4 *act = reinterpret_cast<uint4 *>(act_s);
     float2 *gs = reinterpret_cast<float2 *>(act_s + (uint64_t)p.groups * 256);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int run = lane + 32 * i;
+    for (int i = 0; i < 2; ++i) {
+        const int run = t + 64 * i;
         const uint4 raw = reinterpret_cast<const uint4 *>(qs)[run];
         const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};     // x16 pairs (2e, 2e+1)
         // entry p = (x16[p], x16[4 + p]) of the run
@@ -208,7 +232,7 @@ __device__ __forceinline__ void prepare_block(const IntParams &p, uint8_t *act_s
         const uint32_t G = b * 8 + (run >> 4);     // 16 runs per group of 128
         if ((lane & 15) == 0 && G < p.groups) gs[G] = make_float2(ldexpf(1.f, -E), __int_as_float(sum));
     }
-    __syncwarp();                             // qs is read before the next block reuses the tile
+    named_barrier(bar, 64);      // qs is read before the next block reuses the tile
 }
 
 __global__ void __launch_bounds__(kThreads, 1) gemv_pq2_int_kernel(const __grid_constant__ IntParams p) {
@@ -240,29 +264,31 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_pq2_int_kernel(const __grid_
         // weights are read-only parameters: a few items before the dependency wait
         for (uint32_t i = 0; i < pre; ++i) issue_item(p, smem, i, last_cta);
     }
-    // rotation: warp w < nrot takes blocks w, w + nrot, ...
-    const uint32_t nrot = p.nblk < kRotWarps ? p.nblk : kRotWarps;
-    float d[32];
-    if (p.signs && (uint32_t)warp < nrot) load_block_signs(p, warp, lane, d);     // also read-only
+    // rotation: warp pair pr = warp / 2 < nrot takes blocks pr, pr + nrot, ...
+    const uint32_t nrot = p.nblk < kRotPairs ? p.nblk : kRotPairs;
+    const uint32_t pr = warp >> 1;
+    const int t = tid & 63;
+    float d[16];
+    if (p.signs && pr < nrot) load_signs16(p, pr, t, d);     // also read-only
     pdl_launch_dependents();
     pdl_wait();          // x may come from the preceding kernel
 
-    float v[32];
-    if ((uint32_t)warp < nrot) load_block(p, warp, lane, v);
+    float v[16];
+    if (pr < nrot) load_run16(p, pr, t, v);
     __syncthreads();     // every warp's x request is out: the rest of the ring queues behind them
     if (tid == 0) {
         for (uint32_t i = pre; i < ring_to; ++i) issue_item(p, smem, i, last_cta);
         *issued = ring_to;
     }
     uint8_t *act_s = smem + p.off_act;
-    if ((uint32_t)warp < nrot) {
-        float *tile = reinterpret_cast<float *>(smem + p.off_part + warp * kRotScratch);
-        for (uint32_t b = warp; b < p.nblk; b += nrot) {
-            if (b != (uint32_t)warp) {
-                if (p.signs) load_block_signs(p, b, lane, d);
-                load_block(p, b, lane, v);
+    if (pr < nrot) {
+        float *tile = reinterpret_cast<float *>(smem + p.off_part + pr * kRotScratch);
+        for (uint32_t b = pr; b < p.nblk; b += nrot) {
+            if (b != pr) {
+                if (p.signs) load_signs16(p, b, t, d);
+                load_run16(p, b, t, v);
             }
-            prepare_block(p, act_s, b, lane, v, d, tile);
+            prepare_block(p, act_s, b, t, v, d, tile, 1 + pr);
         }
     }
     __syncthreads();
@@ -378,8 +404,8 @@ bool gemv_pq2_int_plan(const ninfer_row_split_geometry &g, uint64_t M, bool rota
     if (g.k > (1u << 24) || g.n > (1ull << 31)) return false;
     const uint32_t groups = (uint32_t)g.groups_per_row;
     const uint32_t act_bytes = ((groups * 264 + 15) / 16) * 16;
-    // tile partial sums, and before them the rotation's scratch (one 32 x 33 tile per rotating warp)
-    const uint32_t nrot = std::min<uint32_t>((uint32_t)((g.k + 1023) / 1024), kRotWarps);
+    // tile partial sums, and before them the rotation's scratch (one padded tile per rotating warp pair)
+    const uint32_t nrot = std::min<uint32_t>((uint32_t)((g.k + 1023) / 1024), kRotPairs);
     const uint32_t part_bytes = std::max<uint32_t>(kWarps * kRows * 4, nrot * kRotScratch);
     const uint32_t bar_bytes = kMaxSlots * 8;
     const uint32_t cnt_bytes = (kMaxSlots + 4) * 4;
