@@ -82,7 +82,7 @@ def sources_sha256(files) -> str:
 
 _COMMON = ["bit_gemv_gb300/csrc/gemv_common.cu", "bit_gemv_gb300/csrc/async.cuh",
            "bit_gemv_gb300/csrc/device.cuh", "bit_gemv_gb300/csrc/gemv.h"]
-GEMV_SOURCES = ["bit_gemv_gb300/csrc/gemv_pq2_int.cu"] + _COMMON
+GEMV_SOURCES = ["bit_gemv_gb300/csrc/gemv_pq2_int.cu", "bit_gemv_gb300/csrc/act16.cuh"] + _COMMON
 KERNEL_TAG = "gemv"
 
 
@@ -94,6 +94,8 @@ def dominant_kernel(w):
         return "gemv_m8", ["bit_gemv_gb300/csrc/gemv_pq2.cu"] + _COMMON
     if w.fmt == "PQ2_0_G128":
         return "gemm_tc", ["bit_gemv_gb300/csrc/gemm_tc.cu"] + _COMMON
+    if w.M == 1:
+        return "gemv_ptq1", ["bit_gemv_gb300/csrc/gemv_ptq1_int.cu", "bit_gemv_gb300/csrc/act16.cuh"] + _COMMON
     return "gemm_simple", ["bit_gemv_gb300/csrc/gemm_simple.cu", "bit_gemv_gb300/csrc/plane.cuh"] + _COMMON
 
 
@@ -300,7 +302,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
 
 def path_dtype(w) -> str:
     """Arithmetic type of the path that serves workload w."""
-    if w.fmt == "PQ2_0_G128" and w.M == 1:
+    if w.M == 1:
         return "int16*ternary->int32->f32"
     if w.fmt == "PQ2_0_G128" and w.M <= 8:
         return "e4m3*e4m3->f32"
@@ -318,9 +320,10 @@ def tensor_roofline(M, n, k, s_step, traffic):
 
 
 def kernels_per_step(w) -> int:
-    """Kernels one projection launches: the PQ2_0 decode kernels (M <= 8) rotate
-    x themselves; the general path runs the transform and then the tiled GEMM."""
-    return 1 if (w.fmt == "PQ2_0_G128" and w.M <= 8) else 2
+    """Kernels one projection launches: the decode kernels (M = 1, and PQ2_0 up
+    to M = 8) rotate x themselves; the prefill and general paths run a transform
+    kernel and then the GEMM."""
+    return 1 if (w.M == 1 or (w.fmt == "PQ2_0_G128" and w.M <= 8)) else 2
 
 
 # ------------------------------------------------------------ CPU oracle ---

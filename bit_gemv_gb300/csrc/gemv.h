@@ -52,6 +52,18 @@ int gemv_pq2_launch(const GemvPlan &plan, const uint8_t *payload, const ninfer_r
                     int x_dtype, const uint16_t *signs, void *y, int y_dtype, uint64_t M, cudaStream_t stream,
                     bool pdl);
 
+// M = 1 integer kernel (PTQ1_0_G128), rotation fused in.
+struct Ptq1Plan {
+    bool ok;
+    uint32_t grid, rows_per_cta, nch, nslots, pre_issue;
+    uint32_t off_ring, off_lut, off_act, off_rot, off_rem, off_part, off_bar, off_cnt, smem;
+};
+bool gemv_ptq1_int_plan(const ninfer_row_split_geometry &g, uint64_t M, bool rotate, int sms, int smem_limit,
+                        Ptq1Plan *plan);
+int gemv_ptq1_int_launch(const Ptq1Plan &plan, const uint8_t *payload, const ninfer_row_split_geometry &g,
+                         const void *x, int x_dtype, const uint16_t *signs, void *y, int y_dtype, cudaStream_t stream,
+                         bool pdl);
+
 // Prefill (M > 8) tensor-core path for PQ2_0_G128 (gemm_tc.cu).
 struct TcPlan {
     bool ok;

@@ -40,6 +40,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "act16.cuh"
 #include "async.cuh"
 #include "common.h"
 #include "device.cuh"
@@ -70,17 +71,6 @@ struct IntParams {
     uint32_t *err;
 };
 
-__device__ __forceinline__ int dp2a_lo(uint32_t a, uint32_t b, int c) {
-    int d;
-    asm("dp2a.lo.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-    return d;
-}
-__device__ __forceinline__ int dp2a_hi(uint32_t a, uint32_t b, int c) {
-    int d;
-    asm("dp2a.hi.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-    return d;
-}
-
 // Item i = tile * nitem + j (groups 8j .. 8j + 7 of the tile's rows): its two
 // weight boxes and its scale box into ring slot i % nslots (one thread).
 __device__ __forceinline__ void issue_item(const IntParams &p, uint8_t *smem, uint32_t item, bool last_cta) {
@@ -100,117 +90,16 @@ __device__ __forceinline__ void issue_item(const IntParams &p, uint8_t *smem, ui
     }
 }
 
-// Activation preparation, two warps (64 threads) per 1024-block, 16 elements
-// per thread, in three register passes over index bits 0-3, 4-7 and 8-9 with
-// transposes through a padded float tile between them (element e at e + e/16,
-// conflict-free for the first two layouts). The quantised values go through
-// the same scratch as int16 in natural order, so that each thread reads
-// 16-byte runs of eight consecutive elements for the operand words.
-constexpr uint32_t kRotScratch = (1024 + 64) * 4 + 16;     // bytes per rotating warp pair
-
-__device__ __forceinline__ int pad16(int e) { return e + (e >> 4); }
-
-// x (times the signs) of block b: thread t (0..63) gets elements 16t .. 16t + 15 (zero past k).
-__device__ __forceinline__ void load_run16(const IntParams &p, uint32_t b, int t, float (&v)[16]) {
-    const uint64_t e0 = (uint64_t)b * 1024 + 16 * t;
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        float u[8];
-        const uint64_t idx = e0 + 8 * i;
-        if (idx + 8 <= p.k) {
-            load8(p.x, idx, p.x_dtype, u);
-        } else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) u[e] = idx + e < p.k ? load1(p.x, idx + e, p.x_dtype) : 0.f;
-        }
-#pragma unroll
-        for (int e = 0; e < 8; ++e) v[8 * i + e] = u[e];
-    }
-}
-
-__device__ __forceinline__ void load_signs16(const IntParams &p, uint32_t b, int t, float (&d)[16]) {
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        float u[8];
-        load_signs8(p.signs, (uint64_t)b * 1024 + 16 * t + 8 * i, u);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) d[8 * i + e] = u[e];
-    }
-}
-
-// Butterflies over register index bits lo .. lo + nbits - 1 of 16 values.
-template <int kLo, int kBits>
-__device__ __forceinline__ void butterfly16(float (&v)[16]) {
-#pragma unroll
-    for (int bit = kLo; bit < kLo + kBits; ++bit)
-#pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            if (r & (1 << bit)) continue;
-            const float a0 = v[r], a1 = v[r | (1 << bit)];
-            v[r] = a0 + a1;
-            v[r | (1 << bit)] = a0 - a1;
-        }
-}
-
-// Rotates and quantises block b (x in v, signs in d) and writes its dp2a
-// operand words and group entries to shared memory:
+// Writes block b's dp2a operand words and group entries (x16 from
+// rotate_quantize16, act16.cuh):
 //   act[word][4h + p] = (x16[16 word + 8h + p], x16[16 word + 8h + 4 + p]),
-//   gs[group] = {2^-E, sum of the group's x16 (as int bits)},
-// x16 = rint(xr * 2^E), E per block so that max |x16| < 2^14. t = thread of
-// the pair (0..63), bar = the pair's named barrier.
-__device__ __forceinline__ void prepare_block(const IntParams &p, uint8_t *act_s, uint32_t b, int t, float (&v)[16],
-                                              const float (&d)[16], float *tile, uint32_t bar) {
-    const bool rotate = p.signs != nullptr;
+//   gs[group] = {2^-E, sum of the group's x16 (as int bits)}.
+// Thread t of the pair takes runs t and t + 64 of eight consecutive elements.
+__device__ __forceinline__ void pack_pq2(const int16_t *qs, uint8_t *act_s, uint32_t groups, uint32_t b, int t, int E,
+                                         uint32_t bar) {
     const int lane = t & 31;
-    float *pmax = tile + 1024 + 64;
-    if (rotate) {
-#pragma unroll
-        for (int r = 0; r < 16; ++r) v[r] *= d[r];
-        butterfly16<0, 4>(v);                                    // bits 0-3: elements 16t + r
-#pragma unroll
-        for (int r = 0; r < 16; ++r) tile[17 * t + r] = v[r];      // pad16(16t + r)
-        named_barrier(bar, 64);
-        // bits 4-7: thread t = (hi2, lo4) takes elements 256 hi2 + 16 r + lo4
-        const int hi2 = t >> 4, lo4 = t & 15;
-#pragma unroll
-        for (int r = 0; r < 16; ++r) v[r] = tile[272 * hi2 + 17 * r + lo4];
-        butterfly16<0, 4>(v);
-#pragma unroll
-        for (int r = 0; r < 16; ++r) tile[272 * hi2 + 17 * r + lo4] = v[r];
-        named_barrier(bar, 64);
-        // bits 8-9: thread t takes elements 256 a + 4t + c (a = r / 4, c = r % 4)
-#pragma unroll
-        for (int r = 0; r < 16; ++r) v[r] = tile[pad16(256 * (r >> 2) + 4 * t + (r & 3))];
-        butterfly16<2, 2>(v);                                    // register bits 2-3 = element bits 8-9
-#pragma unroll
-        for (int r = 0; r < 16; ++r) v[r] *= 0.03125f;
-    } else {
-#pragma unroll
-        for (int r = 0; r < 16; ++r) tile[17 * t + r] = v[r];
-        named_barrier(bar, 64);
-#pragma unroll
-        for (int r = 0; r < 16; ++r) v[r] = tile[pad16(256 * (r >> 2) + 4 * t + (r & 3))];
-    }
-    float mx = 0.f;
-#pragma unroll
-    for (int r = 0; r < 16; ++r) mx = fmaxf(mx, fabsf(v[r]));
-#pragma unroll
-    for (int s = 16; s > 0; s >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, s));
-    if (lane == 0) pmax[t >> 5] = mx;
-    named_barrier(bar, 64);      // also: every thread has read its tile values
-    mx = fmaxf(pmax[0], pmax[1]);
-    int E = 0;
-    if (mx > 0.f) E = 13 - ilogbf(mx);     // max |x16| < 2^14
-    E = max(-100, min(100, E));
-    const float up = ldexpf(1.f, E);
-    int16_t *qs = reinterpret_cast<int16_t *>(tile);
-#pragma unroll
-    for (int r = 0; r < 16; ++r)           // adding 1.5 * 2^23 rounds to nearest, ties to even
-        qs[256 * (r >> 2) + 4 * t + (r & 3)] = (int16_t)(__float_as_int(fmaf(v[r], up, 12582912.0f)) - 0x4B400000);
-    named_barrier(bar, 64);
-    // 128 runs of eight elements; thread t takes runs t and t + 64 (operand word run/2, half run&1)
     uint4 *act = reinterpret_cast<uint4 *>(act_s);
-    float2 *gs = reinterpret_cast<float2 *>(act_s + (uint64_t)p.groups * 256);
+    float2 *gs = reinterpret_cast<float2 *>(act_s + (uint64_t)groups * 256);
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
         const int run = t + 64 * i;
@@ -223,14 +112,14 @@ __device__ __forceinline__ void prepare_block(const IntParams &p, uint8_t *act_s
         pk.z = __byte_perm(w[1], w[3], 0x5410);
         pk.w = __byte_perm(w[1], w[3], 0x7632);
         const uint32_t word = b * 64 + (run >> 1);
-        if (word < p.groups * 8) act[word * 2 + (run & 1)] = pk;
+        if (word < groups * 8) act[word * 2 + (run & 1)] = pk;
         int sum = 0;
 #pragma unroll
         for (int q = 0; q < 4; ++q) sum += (int)(int16_t)(w[q] & 0xffff) + (int)(int16_t)(w[q] >> 16);
 #pragma unroll
         for (int sh = 8; sh > 0; sh >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, sh);
         const uint32_t G = b * 8 + (run >> 4);     // 16 runs per group of 128
-        if ((lane & 15) == 0 && G < p.groups) gs[G] = make_float2(ldexpf(1.f, -E), __int_as_float(sum));
+        if ((lane & 15) == 0 && G < groups) gs[G] = make_float2(ldexpf(1.f, -E), __int_as_float(sum));
     }
     named_barrier(bar, 64);      // qs is read before the next block reuses the tile
 }
@@ -268,13 +157,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_pq2_int_kernel(const __grid_
     const uint32_t nrot = p.nblk < kRotPairs ? p.nblk : kRotPairs;
     const uint32_t pr = warp >> 1;
     const int t = tid & 63;
+    const XSource xsrc{p.x, p.signs, p.k, p.x_dtype};
     float d[16];
-    if (p.signs && pr < nrot) load_signs16(p, pr, t, d);     // also read-only
+    if (p.signs && pr < nrot) load_signs16(xsrc, pr, t, d);     // also read-only
     pdl_launch_dependents();
     pdl_wait();          // x may come from the preceding kernel
 
     float v[16];
-    if (pr < nrot) load_run16(p, pr, t, v);
+    if (pr < nrot) load_run16(xsrc, pr, t, v);
     __syncthreads();     // every warp's x request is out: the rest of the ring queues behind them
     if (tid == 0) {
         for (uint32_t i = pre; i < ring_to; ++i) issue_item(p, smem, i, last_cta);
@@ -285,10 +175,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_pq2_int_kernel(const __grid_
         float *tile = reinterpret_cast<float *>(smem + p.off_part + pr * kRotScratch);
         for (uint32_t b = pr; b < p.nblk; b += nrot) {
             if (b != pr) {
-                if (p.signs) load_signs16(p, b, t, d);
-                load_run16(p, b, t, v);
+                if (p.signs) load_signs16(xsrc, b, t, d);
+                load_run16(xsrc, b, t, v);
             }
-            prepare_block(p, act_s, b, t, v, d, tile, 1 + pr);
+            int E;
+            const int16_t *qs = rotate_quantize16(p.signs != nullptr, t, v, d, tile, 1 + pr, &E);
+            pack_pq2(qs, act_s, p.groups, b, t, E, 1 + pr);
         }
     }
     __syncthreads();

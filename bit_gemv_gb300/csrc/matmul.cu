@@ -38,12 +38,13 @@ static bool g_pdl = true;
 using namespace ninfer;
 
 namespace {
-enum class Path { kIntPq2, kFusedPq2, kTcPq2, kTiled };
+enum class Path { kIntPq2, kIntPtq1, kFusedPq2, kTcPq2, kTiled };
 
 struct MatmulPlan {
     Path path;
     GemvPlan gemv;
     IntPlan gint;
+    Ptq1Plan gptq;
     TcPlan gtc;
     uint64_t workspace;
 };
@@ -56,6 +57,10 @@ int plan_matmul(int fmt, const ninfer_row_split_geometry &g, uint64_t M, bool ro
     if (fmt == NINFER_PQ2_0_G128 && gemv_pq2_int_plan(g, M, rotate, d.sms, d.smem_optin, &mp->gint)) {
         mp->path = Path::kIntPq2;
         mp->workspace = mp->gint.workspace;     // none: each CTA rotates x itself
+        return NINFER_OK;
+    }
+    if (fmt == NINFER_PTQ1_0_G128 && gemv_ptq1_int_plan(g, M, rotate, d.sms, d.smem_optin, &mp->gptq)) {
+        mp->path = Path::kIntPtq1;
         return NINFER_OK;
     }
     if (fmt == NINFER_PQ2_0_G128 && gemv_pq2_plan(g, M, rotate, d.sms, d.smem_optin, &mp->gemv)) {
@@ -126,6 +131,8 @@ extern "C" int ninfer_ternary_matmul(int fmt, const uint8_t *payload, uint64_t p
     cudaStream_t s = (cudaStream_t)stream;
     if (mp.path == Path::kIntPq2)
         return gemv_pq2_int_launch(mp.gint, payload, g, x, x_dtype, signs_bf16, y, y_dtype, s, g_pdl);
+    if (mp.path == Path::kIntPtq1)
+        return gemv_ptq1_int_launch(mp.gptq, payload, g, x, x_dtype, signs_bf16, y, y_dtype, s, g_pdl);
     if (mp.path == Path::kFusedPq2)
         return gemv_pq2_launch(mp.gemv, payload, g, x, x_dtype, signs_bf16, y, y_dtype, M, s, g_pdl);
     if (mp.path == Path::kTcPq2)
