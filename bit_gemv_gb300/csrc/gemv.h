@@ -57,12 +57,15 @@ struct Ptq1Plan {
     bool ok;
     uint32_t grid, rows_per_cta, nch, nslots, pre_issue;
     uint32_t off_ring, off_lut, off_act, off_rot, off_rem, off_part, off_bar, off_cnt, smem;
+    bool split;              // operand words from a separate prep kernel (wide x)
+    uint32_t act_bytes;
+    uint64_t workspace;
 };
 bool gemv_ptq1_int_plan(const ninfer_row_split_geometry &g, uint64_t M, bool rotate, int sms, int smem_limit,
                         Ptq1Plan *plan);
 int gemv_ptq1_int_launch(const Ptq1Plan &plan, const uint8_t *payload, const ninfer_row_split_geometry &g,
-                         const void *x, int x_dtype, const uint16_t *signs, void *y, int y_dtype, cudaStream_t stream,
-                         bool pdl);
+                         const void *x, int x_dtype, const uint16_t *signs, void *y, int y_dtype, void *workspace,
+                         cudaStream_t stream, bool pdl);
 
 // Prefill (M > 8) tensor-core path for PQ2_0_G128 (gemm_tc.cu).
 struct TcPlan {

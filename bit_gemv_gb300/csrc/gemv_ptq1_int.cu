@@ -62,6 +62,8 @@ struct Ptq1Params {
     uint64_t base_row, high_row, scale_row;
     const void *x;
     const uint16_t *signs;
+    const uint8_t *act_g;               // operand words from ptq1_prep_kernel, or null (rotate here)
+    uint32_t act_bytes;
     void *y;
     uint64_t n;
     uint32_t k, groups, nblk, nch, rows_per_cta;
@@ -119,25 +121,31 @@ __device__ __forceinline__ void issue_item(const Ptq1Params &p, uint8_t *smem, u
 // Operand words of block b from its x16 (rotate_quantize16): per group G,
 //   word 3j + c (j < 24): c = 0 -> (x16[5j], x16[5j+1]), 1 -> (x16[5j+2], x16[5j+3]), 2 -> (x16[5j+4], 0)
 //   word 72 + 2h + c (h < 2): (x16[120+4h+2c], x16[121+4h+2c])
-// and gs[G] = {2^-E, sum of the group's x16 (as int bits)}.
+// and gs[G] = {2^-E, sum of the group's x16 (as int bits)}. The block's 8
+// groups have 208 code bytes (192 base, 16 high); thread t of the pair takes
+// bytes t, t + 64, t + 128 and t + 192.
 __device__ __forceinline__ void pack_ptq1(const int16_t *qs, uint8_t *act_s, uint32_t groups, uint32_t b, int t, int E,
                                           uint32_t bar) {
     uint32_t *act = reinterpret_cast<uint32_t *>(act_s);
-    for (uint32_t w = t; w < 8 * kActWords; w += 64) {
-        const uint32_t gl = w / kActWords, idx = w % kActWords, G = b * 8 + gl;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t u = t + 64 * i;
+        if (u >= 208) break;
+        const uint32_t gl = u < 192 ? u / 24 : (u - 192) >> 1, G = b * 8 + gl;
         if (G >= groups) continue;
-        uint32_t e0;
-        bool single = false;
-        if (idx < 72) {
-            const uint32_t j = idx / 3, c = idx % 3;
-            e0 = 128 * gl + 5 * j + 2 * c;
-            single = c == 2;
+        uint32_t *dst = act + (uint64_t)G * kActWords;
+        if (u < 192) {
+            const uint32_t j = u % 24;
+            const int16_t *e = qs + 128 * gl + 5 * j;
+            dst[3 * j] = (uint32_t)(uint16_t)e[0] | ((uint32_t)(uint16_t)e[1] << 16);
+            dst[3 * j + 1] = (uint32_t)(uint16_t)e[2] | ((uint32_t)(uint16_t)e[3] << 16);
+            dst[3 * j + 2] = (uint32_t)(uint16_t)e[4];
         } else {
-            const uint32_t hh = (idx - 72) >> 1, c = (idx - 72) & 1;
-            e0 = 128 * gl + 120 + 4 * hh + 2 * c;
+            const uint32_t hh = (u - 192) & 1;
+            const int16_t *e = qs + 128 * gl + 120 + 4 * hh;
+            dst[72 + 2 * hh] = (uint32_t)(uint16_t)e[0] | ((uint32_t)(uint16_t)e[1] << 16);
+            dst[73 + 2 * hh] = (uint32_t)(uint16_t)e[2] | ((uint32_t)(uint16_t)e[3] << 16);
         }
-        const uint32_t lo = (uint16_t)qs[e0], hi = single ? 0u : (uint16_t)qs[e0 + 1];
-        act[(uint64_t)G * kActWords + idx] = lo | (hi << 16);
     }
     // group sums: thread t sums elements 16t .. 16t + 15 (group t / 8)
     int sum = 0;
@@ -152,6 +160,24 @@ __device__ __forceinline__ void pack_ptq1(const int16_t *qs, uint8_t *act_s, uin
     named_barrier(bar, 64);      // qs is read before the next block reuses the tile
 }
 
+// Wide inputs (more 1024-blocks than rotating pairs in a CTA): one warp pair
+// per block rotates x once for the whole grid and writes the operand words and
+// group entries in the decode kernel's shared-memory layout.
+__global__ void __launch_bounds__(64) ptq1_prep_kernel(const XSource xsrc, uint32_t groups, uint8_t *out) {
+    __shared__ __align__(16) float tile[kRotScratch / 4];
+    const int t = threadIdx.x;
+    const uint32_t b = blockIdx.x;
+    float d[16];
+    if (xsrc.signs) load_signs16(xsrc, b, t, d);     // read-only parameter: before the dependency wait
+    pdl_launch_dependents();
+    pdl_wait();
+    float v[16];
+    load_run16(xsrc, b, t, v);
+    int E;
+    const int16_t *qs = rotate_quantize16(xsrc.signs != nullptr, t, v, d, tile, 1, &E);
+    pack_ptq1(qs, out, groups, b, t, E, 1);
+}
+
 // sum_j t_j x16_j of one group: 24 base bytes (six words) and 2 high bytes,
 // table lookups in lane-private copies, operand words from shared memory.
 __device__ __forceinline__ int group_dot(const uint32_t (&bw)[6], uint32_t hb, const uint32_t *lut, int lane,
@@ -161,10 +187,13 @@ __device__ __forceinline__ int group_dot(const uint32_t (&bw)[6], uint32_t hb, c
     for (int i = 0; i < 19; ++i) a[i] = aw[i];
     const uint32_t *av = reinterpret_cast<const uint32_t *>(a);
     int acc[4] = {0, 0, 0, 0}, acc4 = 0;
+    const uint8_t *lutb = reinterpret_cast<const uint8_t *>(lut) + 4 * lane;
 #pragma unroll
     for (int j = 0; j < 24; ++j) {
-        const uint32_t byte = (bw[j >> 2] >> (8 * (j & 3))) & 0xffu;
-        const uint32_t W = lut[byte * 32 + lane];
+        // byte (j & 3) of word j >> 2, times 128 (one table row of 32 copies)
+        const int sh = 8 * (j & 3) - 7;
+        const uint32_t off = (sh >= 0 ? bw[j >> 2] >> sh : bw[j >> 2] << (-sh)) & 0x7F80u;
+        const uint32_t W = *reinterpret_cast<const uint32_t *>(lutb + off);
         const uint32_t m = W & 0x03030303u;
         acc[j & 3] = dp2a_lo(av[3 * j], m, acc[j & 3]);
         acc[j & 3] = dp2a_hi(av[3 * j + 1], m, acc[j & 3]);
@@ -172,7 +201,9 @@ __device__ __forceinline__ int group_dot(const uint32_t (&bw)[6], uint32_t hb, c
     }
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
-        const uint32_t W = lut[((hb >> (8 * hh)) & 0xffu) * 32 + lane];
+        const int sh = 8 * hh - 7;
+        const uint32_t off = (sh >= 0 ? hb >> sh : hb << (-sh)) & 0x7F80u;
+        const uint32_t W = *reinterpret_cast<const uint32_t *>(lutb + off);
         const uint32_t m = W & 0x03030303u;
         acc[hh] = dp2a_lo(av[72 + 2 * hh], m, acc[hh]);
         acc[hh] = dp2a_hi(av[73 + 2 * hh], m, acc[hh]);
@@ -202,6 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ptq1_int_kernel(const __grid
             cnt[s] = 0;
         }
         mbar_init(rem_bar, 1);
+        mbar_init(rem_bar + 8, 1);
         *failed = 0;
         fence_mbar_init();
     }
@@ -224,20 +256,25 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ptq1_int_kernel(const __grid
             }
         }
     }
-    // digit table, replicated per bank: entry (B, l) at 32 B + l
-    for (uint32_t e = tid; e < 256 * 32; e += kThreads) {
-        uint32_t B = e >> 5, W = 0;
+    // digit table, replicated per bank: entry (B, l) at 32 B + l; thread tid
+    // computes entry tid / 2 and writes 16 of its copies
+    {
+        uint32_t B = (uint32_t)tid >> 1, W = 0;
 #pragma unroll
         for (int i = 0; i < 5; ++i) {
             const uint32_t t = B % 3;
             B /= 3;
             W |= i < 4 ? t << (8 * i) : t << 2;
         }
-        lut[e] = W;
+        uint4 *dst = reinterpret_cast<uint4 *>(lut + (tid >> 1) * 32 + 16 * (tid & 1));
+        const uint4 w4 = make_uint4(W, W, W, W);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) dst[c] = w4;
     }
     // rotation: warp pair pr = warp / 2 < nrot takes blocks pr, pr + nrot, ...
+    // (none when the prep kernel has already written the operand words)
     const XSource xsrc{p.x, p.signs, p.k, p.x_dtype};
-    const uint32_t nrot = p.nblk < kRotPairs ? p.nblk : kRotPairs;
+    const uint32_t nrot = p.act_g ? 0 : (p.nblk < kRotPairs ? p.nblk : kRotPairs);
     const uint32_t pr = warp >> 1;
     const int t = tid & 63;
     float d[16];
@@ -247,12 +284,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ptq1_int_kernel(const __grid
 
     float v[16];
     if (pr < nrot) load_run16(xsrc, pr, t, v);
+    uint8_t *act_s = smem + p.off_act;
+    const uint32_t act_bar = rem_bar + 8;
+    if (p.act_g && tid == 0) {          // the operand words, ahead of the rest of the ring
+        mbar_arrive_expect_tx(act_bar, p.act_bytes);
+        bulk_g2s(smem_u32(act_s), p.act_g, p.act_bytes, act_bar);
+    }
     __syncthreads();     // every warp's x request is out: the rest of the ring queues behind them
     if (tid == 0) {
         for (uint32_t i = pre; i < ring_to; ++i) issue_item(p, smem, i, last_cta);
         *issued = ring_to;
     }
-    uint8_t *act_s = smem + p.off_act;
     if (pr < nrot) {
         float *tile = reinterpret_cast<float *>(smem + p.off_rot + pr * kRotScratch);
         for (uint32_t b = pr; b < p.nblk; b += nrot) {
@@ -267,15 +309,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ptq1_int_kernel(const __grid
     }
     __syncthreads();
 
+    bool ok = true;
+    if (p.act_g) ok = mbar_wait(act_bar, 0, p.err);
     const uint32_t *act_w = reinterpret_cast<const uint32_t *>(act_s);
     const float2 *gs = reinterpret_cast<const float2 *>(act_s + (uint64_t)p.groups * kActWords * 4);
     float *part = reinterpret_cast<float *>(smem + p.off_part);
     float *part_rem = part + kWarps * kRows;      // [kMaxRem][groups]
-    bool ok = true;
 
     // remainder rows: lanes = (row, group of the chunk); warp w takes chunks w, w + 16, ...
     if (cr.rem) {
-        ok = mbar_wait(rem_bar, 0, p.err);
+        ok = ok && mbar_wait(rem_bar, 0, p.err);
         const uint32_t rb_bytes = (uint32_t)(p.base_row + p.high_row + p.scale_row);
         const uint32_t rr = lane >> 4;
         for (uint32_t ch = warp; ok && ch < p.nch; ch += kWarps) {
@@ -374,6 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ptq1_int_kernel(const __grid
         for (uint32_t i = n_issued > p.nslots ? n_issued - p.nslots : 0; i < n_issued; ++i)
             mbar_wait(bar0 + 8 * (i % p.nslots), (i / p.nslots) & 1, p.err, 200000000ll);
         if (cr.rem) mbar_wait(rem_bar, 0, p.err, 200000000ll);
+        if (p.act_g) mbar_wait(rem_bar + 8, 0, p.err, 200000000ll);
     }
 }
 
@@ -390,16 +434,19 @@ bool gemv_ptq1_int_plan(const ninfer_row_split_geometry &g, uint64_t M, bool rot
     const uint32_t groups = (uint32_t)g.groups_per_row;
     const uint32_t nblk = (uint32_t)((g.k + 1023) / 1024);
     const uint32_t act_bytes = ((groups * (kActWords * 4 + 8) + 15) / 16) * 16;
-    const uint32_t nrot = std::min<uint32_t>(nblk, kRotPairs);
+    const bool split = nblk > kRotPairs;       // rotate in a separate kernel, once for the grid
+    const uint32_t nrot = split ? 0 : std::min<uint32_t>(nblk, kRotPairs);
     const uint32_t rot_bytes = nrot * kRotScratch;
     const uint32_t rem_bytes = (uint32_t)(kMaxRem * (g.base_row_bytes + g.high_row_bytes + g.scale_row_bytes));
     const uint32_t part_bytes = (kWarps * kRows + kMaxRem * groups) * 4;
-    const uint32_t bar_bytes = (kMaxSlots + 1) * 8;
+    const uint32_t bar_bytes = (kMaxSlots + 2) * 8;
     const uint32_t cnt_bytes = (kMaxSlots + 4) * 4;
     const uint32_t fixed = kLutBytes + act_bytes + ((rot_bytes + 15) / 16) * 16 + ((rem_bytes + 15) / 16) * 16 +
                            ((part_bytes + 15) / 16) * 16 + bar_bytes + cnt_bytes;
-    if ((int64_t)fixed + 2 * kItemBytes > smem_limit) return false;
-    const uint32_t nslots = std::min<uint32_t>(kMaxSlots, (uint32_t)((smem_limit - (int)fixed) / (int)kItemBytes));
+    // with a prep kernel, leave room on the SM for one of its CTAs next to this kernel's
+    const int limit = split ? smem_limit - 8 * 1024 : smem_limit;
+    if ((int64_t)fixed + 2 * kItemBytes > limit) return false;
+    const uint32_t nslots = std::min<uint32_t>(kMaxSlots, (uint32_t)((limit - (int)fixed) / (int)kItemBytes));
     // one CTA per SM with ~n / SMs rows each
     const uint64_t grid0 = std::max<uint64_t>(1, std::min<uint64_t>((uint64_t)sms, g.n / 32));
     const uint64_t R = (g.n + grid0 - 1) / grid0;
@@ -428,12 +475,15 @@ bool gemv_ptq1_int_plan(const ninfer_row_split_geometry &g, uint64_t M, bool rot
     plan->off_cnt = off;
     off += cnt_bytes;
     plan->smem = off;
+    plan->split = split;
+    plan->act_bytes = act_bytes;
+    plan->workspace = split ? act_bytes : 0;
     return true;
 }
 
 int gemv_ptq1_int_launch(const Ptq1Plan &plan, const uint8_t *payload, const ninfer_row_split_geometry &g,
-                         const void *x, int x_dtype, const uint16_t *signs, void *y, int y_dtype, cudaStream_t stream,
-                         bool pdl) {
+                         const void *x, int x_dtype, const uint16_t *signs, void *y, int y_dtype, void *workspace,
+                         cudaStream_t stream, bool pdl) {
     Ptq1Params p;
     std::memset(&p, 0, sizeof p);
     p.base = payload + g.base_offset;
@@ -444,6 +494,8 @@ int gemv_ptq1_int_launch(const Ptq1Plan &plan, const uint8_t *payload, const nin
     p.scale_row = g.scale_row_bytes;
     p.x = x;
     p.signs = signs;
+    p.act_g = plan.split ? static_cast<const uint8_t *>(workspace) : nullptr;
+    p.act_bytes = plan.act_bytes;
     p.y = y;
     p.n = g.n;
     p.k = (uint32_t)g.k;
@@ -478,6 +530,20 @@ int gemv_ptq1_int_launch(const Ptq1Plan &plan, const uint8_t *payload, const nin
     if (!st)
         st = encode_rows(&p.smap_last, p.scale + lr * g.scale_row_bytes, g.scale_row_bytes, last_rows, 1, 32, kRows, false);
     if (st) return st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    if (plan.split) {
+        cudaLaunchConfig_t pc = {};
+        pc.gridDim = dim3(p.nblk);
+        pc.blockDim = dim3(64);
+        pc.stream = stream;
+        pc.attrs = attr;
+        pc.numAttrs = 1;
+        const XSource xsrc{x, signs, p.k, x_dtype};
+        cudaError_t pe = cudaLaunchKernelEx(&pc, ptq1_prep_kernel, xsrc, p.groups, static_cast<uint8_t *>(workspace));
+        if (pe != cudaSuccess) return fail(NINFER_ERR_CUDA, "ptq1 prep launch: %s", cudaGetErrorString(pe));
+    }
     cudaError_t e = cudaFuncSetAttribute(gemv_ptq1_int_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.smem);
     if (e != cudaSuccess) return fail(NINFER_ERR_CUDA, "ptq1 gemv: smem attribute: %s", cudaGetErrorString(e));
     cudaLaunchConfig_t cfg = {};
@@ -485,9 +551,6 @@ int gemv_ptq1_int_launch(const Ptq1Plan &plan, const uint8_t *payload, const nin
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = plan.smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, gemv_ptq1_int_kernel, p);

@@ -61,6 +61,7 @@ int plan_matmul(int fmt, const ninfer_row_split_geometry &g, uint64_t M, bool ro
     }
     if (fmt == NINFER_PTQ1_0_G128 && gemv_ptq1_int_plan(g, M, rotate, d.sms, d.smem_optin, &mp->gptq)) {
         mp->path = Path::kIntPtq1;
+        mp->workspace = mp->gptq.workspace;     // operand words when x is rotated by the prep kernel
         return NINFER_OK;
     }
     if (fmt == NINFER_PQ2_0_G128 && gemv_pq2_plan(g, M, rotate, d.sms, d.smem_optin, &mp->gemv)) {
@@ -132,7 +133,7 @@ extern "C" int ninfer_ternary_matmul(int fmt, const uint8_t *payload, uint64_t p
     if (mp.path == Path::kIntPq2)
         return gemv_pq2_int_launch(mp.gint, payload, g, x, x_dtype, signs_bf16, y, y_dtype, s, g_pdl);
     if (mp.path == Path::kIntPtq1)
-        return gemv_ptq1_int_launch(mp.gptq, payload, g, x, x_dtype, signs_bf16, y, y_dtype, s, g_pdl);
+        return gemv_ptq1_int_launch(mp.gptq, payload, g, x, x_dtype, signs_bf16, y, y_dtype, workspace, s, g_pdl);
     if (mp.path == Path::kFusedPq2)
         return gemv_pq2_launch(mp.gemv, payload, g, x, x_dtype, signs_bf16, y, y_dtype, M, s, g_pdl);
     if (mp.path == Path::kTcPq2)
