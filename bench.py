@@ -91,7 +91,7 @@ def dominant_kernel(w):
     if w.fmt == "PQ2_0_G128" and w.M == 1:
         return KERNEL_TAG, GEMV_SOURCES
     if w.fmt == "PQ2_0_G128" and w.M <= 8:
-        return "gemv_m8", ["bit_gemv_gb300/csrc/gemv_pq2.cu"] + _COMMON
+        return "gemv_mma", ["bit_gemv_gb300/csrc/gemv_pq2_mma.cu", "bit_gemv_gb300/csrc/act16.cuh"] + _COMMON
     if w.fmt == "PQ2_0_G128":
         return "gemm_tc", ["bit_gemv_gb300/csrc/gemm_tc.cu"] + _COMMON
     if w.M == 1:
@@ -305,7 +305,7 @@ def path_dtype(w) -> str:
     if w.M == 1:
         return "int16*ternary->int32->f32"
     if w.fmt == "PQ2_0_G128" and w.M <= 8:
-        return "e4m3*e4m3->f32"
+        return "f16*f16->f32"
     if w.fmt == "PQ2_0_G128":
         return "f16*f16->f32"
     return "f32"
@@ -320,10 +320,12 @@ def tensor_roofline(M, n, k, s_step, traffic):
 
 
 def kernels_per_step(w) -> int:
-    """Kernels one projection launches: the decode kernels (M = 1, and PQ2_0 up
-    to M = 8) rotate x themselves; the prefill and general paths run a transform
-    kernel and then the GEMM."""
-    return 1 if (w.M == 1 or (w.fmt == "PQ2_0_G128" and w.M <= 8)) else 2
+    """Kernels one projection launches: the M = 1 decode kernels rotate x
+    themselves (PTQ1_0 with k > 8192 also runs its prep kernel); the M <= 8,
+    prefill and general paths run a prep or transform kernel and then the main one."""
+    if w.M == 1:
+        return 2 if (w.fmt == "PTQ1_0_G128" and w.k > 8192) else 1
+    return 2
 
 
 # ------------------------------------------------------------ CPU oracle ---

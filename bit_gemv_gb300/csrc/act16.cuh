@@ -83,12 +83,13 @@ __device__ __forceinline__ void butterfly16(float (&v)[16]) {
         }
 }
 
-// Rotates and quantises block b (x in v, signs in d). On return the block's
-// x16 values sit in the tile as int16 in natural order, visible to the whole
-// pair, and *E_out is the block's exponent. t = thread of the pair (0..63),
-// bar = the pair's named barrier.
-__device__ __forceinline__ const int16_t *rotate_quantize16(bool rotate, int t, float (&v)[16], const float (&d)[16],
-                                                           float *tile, uint32_t bar, int *E_out) {
+// Rotates block b (x in v, signs in d) in place: on return v[r] holds xr of
+// element 256 (r / 4) + 4t + r % 4, and the return value is the block's
+// largest |xr|. The tile's first 1088 floats are free again; the two after
+// them hold the warps' maxima until the pair's next barrier. t = thread of the
+// pair (0..63), bar = the pair's named barrier.
+__device__ __forceinline__ float rotate16(bool rotate, int t, float (&v)[16], const float (&d)[16], float *tile,
+                                          uint32_t bar) {
     const int lane = t & 31;
     float *pmax = tile + 1024 + 64;
     if (rotate) {
@@ -126,7 +127,16 @@ __device__ __forceinline__ const int16_t *rotate_quantize16(bool rotate, int t, 
     for (int s = 16; s > 0; s >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, s));
     if (lane == 0) pmax[t >> 5] = mx;
     named_barrier(bar, 64);      // also: every thread has read its tile values
-    mx = fmaxf(pmax[0], pmax[1]);
+    return fmaxf(pmax[0], pmax[1]);
+}
+
+// Rotates and quantises block b (x in v, signs in d). On return the block's
+// x16 values sit in the tile as int16 in natural order, visible to the whole
+// pair, and *E_out is the block's exponent. t = thread of the pair (0..63),
+// bar = the pair's named barrier.
+__device__ __forceinline__ const int16_t *rotate_quantize16(bool rotate, int t, float (&v)[16], const float (&d)[16],
+                                                           float *tile, uint32_t bar, int *E_out) {
+    const float mx = rotate16(rotate, t, v, d, tile, bar);
     int E = 0;
     if (mx > 0.f) E = 13 - ilogbf(mx);     // max |x16| < 2^14
     E = max(-100, min(100, E));

@@ -9,11 +9,6 @@
 
 namespace ninfer {
 
-struct GemvPlan {
-    bool ok;
-    uint32_t grid, rows_per_cta, nbox, nt, nslots, slot_bytes;
-    uint32_t off_b, off_fo, off_red, off_bar, smem;
-};
 
 // Device properties the plans depend on (queried once per device).
 struct DeviceInfo {
@@ -46,11 +41,6 @@ bool gemv_pq2_int_plan(const ninfer_row_split_geometry &g, uint64_t M, bool rota
 int gemv_pq2_int_launch(const IntPlan &plan, const uint8_t *payload, const ninfer_row_split_geometry &g, const void *x,
                         int x_dtype, const uint16_t *signs, void *y, int y_dtype, cudaStream_t stream, bool pdl);
 
-bool gemv_pq2_plan(const ninfer_row_split_geometry &g, uint64_t M, bool rotate, int sms, int smem_limit,
-                   GemvPlan *plan);
-int gemv_pq2_launch(const GemvPlan &plan, const uint8_t *payload, const ninfer_row_split_geometry &g, const void *x,
-                    int x_dtype, const uint16_t *signs, void *y, int y_dtype, uint64_t M, cudaStream_t stream,
-                    bool pdl);
 
 // M = 1 integer kernel (PTQ1_0_G128), rotation fused in.
 struct Ptq1Plan {
@@ -66,6 +56,19 @@ bool gemv_ptq1_int_plan(const ninfer_row_split_geometry &g, uint64_t M, bool rot
 int gemv_ptq1_int_launch(const Ptq1Plan &plan, const uint8_t *payload, const ninfer_row_split_geometry &g,
                          const void *x, int x_dtype, const uint16_t *signs, void *y, int y_dtype, void *workspace,
                          cudaStream_t stream, bool pdl);
+
+// 2 <= M <= 8, PQ2_0_G128: binary16 mma.sync kernel with a prep kernel for the fragments.
+struct MmaPlan {
+    bool ok;
+    uint32_t grid, rows_per_cta, nitem, nslots, pre_issue, frag_bytes;
+    uint32_t off_ring, off_frag, off_part, off_bar, off_cnt, smem;
+    uint64_t workspace;
+};
+bool gemv_pq2_mma_plan(const ninfer_row_split_geometry &g, uint64_t M, bool rotate, int sms, int smem_limit,
+                       MmaPlan *plan);
+int gemv_pq2_mma_launch(const MmaPlan &plan, const uint8_t *payload, const ninfer_row_split_geometry &g, const void *x,
+                        int x_dtype, const uint16_t *signs, void *y, int y_dtype, uint64_t M, void *workspace,
+                        cudaStream_t stream, bool pdl);
 
 // Prefill (M > 8) tensor-core path for PQ2_0_G128 (gemm_tc.cu).
 struct TcPlan {

@@ -38,13 +38,13 @@ static bool g_pdl = true;
 using namespace ninfer;
 
 namespace {
-enum class Path { kIntPq2, kIntPtq1, kFusedPq2, kTcPq2, kTiled };
+enum class Path { kIntPq2, kIntPtq1, kMmaPq2, kTcPq2, kTiled };
 
 struct MatmulPlan {
     Path path;
-    GemvPlan gemv;
     IntPlan gint;
     Ptq1Plan gptq;
+    MmaPlan gmma;
     TcPlan gtc;
     uint64_t workspace;
 };
@@ -64,8 +64,9 @@ int plan_matmul(int fmt, const ninfer_row_split_geometry &g, uint64_t M, bool ro
         mp->workspace = mp->gptq.workspace;     // operand words when x is rotated by the prep kernel
         return NINFER_OK;
     }
-    if (fmt == NINFER_PQ2_0_G128 && gemv_pq2_plan(g, M, rotate, d.sms, d.smem_optin, &mp->gemv)) {
-        mp->path = Path::kFusedPq2;
+    if (fmt == NINFER_PQ2_0_G128 && gemv_pq2_mma_plan(g, M, rotate, d.sms, d.smem_optin, &mp->gmma)) {
+        mp->path = Path::kMmaPq2;
+        mp->workspace = mp->gmma.workspace;     // the activation fragments
         return NINFER_OK;
     }
     if (fmt == NINFER_PQ2_0_G128 && gemm_tc_plan(g, M, d.smem_optin, &mp->gtc)) {
@@ -134,8 +135,8 @@ extern "C" int ninfer_ternary_matmul(int fmt, const uint8_t *payload, uint64_t p
         return gemv_pq2_int_launch(mp.gint, payload, g, x, x_dtype, signs_bf16, y, y_dtype, s, g_pdl);
     if (mp.path == Path::kIntPtq1)
         return gemv_ptq1_int_launch(mp.gptq, payload, g, x, x_dtype, signs_bf16, y, y_dtype, workspace, s, g_pdl);
-    if (mp.path == Path::kFusedPq2)
-        return gemv_pq2_launch(mp.gemv, payload, g, x, x_dtype, signs_bf16, y, y_dtype, M, s, g_pdl);
+    if (mp.path == Path::kMmaPq2)
+        return gemv_pq2_mma_launch(mp.gmma, payload, g, x, x_dtype, signs_bf16, y, y_dtype, M, workspace, s, g_pdl);
     if (mp.path == Path::kTcPq2)
         return gemm_tc_launch(mp.gtc, payload, g, x, x_dtype, signs_bf16, y, y_dtype, M, workspace, s);
     const PlaneView p = make_view(payload, g, fmt);

@@ -205,12 +205,14 @@ int ninfer_ternary_matmul_workspace(int fmt, uint64_t n, uint64_t k, uint64_t M,
  *     bytes (NULL allowed when that is 0); its contents are not preserved.
  *   M >= 1. Decode shapes (M <= 8) run the fused rotate + decode + GEMV
  *   kernels; larger M run the prefill path.
- * Arithmetic: transform in fp32. PQ2_0_G128 with M = 1: the rotated
+ * Arithmetic: transform in fp32. M = 1 (both formats): the rotated
  * activations are rounded to 16-bit fixed point per 1024-block (|x16| < 2^14,
  * relative error <= 2^-14 of the block maximum); code x activation products
  * accumulate exactly in int32 per 128-weight group, then scale in fp32.
- * PQ2_0_G128 with 2 <= M <= 8: a three-term e4m3 expansion per 1024-block
- * (relative error <= 2^-12 per element) with exact products and fp32
+ * PQ2_0_G128 with 2 <= M <= 8: binary16 activations scaled per 1024-block
+ * (relative error <= 2^-11 per element) with exact products and fp32
+ * accumulation. PQ2_0_G128 with M > 8 (prefill): binary16 activations and the
+ * exact binary16 weights (code - 1) * scale on the tensor cores, fp32
  * accumulation. Other shapes: fp32 throughout. Max relative error vs exact
  * (infinity norm over y) is well under 1e-3 for the decode paths.
  * Errors: INVALID_ARGUMENT, UNKNOWN_FORMAT, SHAPE, SIZE_MISMATCH, ALIGNMENT, CUDA.
