@@ -96,6 +96,8 @@ def dominant_kernel(w):
         return "gemm_tc", ["bit_gemv_gb300/csrc/gemm_tc.cu"] + _COMMON
     if w.M == 1:
         return "gemv_ptq1", ["bit_gemv_gb300/csrc/gemv_ptq1_int.cu", "bit_gemv_gb300/csrc/act16.cuh"] + _COMMON
+    if w.M <= 8:
+        return "gemv_ptq1_mma", ["bit_gemv_gb300/csrc/gemv_ptq1_mma.cu", "bit_gemv_gb300/csrc/act16.cuh"] + _COMMON
     return "gemm_simple", ["bit_gemv_gb300/csrc/gemm_simple.cu", "bit_gemv_gb300/csrc/plane.cuh"] + _COMMON
 
 
@@ -304,9 +306,7 @@ def path_dtype(w) -> str:
     """Arithmetic type of the path that serves workload w."""
     if w.M == 1:
         return "int16*ternary->int32->f32"
-    if w.fmt == "PQ2_0_G128" and w.M <= 8:
-        return "f16*f16->f32"
-    if w.fmt == "PQ2_0_G128":
+    if w.M <= 8 or w.fmt == "PQ2_0_G128":
         return "f16*f16->f32"
     return "f32"
 
@@ -321,10 +321,14 @@ def tensor_roofline(M, n, k, s_step, traffic):
 
 def kernels_per_step(w) -> int:
     """Kernels one projection launches: the M = 1 decode kernels rotate x
-    themselves (PTQ1_0 with k > 8192 also runs its prep kernel); the M <= 8,
-    prefill and general paths run a prep or transform kernel and then the main one."""
+    themselves (PTQ1_0 with k > 8192 also runs its prep kernel); the PTQ1_0
+    M <= 8 kernel rotates x itself and, with more than one 1024-block, is
+    followed by the block reduction; the PQ2_0 M <= 8, prefill and general
+    paths run a prep or transform kernel and then the main one."""
     if w.M == 1:
         return 2 if (w.fmt == "PTQ1_0_G128" and w.k > 8192) else 1
+    if w.fmt == "PTQ1_0_G128" and w.M <= 8:
+        return 2 if w.k > 1024 else 1
     return 2
 
 

@@ -338,8 +338,8 @@ int gemm_tc_launch(const TcPlan &plan, const uint8_t *payload, const ninfer_row_
     int st = device_error_word(&p.err);
     if (st) return st;
     st = encode_2d(&p.amap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, xr, g.k, M, g.k * 2, kBK, kBM, true);
-    if (!st) st = encode_rows(&p.cmap, payload + g.base_offset, g.base_row_bytes, g.n, 1, 16, kBN, false);
-    if (!st) st = encode_rows(&p.smap, payload + g.scale_offset, g.scale_row_bytes, g.n, 1, 16, kBN, false);
+    if (!st) st = encode_rows(&p.cmap, payload + g.base_offset, g.base_row_bytes, g.n, 16, kBN, false);
+    if (!st) st = encode_rows(&p.smap, payload + g.scale_offset, g.scale_row_bytes, g.n, 16, kBN, false);
     if (st) return st;
     e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.smem);
     if (e != cudaSuccess) return fail(NINFER_ERR_CUDA, "prefill: smem attribute: %s", cudaGetErrorString(e));

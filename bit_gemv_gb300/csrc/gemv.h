@@ -19,10 +19,15 @@ int device_info(DeviceInfo *out);
 // Device address of the library's error word on the current device.
 int device_error_word(uint32_t **out);
 
-// Row ranges of a plane as a byte tensor {row_bytes, rows, ctas} (3-D when
-// ctas > 1): boxes of box_bytes x box_rows, optionally 128-byte swizzled.
-int encode_rows(CUtensorMap *map, const uint8_t *addr, uint64_t row_bytes, uint64_t rows, uint64_t ctas,
-                uint32_t box_bytes, uint32_t box_rows, bool swizzle128);
+// Rows of a plane as a 2-D byte tensor {row_bytes, rows}, for 2-D box loads:
+// boxes of box_bytes x box_rows, optionally 128-byte swizzled.
+int encode_rows(CUtensorMap *map, const uint8_t *addr, uint64_t row_bytes, uint64_t rows, uint32_t box_bytes,
+                uint32_t box_rows, bool swizzle128);
+// Equal row ranges of a plane as a 3-D byte tensor {row_bytes, rows, tiles},
+// for 3-D box loads (always rank 3, also for a single tile), so that a box never
+// reads past the end of its own range.
+int encode_row_tiles(CUtensorMap *map, const uint8_t *addr, uint64_t row_bytes, uint64_t rows, uint64_t tiles,
+                     uint32_t box_bytes, uint32_t box_rows, bool swizzle128);
 
 // A 2-D tensor map over a row-major array: `inner` elements per row, `outer`
 // rows, rows `row_stride_bytes` apart; boxes of box_inner x box_outer.
@@ -69,6 +74,21 @@ bool gemv_pq2_mma_plan(const ninfer_row_split_geometry &g, uint64_t M, bool rota
 int gemv_pq2_mma_launch(const MmaPlan &plan, const uint8_t *payload, const ninfer_row_split_geometry &g, const void *x,
                         int x_dtype, const uint16_t *signs, void *y, int y_dtype, uint64_t M, void *workspace,
                         cudaStream_t stream, bool pdl);
+
+// 1 <= M <= 8, PTQ1_0_G128: binary16 mma.sync kernel split over the 1024-blocks
+// of k, plus a reduction kernel over the blocks (gemv_ptq1_mma.cu).
+struct Ptq1MmaPlan {
+    bool ok;
+    uint32_t nblk, tiles, rows_per_tile, nslots;
+    uint32_t off_ring, off_rot, off_frag, off_part, off_bar, off_cnt, smem;
+    uint64_t n_pad;
+    uint64_t workspace;
+};
+bool gemv_ptq1_mma_plan(const ninfer_row_split_geometry &g, uint64_t M, bool rotate, int sms, int smem_limit,
+                        Ptq1MmaPlan *plan);
+int gemv_ptq1_mma_launch(const Ptq1MmaPlan &plan, const uint8_t *payload, const ninfer_row_split_geometry &g,
+                         const void *x, int x_dtype, const uint16_t *signs, void *y, int y_dtype, uint64_t M,
+                         void *workspace, cudaStream_t stream, bool pdl);
 
 // Prefill (M > 8) tensor-core path for PQ2_0_G128 (gemm_tc.cu).
 struct TcPlan {

@@ -50,15 +50,13 @@ int encode_fn(EncodeTiledFn *out) {
 }
 }  // namespace
 
-int encode_rows(CUtensorMap *map, const uint8_t *addr, uint64_t row_bytes, uint64_t rows, uint64_t ctas,
-                uint32_t box_bytes, uint32_t box_rows, bool swizzle128) {
+namespace {
+int encode_bytes(CUtensorMap *map, const uint8_t *addr, cuuint32_t rank, const cuuint64_t (&dims)[3],
+                 const cuuint64_t (&strides)[2], uint32_t box_bytes, uint32_t box_rows, bool swizzle128) {
     EncodeTiledFn fn;
     int st = encode_fn(&fn);
     if (st) return st;
     std::memset(map, 0, sizeof *map);
-    const cuuint32_t rank = ctas > 1 ? 3 : 2;
-    const cuuint64_t dims[3] = {row_bytes, rows, ctas};
-    const cuuint64_t strides[2] = {row_bytes, row_bytes * rows};
     const cuuint32_t box[3] = {box_bytes, box_rows, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, rank, const_cast<uint8_t *>(addr), dims, strides, box, estr,
@@ -66,6 +64,21 @@ int encode_rows(CUtensorMap *map, const uint8_t *addr, uint64_t row_bytes, uint6
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(NINFER_ERR_CUDA, "tensor map encode failed (CUresult %d)", (int)r);
     return NINFER_OK;
+}
+}  // namespace
+
+int encode_rows(CUtensorMap *map, const uint8_t *addr, uint64_t row_bytes, uint64_t rows, uint32_t box_bytes,
+                uint32_t box_rows, bool swizzle128) {
+    const cuuint64_t dims[3] = {row_bytes, rows, 1};
+    const cuuint64_t strides[2] = {row_bytes, row_bytes * rows};
+    return encode_bytes(map, addr, 2, dims, strides, box_bytes, box_rows, swizzle128);
+}
+
+int encode_row_tiles(CUtensorMap *map, const uint8_t *addr, uint64_t row_bytes, uint64_t rows, uint64_t tiles,
+                     uint32_t box_bytes, uint32_t box_rows, bool swizzle128) {
+    const cuuint64_t dims[3] = {row_bytes, rows, tiles};
+    const cuuint64_t strides[2] = {row_bytes, row_bytes * rows};
+    return encode_bytes(map, addr, 3, dims, strides, box_bytes, box_rows, swizzle128);
 }
 
 int encode_2d(CUtensorMap *map, CUtensorMapDataType dtype, uint32_t elem_bytes, const void *addr, uint64_t inner,

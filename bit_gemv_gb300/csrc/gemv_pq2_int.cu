@@ -351,14 +351,14 @@ int gemv_pq2_int_launch(const IntPlan &plan, const uint8_t *payload, const ninfe
     if (st) return st;
     const uint64_t R = plan.rows_per_cta, G = plan.grid, last_rows = g.n - (G - 1) * R;
     if (G > 1) {
-        st = encode_rows(&p.wmap_main, base, g.base_row_bytes, R, G - 1, 128, kRows, true);
-        if (!st) st = encode_rows(&p.smap_main, scale, g.scale_row_bytes, R, G - 1, 16, kRows, false);
+        st = encode_row_tiles(&p.wmap_main, base, g.base_row_bytes, R, G - 1, 128, kRows, true);
+        if (!st) st = encode_row_tiles(&p.smap_main, scale, g.scale_row_bytes, R, G - 1, 16, kRows, false);
         if (st) return st;
     }
-    st = encode_rows(&p.wmap_last, base + (G - 1) * R * g.base_row_bytes, g.base_row_bytes, last_rows, 1, 128, kRows,
+    st = encode_rows(&p.wmap_last, base + (G - 1) * R * g.base_row_bytes, g.base_row_bytes, last_rows, 128, kRows,
                      true);
     if (!st)
-        st = encode_rows(&p.smap_last, scale + (G - 1) * R * g.scale_row_bytes, g.scale_row_bytes, last_rows, 1, 16,
+        st = encode_rows(&p.smap_last, scale + (G - 1) * R * g.scale_row_bytes, g.scale_row_bytes, last_rows, 16,
                          kRows, false);
     if (st) return st;
     cudaError_t e = cudaFuncSetAttribute(gemv_pq2_int_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.smem);

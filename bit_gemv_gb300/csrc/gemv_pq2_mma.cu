@@ -287,6 +287,7 @@ bool gemv_pq2_mma_plan(const ninfer_row_split_geometry &g, uint64_t M, bool rota
     *plan = MmaPlan{};
     if (M < 2 || M > 8) return false;
     if (rotate && g.k % 1024) return false;
+    if (g.k % 8) return false;     // rows of x after the first stay 16-byte aligned for the vector loads
     if (g.scale_row_bytes % 16 || g.base_row_bytes % 16 || g.payload_bytes % 16) return false;
     if (g.k > (1u << 24) || g.n > (1ull << 31)) return false;
     const uint32_t groups = (uint32_t)g.groups_per_row;
@@ -359,14 +360,14 @@ int gemv_pq2_mma_launch(const MmaPlan &plan, const uint8_t *payload, const ninfe
     if (st) return st;
     const uint64_t R = plan.rows_per_cta, G = plan.grid, last_rows = g.n - (G - 1) * R;
     if (G > 1) {
-        st = encode_rows(&p.wmap_main, base, g.base_row_bytes, R, G - 1, 128, kRows, true);
-        if (!st) st = encode_rows(&p.smap_main, scale, g.scale_row_bytes, R, G - 1, 16, kRows, false);
+        st = encode_row_tiles(&p.wmap_main, base, g.base_row_bytes, R, G - 1, 128, kRows, true);
+        if (!st) st = encode_row_tiles(&p.smap_main, scale, g.scale_row_bytes, R, G - 1, 16, kRows, false);
         if (st) return st;
     }
-    st = encode_rows(&p.wmap_last, base + (G - 1) * R * g.base_row_bytes, g.base_row_bytes, last_rows, 1, 128, kRows,
+    st = encode_rows(&p.wmap_last, base + (G - 1) * R * g.base_row_bytes, g.base_row_bytes, last_rows, 128, kRows,
                      true);
     if (!st)
-        st = encode_rows(&p.smap_last, scale + (G - 1) * R * g.scale_row_bytes, g.scale_row_bytes, last_rows, 1, 16,
+        st = encode_rows(&p.smap_last, scale + (G - 1) * R * g.scale_row_bytes, g.scale_row_bytes, last_rows, 16,
                          kRows, false);
     if (st) return st;
     cudaError_t e = cudaFuncSetAttribute(gemv_pq2_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.smem);

@@ -519,16 +519,16 @@ int gemv_ptq1_int_launch(const Ptq1Plan &plan, const uint8_t *payload, const nin
     if (st) return st;
     const uint64_t R = plan.rows_per_cta, G = plan.grid, last_rows = g.n - (G - 1) * R;
     if (G > 1) {
-        st = encode_rows(&p.bmap_main, p.base, g.base_row_bytes, R, G - 1, 128, kRows, true);
-        if (!st) st = encode_rows(&p.hmap_main, p.high, g.high_row_bytes, R, G - 1, 32, kRows, false);
-        if (!st) st = encode_rows(&p.smap_main, p.scale, g.scale_row_bytes, R, G - 1, 32, kRows, false);
+        st = encode_row_tiles(&p.bmap_main, p.base, g.base_row_bytes, R, G - 1, 128, kRows, true);
+        if (!st) st = encode_row_tiles(&p.hmap_main, p.high, g.high_row_bytes, R, G - 1, 32, kRows, false);
+        if (!st) st = encode_row_tiles(&p.smap_main, p.scale, g.scale_row_bytes, R, G - 1, 32, kRows, false);
         if (st) return st;
     }
     const uint64_t lr = (G - 1) * R;
-    st = encode_rows(&p.bmap_last, p.base + lr * g.base_row_bytes, g.base_row_bytes, last_rows, 1, 128, kRows, true);
-    if (!st) st = encode_rows(&p.hmap_last, p.high + lr * g.high_row_bytes, g.high_row_bytes, last_rows, 1, 32, kRows, false);
+    st = encode_rows(&p.bmap_last, p.base + lr * g.base_row_bytes, g.base_row_bytes, last_rows, 128, kRows, true);
+    if (!st) st = encode_rows(&p.hmap_last, p.high + lr * g.high_row_bytes, g.high_row_bytes, last_rows, 32, kRows, false);
     if (!st)
-        st = encode_rows(&p.smap_last, p.scale + lr * g.scale_row_bytes, g.scale_row_bytes, last_rows, 1, 32, kRows, false);
+        st = encode_rows(&p.smap_last, p.scale + lr * g.scale_row_bytes, g.scale_row_bytes, last_rows, 32, kRows, false);
     if (st) return st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -38,13 +38,14 @@ static bool g_pdl = true;
 using namespace ninfer;
 
 namespace {
-enum class Path { kIntPq2, kIntPtq1, kMmaPq2, kTcPq2, kTiled };
+enum class Path { kIntPq2, kIntPtq1, kMmaPq2, kMmaPtq1, kTcPq2, kTiled };
 
 struct MatmulPlan {
     Path path;
     IntPlan gint;
     Ptq1Plan gptq;
     MmaPlan gmma;
+    Ptq1MmaPlan gpm;
     TcPlan gtc;
     uint64_t workspace;
 };
@@ -67,6 +68,11 @@ int plan_matmul(int fmt, const ninfer_row_split_geometry &g, uint64_t M, bool ro
     if (fmt == NINFER_PQ2_0_G128 && gemv_pq2_mma_plan(g, M, rotate, d.sms, d.smem_optin, &mp->gmma)) {
         mp->path = Path::kMmaPq2;
         mp->workspace = mp->gmma.workspace;     // the activation fragments
+        return NINFER_OK;
+    }
+    if (fmt == NINFER_PTQ1_0_G128 && M >= 2 && gemv_ptq1_mma_plan(g, M, rotate, d.sms, d.smem_optin, &mp->gpm)) {
+        mp->path = Path::kMmaPtq1;
+        mp->workspace = mp->gpm.workspace;      // per-block partial sums
         return NINFER_OK;
     }
     if (fmt == NINFER_PQ2_0_G128 && gemm_tc_plan(g, M, d.smem_optin, &mp->gtc)) {
@@ -137,6 +143,8 @@ extern "C" int ninfer_ternary_matmul(int fmt, const uint8_t *payload, uint64_t p
         return gemv_ptq1_int_launch(mp.gptq, payload, g, x, x_dtype, signs_bf16, y, y_dtype, workspace, s, g_pdl);
     if (mp.path == Path::kMmaPq2)
         return gemv_pq2_mma_launch(mp.gmma, payload, g, x, x_dtype, signs_bf16, y, y_dtype, M, workspace, s, g_pdl);
+    if (mp.path == Path::kMmaPtq1)
+        return gemv_ptq1_mma_launch(mp.gpm, payload, g, x, x_dtype, signs_bf16, y, y_dtype, M, workspace, s, g_pdl);
     if (mp.path == Path::kTcPq2)
         return gemm_tc_launch(mp.gtc, payload, g, x, x_dtype, signs_bf16, y, y_dtype, M, workspace, s);
     const PlaneView p = make_view(payload, g, fmt);

@@ -64,11 +64,49 @@ def test_matmul_tiny_workload():
 
 @pytest.mark.parametrize("fmt", ["PQ2_0_G128", "PTQ1_0_G128"])
 @pytest.mark.parametrize("n,k,M", [(300, 2048, 1), (300, 2048, 8), (77, 3072, 3), (1, 1024, 1), (17, 5120, 2),
-                                   (1000, 1024, 5), (31, 2048, 1), (517, 5120, 1), (50001, 1024, 1)])
+                                   (1000, 1024, 5), (31, 2048, 1), (517, 5120, 1), (50001, 1024, 1),
+                                   (150, 2048, 1), (80, 2048, 1), (150, 2048, 4)])
 def test_matmul_small_shapes(fmt, n, k, M):
     c = synth.make_case("gateup", n=n, k=k, M=M, seed=n * 7 + k + M)
     y = run_matmul(fmt, c)
     ref = oracle_matmul_rows(fmt, c, np.arange(n))
+    assert oracle.max_rel_error(y, ref) <= TOL_DECODE
+
+
+@pytest.mark.parametrize("n,k,M", [(4099, 3072, 7), (2100, 2048, 8), (63, 9216, 4), (16, 1024, 2)])
+def test_matmul_ptq1_block_split(n, k, M):
+    """PTQ1_0 with 2 <= M <= 8: the CTA grid is 1024-blocks x row tiles (each
+    tile a multiple of 16 rows, the last one ragged) and the per-block partial
+    sums are added by a second kernel; n % 4 != 0 pads the partial rows."""
+    c = synth.make_case("down", n=n, k=k, M=M, seed=n + k + M)
+    y = run_matmul("PTQ1_0_G128", c)
+    ref = oracle_matmul_rows("PTQ1_0_G128", c, np.arange(n))
+    assert oracle.max_rel_error(y, ref) <= TOL_DECODE
+
+
+@pytest.mark.slow
+def test_matmul_ptq1_ring_refill():
+    """Row tiles longer than the shared-memory ring (more than six items of 128
+    rows per CTA at k = 17408): slots are released and refilled mid-tile.
+    Sampled rows from every tile."""
+    c = synth.make_case("down", n=8000, k=17408, M=3, seed=44)
+    y = run_matmul("PTQ1_0_G128", c)
+    rng = np.random.default_rng(7)
+    rows = np.unique(np.concatenate([np.arange(0, 8000, 97), [7999], rng.integers(0, 8000, 400)]))
+    ref = oracle_matmul_rows("PTQ1_0_G128", c, rows)
+    assert oracle.max_rel_error(y[:, rows], ref) <= TOL_DECODE
+
+
+@pytest.mark.parametrize("fmt", ["PQ2_0_G128", "PTQ1_0_G128"])
+@pytest.mark.parametrize("n,k,M", [(70, 1000, 4), (40, 1001, 3), (33, 2040, 1)])
+def test_matmul_unrotated_ragged_k(fmt, n, k, M):
+    """Raw input with k just under a multiple of 1024: the decode kernels take
+    k = 1000 and 2040 (x rows stay 16-byte aligned, the missing elements of the
+    last block are zero); k = 1001 leaves the rows of x unaligned and must be
+    served by the general path."""
+    c = synth.make_case("gateup", n=n, k=k, M=M, seed=n + k)
+    y = run_matmul(fmt, c, rotate=False)
+    ref = oracle_matmul_rows(fmt, c, np.arange(n), rotate=False)
     assert oracle.max_rel_error(y, ref) <= TOL_DECODE
 
 
