@@ -80,7 +80,7 @@ int gemv_pq2_mma_launch(const MmaPlan &plan, const uint8_t *payload, const ninfe
 struct Ptq1MmaPlan {
     bool ok;
     uint32_t nblk, tiles, rows_per_tile, nslots;
-    uint32_t off_ring, off_rot, off_frag, off_part, off_bar, off_cnt, smem;
+    uint32_t off_ring, off_lut, off_rot, off_frag, off_bar, off_cnt, smem;
     uint64_t n_pad;
     uint64_t workspace;
 };

@@ -67,6 +67,10 @@ constexpr uint32_t kLutBytes = 256 * 32 * 4;
 constexpr uint32_t kFragBytes = 8 * 8 * 32 * 8;            // 8 groups x 8 k-steps x 32 lanes x 2 registers
 constexpr uint32_t kFxBytes = (8 * 8 + 8) * 4;             // X per (group, row), then 2^-E per row
 constexpr uint32_t kPartBytes = 2 * 8 * 32 * 16;           // double-buffered float4 per lane of the odd warps
+constexpr uint32_t kRotBytes = kPairs * kRotScratch;         // rotation tiles; then the slice partials
+static_assert(kPartBytes <= kRotBytes, "slice partials live in the rotation tiles");
+constexpr bool kHoldB = true;     // keep the warp's B fragments in registers (else read them per k-step)
+constexpr bool kSplitC = false;   // two accumulator chains per group (even / odd k-steps)
 
 struct Ptq1MmaParams {
     CUtensorMap bmap_main, bmap_last;   // base rows {row bytes, R rows, tile} / last tile {row bytes, rows}
@@ -80,7 +84,7 @@ struct Ptq1MmaParams {
     uint32_t k, M, rows_per_tile;
     int x_dtype, y_dtype;
     uint32_t nslots;
-    uint32_t off_ring, off_rot, off_frag, off_part, off_bar, off_cnt;
+    uint32_t off_ring, off_lut, off_rot, off_frag, off_bar, off_cnt;
     uint32_t *err;
 };
 
@@ -113,28 +117,6 @@ __device__ __forceinline__ uint32_t digits01(uint32_t e) { return e & 0x00030003
 __device__ __forceinline__ uint32_t digits23(uint32_t e) { return __byte_perm(e, 0u, 0x4341); }    // (t2, t3)
 __device__ __forceinline__ uint32_t digits44(uint32_t ea, uint32_t eb) {                           // (t4 of a, t4 of b)
     return (__byte_perm(ea, eb, 0x5410) >> 2) & 0x00030003u;
-}
-
-// Position of weight w (0..127) of a group in the K order: k-step s, lane c of
-// the quad and slot pos (0: K = 2c, 1: 2c + 1, 2: 2c + 8, 3: 2c + 9).
-__device__ __forceinline__ void k_slot(uint32_t w, uint32_t &s, uint32_t &c, uint32_t &pos) {
-    if (w < 120) {
-        const uint32_t j = w / 5, i = w % 5;
-        c = j & 3;
-        if (i < 4) {
-            s = j >> 2;
-            pos = i;
-        } else {
-            const uint32_t q = j >> 2;     // base word of byte j
-            s = q < 4 ? 6 : 7;
-            pos = q < 4 ? q : q - 4;
-        }
-    } else {
-        const uint32_t h = (w - 120) >> 2, d = (w - 120) & 3;
-        c = 2 * h + (d >> 1);
-        s = 7;
-        pos = 2 + (d & 1);
-    }
 }
 
 // Item i of the CTA's tile (rows 128 i .. 128 i + 127 of the tile, groups of
@@ -192,56 +174,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ptq1_mma_kernel(const __grid
         *issued = ring_to;
     }
 
-    // B fragments of block b: warp pair m rotates activation row m
-    const uint32_t m = warp >> 1;
-    const int t = tid & 63;
-    const XSource xsrc{p.x, p.signs, p.k, p.x_dtype};
-    float d[16];
-    if (p.signs && m < p.M) load_signs16(xsrc, b, t, d);     // read-only parameter: before the dependency wait
-    pdl_launch_dependents();
-    pdl_wait();          // x may come from the preceding kernel
-    uint16_t *frag = reinterpret_cast<uint16_t *>(smem + p.off_frag);
-    float *fx = reinterpret_cast<float *>(smem + p.off_frag + kFragBytes);     // X[g * 8 + m], then 2^-E[m]
-    {
-        float v[16];
-        int E = 0;
-        if (m < p.M) {
-            XSource xs = xsrc;
-            xs.x = static_cast<const uint8_t *>(p.x) + m * p.x_row_bytes;
-            load_run16(xs, b, t, v);
-            float *tile = reinterpret_cast<float *>(smem + p.off_rot + m * kRotScratch);
-            const float mx = rotate16(p.signs != nullptr, t, v, d, tile, 1 + m);
-            if (mx > 0.f) E = 10 - ilogbf(mx);      // max |xr * 2^E| < 2^11
-            E = max(-100, min(100, E));
-        } else {
-#pragma unroll
-            for (int r = 0; r < 16; ++r) v[r] = 0.f;
-        }
-        const float up = ldexpf(1.f, E);
-        float gsum[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            // v[r] is element 256 (r / 4) + 4t + r % 4 of the block: group 2 (r / 4) + t / 32
-            const uint32_t e = 256 * (r >> 2) + 4 * t + (r & 3), g = e >> 7;
-            uint32_t s, c, pos;
-            k_slot(e & 127, s, c, pos);
-            const __half h = __float2half_rn(v[r] * up);
-            gsum[r >> 2] += __half2float(h);
-            frag[((g * 8 + s) * 32 + 4 * m + c) * 4 + pos] = __half_as_ushort(h);
-        }
-#pragma unroll
-        for (int a = 0; a < 4; ++a) {
-            float sum = gsum[a];
-#pragma unroll
-            for (int sh = 16; sh > 0; sh >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, sh);
-            if (lane == 0) fx[(2 * a + (t >> 5)) * 8 + m] = sum;
-        }
-        if (t == 0) fx[64 + m] = m < p.M ? ldexpf(1.f, -E) : 0.f;
-    }
-    __syncthreads();     // fragments complete; the rotation scratch is free
     // digit table, lane-private copies: entry (B, l) at word 32 B + l; thread
-    // tid computes entry tid / 2 and writes 16 of its copies
-    uint32_t *lut = reinterpret_cast<uint32_t *>(smem + p.off_rot);
+    // tid computes entry tid / 2 and writes 16 of its copies (before the
+    // dependency wait: it depends on nothing)
+    uint32_t *lut = reinterpret_cast<uint32_t *>(smem + p.off_lut);
     {
         const uint32_t W = digit_entry((uint32_t)tid >> 1);
         uint4 *dst = reinterpret_cast<uint4 *>(lut + (tid >> 1) * 32 + 16 * (tid & 1));
@@ -249,27 +185,100 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ptq1_mma_kernel(const __grid
 #pragma unroll
         for (int i = 0; i < 4; ++i) dst[i] = w4;
     }
+    // B fragments of block b: warp pair m rotates activation row m into
+    // binary16 (natural order, in its own rotation tile), then all threads
+    // gather the fragments from those rows
+    const uint32_t m = warp >> 1;
+    const int t = tid & 63;
+    const XSource xsrc{p.x, p.signs, p.k, p.x_dtype};
+    float d[16];
+    if (p.signs && m < p.M) load_signs16(xsrc, b, t, d);     // read-only parameter: before the dependency wait
+    pdl_launch_dependents();
+    pdl_wait();          // x may come from the preceding kernel
+    float *fx = reinterpret_cast<float *>(smem + p.off_frag + kFragBytes);     // X[g * 8 + m], then 2^-E[m]
+    {
+        float *tile = reinterpret_cast<float *>(smem + p.off_rot + m * kRotScratch);
+        float v[16];
+        int E = 0;
+        if (m < p.M) {
+            XSource xs = xsrc;
+            xs.x = static_cast<const uint8_t *>(p.x) + m * p.x_row_bytes;
+            load_run16(xs, b, t, v);
+            const float mx = rotate16(p.signs != nullptr, t, v, d, tile, 1 + m);
+            if (mx > 0.f) E = 10 - ilogbf(mx);      // max |xr * 2^E| < 2^11
+            E = max(-100, min(100, E));
+        } else {
+#pragma unroll
+            for (int r = 0; r < 16; ++r) v[r] = 0.f;
+        }
+        // v[r] is element 256 (r / 4) + 4t + r % 4 of the block (group 2 (r / 4) + t / 32)
+        const float up = ldexpf(1.f, E);
+        uint2 *row = reinterpret_cast<uint2 *>(tile);     // 1024 binary16, elements 4j .. 4j + 3 per uint2
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+            __half h[4];
+            float sum = 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                h[i] = __float2half_rn(v[4 * a + i] * up);
+                sum += __half2float(h[i]);
+            }
+            row[64 * a + t] = make_uint2((uint32_t)__half_as_ushort(h[0]) | (uint32_t)__half_as_ushort(h[1]) << 16,
+                                         (uint32_t)__half_as_ushort(h[2]) | (uint32_t)__half_as_ushort(h[3]) << 16);
+#pragma unroll
+            for (int sh = 16; sh > 0; sh >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, sh);
+            if (lane == 0) fx[(2 * a + (t >> 5)) * 8 + m] = sum;
+        }
+        if (t == 0) fx[64 + m] = m < p.M ? ldexpf(1.f, -E) : 0.f;
+    }
+    __syncthreads();     // binary16 rows complete
+    {
+        // fragment word u = (g * 8 + s) * 32 + lane of column m = lane / 4, quad lane c
+        // = lane % 4: the weights that the group's K order (above) puts at k-step s,
+        // slots 2c, 2c + 1, 2c + 8, 2c + 9
+        uint2 *fw = reinterpret_cast<uint2 *>(smem + p.off_frag);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t u = (uint32_t)tid + 512 * i, s = (u >> 5) & 7, g = u >> 8, mm = lane >> 2, c = lane & 3;
+            const uint16_t *st = reinterpret_cast<const uint16_t *>(smem + p.off_rot + mm * kRotScratch) + 128 * g;
+            uint32_t w[4];
+            if (s < 6) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) w[q] = st[20 * s + 5 * c + q];
+            } else if (s == 6) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) w[q] = st[5 * c + 20 * q + 4];
+            } else {
+                w[0] = st[5 * c + 84];
+                w[1] = st[5 * c + 104];
+                w[2] = st[120 + 2 * c];
+                w[3] = st[121 + 2 * c];
+            }
+            fw[u] = make_uint2(w[0] | w[1] << 16, w[2] | w[3] << 16);
+        }
+    }
+    __syncthreads();     // fragments complete; the rotation tiles are free (they hold the slice partials next)
+    uint16_t *frag = reinterpret_cast<uint16_t *>(smem + p.off_frag);
     const uint32_t slice = warp >> 1, gh = warp & 1, g4 = lane >> 2, c = lane & 3;
     // this warp's B fragments (groups 4 gh .. 4 gh + 3), X and 2^-E of columns 2c, 2c + 1
     uint2 bfr[4][8];
     float X0[4], X1[4];
-    {
-        const uint2 *fw = reinterpret_cast<const uint2 *>(frag);
+    const uint2 *fw = reinterpret_cast<const uint2 *>(frag) + (4 * gh) * 8 * 32 + lane;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < 4; ++q) {
+        if (kHoldB) {
 #pragma unroll
-            for (int s = 0; s < 8; ++s) bfr[q][s] = fw[((4 * gh + q) * 8 + s) * 32 + lane];
-            X0[q] = fx[(4 * gh + q) * 8 + 2 * c];
-            X1[q] = fx[(4 * gh + q) * 8 + 2 * c + 1];
+            for (int s = 0; s < 8; ++s) bfr[q][s] = fw[(q * 8 + s) * 32];
         }
+        X0[q] = fx[(4 * gh + q) * 8 + 2 * c];
+        X1[q] = fx[(4 * gh + q) * 8 + 2 * c + 1];
     }
     const float sc0 = fx[64 + 2 * c], sc1 = fx[64 + 2 * c + 1];
-    __syncthreads();     // digit table complete
 
     const uint32_t lutl = smem_u32(lut) + 4 * lane;
     const uint32_t selc = 0x4440u | c;          // byte c of a word to byte 0, zeros above
     const uint32_t selh = (c & 1) ? 0x4341u : 0x4240u;     // digits (t2, t3) or (t0, t1) of a high byte
-    float4 *part = reinterpret_cast<float4 *>(smem + p.off_part);
+    float4 *part = reinterpret_cast<float4 *>(smem + p.off_rot);
     const bool refill = nitems > p.nslots;
     bool ok = true;
     uint32_t slot = 0, phase = 0;
@@ -295,19 +304,25 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ptq1_mma_kernel(const __grid
                     wB[2 * i + 1] = bb.y;
                 }
                 uint32_t eA[6], eB[6];
-                float C[4] = {0.f, 0.f, 0.f, 0.f};
+                float C[4] = {0.f, 0.f, 0.f, 0.f}, D[4] = {0.f, 0.f, 0.f, 0.f};
+                auto bf = [&](int st) { return kHoldB ? bfr[q][st] : fw[(q * 8 + st) * 32]; };
 #pragma unroll
-                for (int s = 0; s < 6; ++s) {
-                    eA[s] = lds32(lutl + (__byte_perm(wA[s], 0u, selc) << 7));
-                    eB[s] = lds32(lutl + (__byte_perm(wB[s], 0u, selc) << 7));
-                    mma16816(C, digits01(eA[s]), digits01(eB[s]), digits23(eA[s]), digits23(eB[s]), bfr[q][s]);
+                for (int st = 0; st < 6; ++st) {
+                    eA[st] = lds32(lutl + (__byte_perm(wA[st], 0u, selc) << 7));
+                    eB[st] = lds32(lutl + (__byte_perm(wB[st], 0u, selc) << 7));
+                    mma16816(kSplitC && (st & 1) ? D : C, digits01(eA[st]), digits01(eB[st]), digits23(eA[st]),
+                             digits23(eB[st]), bf(st));
                 }
                 mma16816(C, digits44(eA[0], eA[1]), digits44(eB[0], eB[1]), digits44(eA[2], eA[3]),
-                         digits44(eB[2], eB[3]), bfr[q][6]);
+                         digits44(eB[2], eB[3]), bf(6));
                 const uint32_t hA = lds32(lutl + (lds8(sideA + 2 * gl + (c >> 1)) << 7));
                 const uint32_t hB = lds32(lutl + (lds8(sideB + 2 * gl + (c >> 1)) << 7));
-                mma16816(C, digits44(eA[4], eA[5]), digits44(eB[4], eB[5]), __byte_perm(hA, 0u, selh) & 0x00030003u,
-                         __byte_perm(hB, 0u, selh) & 0x00030003u, bfr[q][7]);
+                mma16816(kSplitC ? D : C, digits44(eA[4], eA[5]), digits44(eB[4], eB[5]),
+                         __byte_perm(hA, 0u, selh) & 0x00030003u, __byte_perm(hB, 0u, selh) & 0x00030003u, bf(7));
+                if (kSplitC) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) C[i] += D[i];
+                }
                 const float sA = __half2float(__ushort_as_half((unsigned short)lds16(sideA + kSideBox + 2 * gl)));
                 const float sB = __half2float(__ushort_as_half((unsigned short)lds16(sideB + kSideBox + 2 * gl)));
                 acc[0] = fmaf(sA, fmaf(C[0], 16777216.f, -X0[q]), acc[0]);
@@ -371,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ptq1_mma_kernel(const __grid
 }
 
 // y[m][r] = sum over blocks b (in order) of P[b][m][r]; four rows per thread.
-__global__ void __launch_bounds__(256) ptq1_reduce_kernel(const float *part, uint32_t nblk, uint32_t M, uint64_t n,
+__global__ void __launch_bounds__(128) ptq1_reduce_kernel(const float *part, uint32_t nblk, uint32_t M, uint64_t n,
                                                           uint64_t n_pad, void *y, int y_dtype) {
     pdl_launch_dependents();
     pdl_wait();          // the partial sums come from the preceding kernel
@@ -380,14 +395,24 @@ __global__ void __launch_bounds__(256) ptq1_reduce_kernel(const float *part, uin
     if (q >= (uint64_t)M * per_m) return;
     const uint32_t m = (uint32_t)(q / per_m);
     const uint64_t j = q % per_m;
-    const float4 *src = reinterpret_cast<const float4 *>(part);
+    const float4 *src = reinterpret_cast<const float4 *>(part) + (uint64_t)m * per_m + j;
+    const uint64_t bstride = (uint64_t)M * per_m;
     float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (uint32_t bb = 0; bb < nblk; ++bb) {
-        const float4 v = __ldcg(src + ((uint64_t)bb * M + m) * per_m + j);
-        s.x += v.x;
-        s.y += v.y;
-        s.z += v.z;
-        s.w += v.w;
+    for (uint32_t bb = 0; bb < nblk; bb += 16) {
+        // sixteen blocks' loads in flight, then their sums in block order
+        float4 v[16];
+#pragma unroll
+        for (uint32_t i = 0; i < 16; ++i)
+            if (bb + i < nblk) v[i] = __ldcg(src + (uint64_t)(bb + i) * bstride);
+#pragma unroll
+        for (uint32_t i = 0; i < 16; ++i) {
+            if (bb + i < nblk) {
+                s.x += v[i].x;
+                s.y += v[i].y;
+                s.z += v[i].z;
+                s.w += v[i].w;
+            }
+        }
     }
     const float o[4] = {s.x, s.y, s.z, s.w};
 #pragma unroll
@@ -417,10 +442,9 @@ bool gemv_ptq1_mma_plan(const ninfer_row_split_geometry &g, uint64_t M, bool rot
     const uint64_t R = ((g.n + T - 1) / T + 15) / 16 * 16;
     T = (g.n + R - 1) / R;
     const uint32_t nitem = (uint32_t)((R + kRows - 1) / kRows);
-    const uint32_t rot_bytes = std::max<uint32_t>(kPairs * kRotScratch, kLutBytes);
     const uint32_t bar_bytes = kMaxSlots * 8;
     const uint32_t cnt_bytes = (kMaxSlots + 4) * 4;
-    const uint32_t fixed = rot_bytes + kFragBytes + kFxBytes + kPartBytes + bar_bytes + cnt_bytes;
+    const uint32_t fixed = kLutBytes + kRotBytes + kFragBytes + kFxBytes + bar_bytes + cnt_bytes;
     if ((int64_t)fixed + kItemBytes > smem_limit) return false;
     uint32_t nslots = std::min<uint32_t>(kMaxSlots, (uint32_t)((smem_limit - (int)fixed) / (int)kItemBytes));
     nslots = std::min(nslots, nitem);
@@ -433,12 +457,12 @@ bool gemv_ptq1_mma_plan(const ninfer_row_split_geometry &g, uint64_t M, bool rot
     uint32_t off = 0;
     plan->off_ring = off;
     off += nslots * kItemBytes;
+    plan->off_lut = off;
+    off += kLutBytes;
     plan->off_rot = off;
-    off += rot_bytes;
+    off += kRotBytes;
     plan->off_frag = off;
     off += kFragBytes + kFxBytes;
-    plan->off_part = off;
-    off += kPartBytes;
     plan->off_bar = off;
     off += bar_bytes;
     plan->off_cnt = off;
@@ -469,9 +493,9 @@ int gemv_ptq1_mma_launch(const Ptq1MmaPlan &plan, const uint8_t *payload, const 
     p.y_dtype = y_dtype;
     p.nslots = plan.nslots;
     p.off_ring = plan.off_ring;
+    p.off_lut = plan.off_lut;
     p.off_rot = plan.off_rot;
     p.off_frag = plan.off_frag;
-    p.off_part = plan.off_part;
     p.off_bar = plan.off_bar;
     p.off_cnt = plan.off_cnt;
     int st = device_error_word(&p.err);
@@ -506,8 +530,8 @@ int gemv_ptq1_mma_launch(const Ptq1MmaPlan &plan, const uint8_t *payload, const 
     if (plan.nblk > 1) {
         const uint64_t threads = M * plan.n_pad / 4;
         cudaLaunchConfig_t rc = {};
-        rc.gridDim = dim3((unsigned)((threads + 255) / 256));
-        rc.blockDim = dim3(256);
+        rc.gridDim = dim3((unsigned)((threads + 127) / 128));
+        rc.blockDim = dim3(128);
         rc.stream = stream;
         rc.attrs = attr;
         rc.numAttrs = 1;
