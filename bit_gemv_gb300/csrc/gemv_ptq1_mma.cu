@@ -89,17 +89,11 @@ struct Ptq1MmaParams {
 };
 
 __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint2 b) {
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
         "{%0, %1, %2, %3};"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b.x), "r"(b.y));
-}
-
-__device__ __forceinline__ uint32_t lds8(uint32_t addr) {
-    uint32_t v;
-    asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(addr));
-    return v;
 }
 
 // Digit-table entry of code byte B.
@@ -275,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ptq1_mma_kernel(const __grid
     }
     const float sc0 = fx[64 + 2 * c], sc1 = fx[64 + 2 * c + 1];
 
-    const uint32_t lutl = smem_u32(lut) + 4 * lane;
+    const uint32_t *lutl = lut + lane;        // lane-private copy: entry B at lutl[32 B]
     const uint32_t selc = 0x4440u | c;          // byte c of a word to byte 0, zeros above
     const uint32_t selh = (c & 1) ? 0x4341u : 0x4240u;     // digits (t2, t3) or (t0, t1) of a high byte
     float4 *part = reinterpret_cast<float4 *>(smem + p.off_rot);
@@ -287,44 +281,49 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ptq1_mma_kernel(const __grid
         float acc[4] = {0.f, 0.f, 0.f, 0.f};      // rows g4, g4 + 8 of the slice x columns 2c, 2c + 1
         const uint32_t item_rows = rows - it * kRows;
         if (ok && slice * 16 < item_rows) {
-            const uint32_t sb = smem_u32(smem + p.off_ring) + slot * kItemBytes;
+            const uint8_t *sb = smem + p.off_ring + slot * kItemBytes;
             const uint32_t rA = slice * 16 + g4;
-            const uint32_t baseA = sb + gh * kBaseBox + rA * 96, baseB = baseA + 8 * 96;
-            const uint32_t sideA = sb + 2 * kBaseBox + rA * 16, sideB = sideA + 8 * 16;
+            const uint8_t *baseA = sb + gh * kBaseBox + rA * 96, *baseB = baseA + 8 * 96;
+            const uint8_t *sideA = sb + 2 * kBaseBox + rA * 16, *sideB = sideA + 8 * 16;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const uint32_t gl = 4 * gh + q;
+                // the group's 24 base bytes of rows A and B: one 16-byte and one 8-byte load each
                 uint32_t wA[6], wB[6];
-#pragma unroll
-                for (int i = 0; i < 3; ++i) {
-                    const uint2 a = lds64(baseA + 24 * q + 8 * i), bb = lds64(baseB + 24 * q + 8 * i);
-                    wA[2 * i] = a.x;
-                    wA[2 * i + 1] = a.y;
-                    wB[2 * i] = bb.x;
-                    wB[2 * i + 1] = bb.y;
+                {
+                    const int o16 = (q & 1) ? 8 : 0, o8 = (q & 1) ? 0 : 16;     // 24q is 16-aligned for even q
+                    const uint4 a4 = *reinterpret_cast<const uint4 *>(baseA + 24 * q + o16);
+                    const uint4 b4 = *reinterpret_cast<const uint4 *>(baseB + 24 * q + o16);
+                    const uint2 a2 = *reinterpret_cast<const uint2 *>(baseA + 24 * q + o8);
+                    const uint2 b2 = *reinterpret_cast<const uint2 *>(baseB + 24 * q + o8);
+                    const int w16 = o16 / 4, w8 = o8 / 4;
+                    wA[w16] = a4.x; wA[w16 + 1] = a4.y; wA[w16 + 2] = a4.z; wA[w16 + 3] = a4.w;
+                    wB[w16] = b4.x; wB[w16 + 1] = b4.y; wB[w16 + 2] = b4.z; wB[w16 + 3] = b4.w;
+                    wA[w8] = a2.x; wA[w8 + 1] = a2.y;
+                    wB[w8] = b2.x; wB[w8 + 1] = b2.y;
                 }
                 uint32_t eA[6], eB[6];
                 float C[4] = {0.f, 0.f, 0.f, 0.f}, D[4] = {0.f, 0.f, 0.f, 0.f};
                 auto bf = [&](int st) { return kHoldB ? bfr[q][st] : fw[(q * 8 + st) * 32]; };
 #pragma unroll
                 for (int st = 0; st < 6; ++st) {
-                    eA[st] = lds32(lutl + (__byte_perm(wA[st], 0u, selc) << 7));
-                    eB[st] = lds32(lutl + (__byte_perm(wB[st], 0u, selc) << 7));
+                    eA[st] = lutl[__byte_perm(wA[st], 0u, selc) << 5];
+                    eB[st] = lutl[__byte_perm(wB[st], 0u, selc) << 5];
                     mma16816(kSplitC && (st & 1) ? D : C, digits01(eA[st]), digits01(eB[st]), digits23(eA[st]),
                              digits23(eB[st]), bf(st));
                 }
                 mma16816(C, digits44(eA[0], eA[1]), digits44(eB[0], eB[1]), digits44(eA[2], eA[3]),
                          digits44(eB[2], eB[3]), bf(6));
-                const uint32_t hA = lds32(lutl + (lds8(sideA + 2 * gl + (c >> 1)) << 7));
-                const uint32_t hB = lds32(lutl + (lds8(sideB + 2 * gl + (c >> 1)) << 7));
+                const uint32_t hA = lutl[(uint32_t)sideA[2 * gl + (c >> 1)] << 5];
+                const uint32_t hB = lutl[(uint32_t)sideB[2 * gl + (c >> 1)] << 5];
                 mma16816(kSplitC ? D : C, digits44(eA[4], eA[5]), digits44(eB[4], eB[5]),
                          __byte_perm(hA, 0u, selh) & 0x00030003u, __byte_perm(hB, 0u, selh) & 0x00030003u, bf(7));
                 if (kSplitC) {
 #pragma unroll
                     for (int i = 0; i < 4; ++i) C[i] += D[i];
                 }
-                const float sA = __half2float(__ushort_as_half((unsigned short)lds16(sideA + kSideBox + 2 * gl)));
-                const float sB = __half2float(__ushort_as_half((unsigned short)lds16(sideB + kSideBox + 2 * gl)));
+                const float sA = __half2float(*reinterpret_cast<const __half *>(sideA + kSideBox + 2 * gl));
+                const float sB = __half2float(*reinterpret_cast<const __half *>(sideB + kSideBox + 2 * gl));
                 acc[0] = fmaf(sA, fmaf(C[0], 16777216.f, -X0[q]), acc[0]);
                 acc[1] = fmaf(sA, fmaf(C[1], 16777216.f, -X1[q]), acc[1]);
                 acc[2] = fmaf(sB, fmaf(C[2], 16777216.f, -X0[q]), acc[2]);
@@ -385,41 +384,35 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ptq1_mma_kernel(const __grid
     }
 }
 
-// y[m][r] = sum over blocks b (in order) of P[b][m][r]; four rows per thread.
+// y[m][r] = sum over blocks b (in order) of P[b][m][r]; two rows per thread,
+// with up to 32 blocks' loads in flight before their sums.
 __global__ void __launch_bounds__(128) ptq1_reduce_kernel(const float *part, uint32_t nblk, uint32_t M, uint64_t n,
                                                           uint64_t n_pad, void *y, int y_dtype) {
     pdl_launch_dependents();
     pdl_wait();          // the partial sums come from the preceding kernel
-    const uint64_t per_m = n_pad / 4;
+    const uint64_t per_m = n_pad / 2;
     const uint64_t q = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (q >= (uint64_t)M * per_m) return;
     const uint32_t m = (uint32_t)(q / per_m);
     const uint64_t j = q % per_m;
-    const float4 *src = reinterpret_cast<const float4 *>(part) + (uint64_t)m * per_m + j;
+    const float2 *src = reinterpret_cast<const float2 *>(part) + (uint64_t)m * per_m + j;
     const uint64_t bstride = (uint64_t)M * per_m;
-    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (uint32_t bb = 0; bb < nblk; bb += 16) {
-        // sixteen blocks' loads in flight, then their sums in block order
-        float4 v[16];
+    float2 s = make_float2(0.f, 0.f);
+    for (uint32_t bb = 0; bb < nblk; bb += 32) {
+        float2 v[32];
 #pragma unroll
-        for (uint32_t i = 0; i < 16; ++i)
+        for (uint32_t i = 0; i < 32; ++i)
             if (bb + i < nblk) v[i] = __ldcg(src + (uint64_t)(bb + i) * bstride);
 #pragma unroll
-        for (uint32_t i = 0; i < 16; ++i) {
+        for (uint32_t i = 0; i < 32; ++i) {
             if (bb + i < nblk) {
                 s.x += v[i].x;
                 s.y += v[i].y;
-                s.z += v[i].z;
-                s.w += v[i].w;
             }
         }
     }
-    const float o[4] = {s.x, s.y, s.z, s.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const uint64_t r = 4 * j + i;
-        if (r < n) store1(y, (uint64_t)m * n + r, y_dtype, o[i]);
-    }
+    if (2 * j < n) store1(y, (uint64_t)m * n + 2 * j, y_dtype, s.x);
+    if (2 * j + 1 < n) store1(y, (uint64_t)m * n + 2 * j + 1, y_dtype, s.y);
 }
 
 }  // namespace
@@ -528,7 +521,7 @@ int gemv_ptq1_mma_launch(const Ptq1MmaPlan &plan, const uint8_t *payload, const 
     e = cudaLaunchKernelEx(&cfg, gemv_ptq1_mma_kernel, p);
     if (e != cudaSuccess) return fail(NINFER_ERR_CUDA, "ptq1 mma gemv launch: %s", cudaGetErrorString(e));
     if (plan.nblk > 1) {
-        const uint64_t threads = M * plan.n_pad / 4;
+        const uint64_t threads = M * plan.n_pad / 2;
         cudaLaunchConfig_t rc = {};
         rc.gridDim = dim3((unsigned)((threads + 127) / 128));
         rc.blockDim = dim3(128);
