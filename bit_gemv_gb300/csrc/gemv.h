@@ -65,8 +65,8 @@ int gemv_ptq1_int_launch(const Ptq1Plan &plan, const uint8_t *payload, const nin
 // 2 <= M <= 8, PQ2_0_G128: binary16 mma.sync kernel with a prep kernel for the fragments.
 struct MmaPlan {
     bool ok;
-    uint32_t grid, rows_per_cta, nitem, nslots, pre_issue, frag_bytes;
-    uint32_t off_ring, off_frag, off_part, off_bar, off_cnt, smem;
+    uint32_t grid, rows_per_cta, nitem, nslots, pre_issue, fx_bytes;
+    uint32_t off_ring, off_frag, off_fx, off_acc, off_part, off_bar, off_cnt, smem;
     uint64_t workspace;
 };
 bool gemv_pq2_mma_plan(const ninfer_row_split_geometry &g, uint64_t M, bool rotate, int sms, int smem_limit,

@@ -22,12 +22,17 @@
 //  * Per group: y += scale * 2^-E * (2^24 * C - X)       (value = code - 1)
 // Products of binary16 operands are exact; the sums are fp32.
 //
-// Data movement (as the M = 1 kernel): one CTA per SM owns a contiguous row
-// range in tiles of 128 rows; weights stream through a ring of 34 KB items of
-// 128 rows x 8 groups (two 128-byte-swizzled code boxes and one scale box). The
-// fragments and {2^-E, X} are bulk-copied once right after the dependency wait.
-// Warp w takes the 16-row slice w / 2 of the tile and groups 4 (w % 2) ..
-// 4 (w % 2) + 3 of every item.
+// Data movement: one CTA per SM owns a contiguous row range in tiles of 128
+// rows; weights stream through a ring of 34 KB items of 128 rows x 8 groups
+// (two 128-byte-swizzled code boxes and one scale box), taken column by column:
+// item i covers groups 8j .. 8j + 7 of tile t with j = i / tiles, t = i % tiles.
+// Warp w takes the 16-row slice w / 2 and groups 4 (w % 2) .. 4 (w % 2) + 3 of
+// every item, so it keeps those four groups' B fragments (64 registers) for a
+// whole column of tiles instead of re-reading them from shared memory per tile.
+// The fragments arrive per column (16 KB, double-buffered bulk copies from the
+// prep kernel's output); the two warps of a slice add their halves through
+// shared memory and the sums accumulate per tile in shared memory until the
+// last column.
 #include <cstring>
 
 #include <cuda.h>
@@ -50,18 +55,21 @@ constexpr uint32_t kBoxBytes = 128 * kRows;
 constexpr uint32_t kItemBytes = 2 * kBoxBytes + 16 * kRows;
 constexpr uint32_t kMaxSlots = 8;
 constexpr uint32_t kWordFrag = 32 * 8;   // B fragments of one 16-weight word: 32 lanes x 2 registers
+constexpr uint32_t kColFrag = 8 * 8 * kWordFrag;   // B fragments of one item column (8 groups)
+constexpr uint32_t kTileAcc = 8 * 32 * 16;         // per tile: a float4 per lane of each of the 8 slices
+constexpr uint32_t kMaxTiles = 16;                 // tiles per CTA (their sums live in shared memory)
 
 struct MmaParams {
     CUtensorMap wmap_main, wmap_last;   // base rows: {row bytes, R rows, CTA} / last CTA {row bytes, rows}
     CUtensorMap smap_main, smap_last;   // scale rows, same views
     const uint8_t *frag;                // mma_prep_kernel output: fragments, then {2^-E, X} per (group, row)
-    uint32_t frag_bytes;
+    uint32_t fx_bytes;
     void *y;
     uint64_t n;
     uint32_t M, groups, nitem, rows_per_cta;
     int y_dtype;
     uint32_t nslots, pre_issue;
-    uint32_t off_ring, off_frag, off_part, off_bar, off_cnt;
+    uint32_t off_ring, off_frag, off_fx, off_acc, off_part, off_bar, off_cnt;
     uint32_t *err;
 };
 
@@ -125,10 +133,11 @@ __global__ void __launch_bounds__(64) mma_prep_kernel(const XSource xsrc, uint64
     }
 }
 
-// Item i = tile * nitem + j (groups 8j .. 8j + 7 of the tile's rows): its two
-// code boxes and its scale box into ring slot i % nslots (one thread).
-__device__ __forceinline__ void issue_item(const MmaParams &p, uint8_t *smem, uint32_t item, bool last_cta) {
-    const uint32_t tile = item / p.nitem, j = item % p.nitem, slot = item % p.nslots;
+// Item i = j * ntile + t (groups 8j .. 8j + 7 of tile t): its two code boxes
+// and its scale box into ring slot i % nslots (one thread).
+__device__ __forceinline__ void issue_item(const MmaParams &p, uint8_t *smem, uint32_t item, uint32_t ntile,
+                                           bool last_cta) {
+    const uint32_t j = item / ntile, tile = item % ntile, slot = item % p.nslots;
     const uint32_t dst = smem_u32(smem + p.off_ring) + slot * kItemBytes;
     const uint32_t bar = smem_u32(smem + p.off_bar) + 8 * slot;
     mbar_arrive_expect_tx(bar, kItemBytes);
@@ -144,6 +153,14 @@ __device__ __forceinline__ void issue_item(const MmaParams &p, uint8_t *smem, ui
     }
 }
 
+// B fragments of item column j (up to 8 groups, 16 KB) into fragment buffer j % 2.
+__device__ __forceinline__ void issue_column(const MmaParams &p, uint8_t *smem, uint32_t j, uint32_t bar) {
+    const uint32_t ng = p.groups - 8 * j < 8 ? p.groups - 8 * j : 8;
+    const uint32_t bytes = ng * 8 * kWordFrag;
+    mbar_arrive_expect_tx(bar, bytes);
+    bulk_g2s(smem_u32(smem + p.off_frag) + (j & 1) * kColFrag, p.frag + (uint64_t)j * kColFrag, bytes, bar);
+}
+
 __global__ void __launch_bounds__(kThreads, 1) gemv_pq2_mma_kernel(const __grid_constant__ MmaParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -153,9 +170,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_pq2_mma_kernel(const __grid_
     const uint32_t ntile = (uint32_t)((r_end - r_begin + kRows - 1) / kRows);
     const uint32_t nitems = ntile * p.nitem;
     const uint32_t bar0 = smem_u32(smem + p.off_bar);
-    const uint32_t frag_bar = bar0 + 8 * kMaxSlots;
+    const uint32_t col_bar = bar0 + 8 * kMaxSlots;      // two: one per fragment buffer
+    const uint32_t fx_bar = col_bar + 16;
     uint32_t *cnt = reinterpret_cast<uint32_t *>(smem + p.off_cnt);
-    uint32_t *issued = cnt + kMaxSlots, *failed = cnt + kMaxSlots + 1;
+    uint32_t *issued = cnt + kMaxSlots, *failed = cnt + kMaxSlots + 1, *ccnt = cnt + kMaxSlots + 2;
+    uint32_t *col_last = cnt + kMaxSlots + 4;           // last column issued into each fragment buffer
 
     if (tid == 0) {
         prefetch_tmap(last_cta ? &p.wmap_last : &p.wmap_main);
@@ -164,7 +183,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_pq2_mma_kernel(const __grid_
             mbar_init(bar0 + 8 * s, 1);
             cnt[s] = 0;
         }
-        mbar_init(frag_bar, 1);
+        mbar_init(col_bar, 1);
+        mbar_init(col_bar + 8, 1);
+        mbar_init(fx_bar, 1);
+        ccnt[0] = ccnt[1] = 0;
+        col_last[0] = 0;
+        col_last[1] = p.nitem > 1 ? 1u : 0xffffffffu;
         *failed = 0;
         fence_mbar_init();
     }
@@ -173,94 +197,139 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_pq2_mma_kernel(const __grid_
     const uint32_t pre = p.pre_issue < ring_to ? p.pre_issue : ring_to;
     if (tid == 0) {
         // weights are read-only parameters: a few items before the dependency wait
-        for (uint32_t i = 0; i < pre; ++i) issue_item(p, smem, i, last_cta);
+        for (uint32_t i = 0; i < pre; ++i) issue_item(p, smem, i, ntile, last_cta);
     }
     pdl_launch_dependents();
     pdl_wait();          // the fragments come from the prep kernel
     if (tid == 0) {
-        mbar_arrive_expect_tx(frag_bar, p.frag_bytes);
-        bulk_g2s(smem_u32(smem + p.off_frag), p.frag, p.frag_bytes, frag_bar);
-        for (uint32_t i = pre; i < ring_to; ++i) issue_item(p, smem, i, last_cta);
+        mbar_arrive_expect_tx(fx_bar, p.fx_bytes);
+        bulk_g2s(smem_u32(smem + p.off_fx), p.frag + (uint64_t)p.groups * 8 * kWordFrag, p.fx_bytes, fx_bar);
+        issue_column(p, smem, 0, col_bar);
+        if (p.nitem > 1) issue_column(p, smem, 1, col_bar + 8);
+        for (uint32_t i = pre; i < ring_to; ++i) issue_item(p, smem, i, ntile, last_cta);
         *issued = ring_to;
     }
-    bool ok = mbar_wait(frag_bar, 0, p.err);
+    bool ok = mbar_wait(fx_bar, 0, p.err);
 
-    const uint2 *fragw = reinterpret_cast<const uint2 *>(smem + p.off_frag);
-    const float2 *fx = reinterpret_cast<const float2 *>(smem + p.off_frag + (uint64_t)p.groups * 8 * kWordFrag);
+    const float2 *fx = reinterpret_cast<const float2 *>(smem + p.off_fx);
     float4 *part = reinterpret_cast<float4 *>(smem + p.off_part);
+    float4 *acc_s = reinterpret_cast<float4 *>(smem + p.off_acc);
     const uint32_t slice = warp >> 1, gh = warp & 1, g4 = lane >> 2, c = lane & 3;
     const uint32_t mask = 0x00030003u << (2 * c);
     const uint32_t r0 = slice * 16 + g4, r1 = r0 + 8;     // tile rows of this lane (MMA rows g4, g4 + 8)
     const bool refill = nitems > p.nslots;
-    uint32_t slot = 0, phase = 0, item = 0;
-    for (uint32_t tile = 0; tile < ntile; ++tile) {
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};       // rows r0, r1 x activation rows 2c, 2c + 1
-        for (uint32_t j = 0; j < p.nitem; ++j, ++item) {
-            ok = ok && mbar_wait(bar0 + 8 * slot, phase, p.err);
-            if (ok) {
-                const uint8_t *sa = smem + p.off_ring + slot * kItemBytes;
-#pragma unroll 1
-                for (uint32_t q4 = 0; q4 < 4; ++q4) {
-                    const uint32_t gl = gh * 4 + q4, G = j * 8 + gl;
-                    if (G >= p.groups) break;
-                    // group gl = 16-byte chunks 2 (gl % 4), +1 of box gl / 4, swizzled by row % 8
-                    const uint8_t *bx = sa + (gl >> 2) * kBoxBytes;
-                    const uint32_t cp = 2 * (gl & 3);
+    uint2 bfr[4][8];
+    uint32_t slot = 0, phase = 0, tile = 0, j = 0;
+    for (uint32_t it = 0; it < nitems; ++it) {
+        if (tile == 0) {
+            // this warp's B fragments of column j; the last of the sixteen warps to
+            // take them refills the buffer with column j + 2
+            ok = ok && mbar_wait(col_bar + 8 * (j & 1), (j >> 1) & 1, p.err);
+            const uint2 *fw = reinterpret_cast<const uint2 *>(smem + p.off_frag + (j & 1) * kColFrag) + lane;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+#pragma unroll
+                for (int w = 0; w < 8; ++w) bfr[q][w] = fw[((4 * gh + q) * 8 + w) * 32];
+            __syncwarp();
+            if (lane == 0) {
+                if (!ok) *failed = 1;
+                __threadfence_block();
+                const uint32_t seen = atomicAdd(&ccnt[j & 1], 1u);
+                if (seen == kWarps - 1) {
+                    ccnt[j & 1] = 0;
+                    if (ok && !*(volatile uint32_t *)failed && j + 2 < p.nitem) {
+                        fence_proxy_async();
+                        issue_column(p, smem, j + 2, col_bar + 8 * (j & 1));
+                        col_last[j & 1] = j + 2;
+                    }
+                }
+            }
+            __syncwarp();
+        }
+        ok = ok && mbar_wait(bar0 + 8 * slot, phase, p.err);
+        float a4[4] = {0.f, 0.f, 0.f, 0.f};       // rows r0, r1 x activation rows 2c, 2c + 1
+        if (ok) {
+            const uint8_t *sa = smem + p.off_ring + slot * kItemBytes;
+            const uint8_t *bx = sa + gh * kBoxBytes;     // groups 4 gh .. 4 gh + 3 = box gh
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint32_t gl = 4 * gh + q, G = j * 8 + gl;
+                if (G < p.groups) {
+                    // group gl = 16-byte chunks 2q, 2q + 1 of its box, swizzled by row % 8
                     float C[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                     for (int hf = 0; hf < 2; ++hf) {
-                        const uint4 w0 = *reinterpret_cast<const uint4 *>(bx + r0 * 128 + (((cp + hf) ^ (r0 & 7)) << 4));
-                        const uint4 w1 = *reinterpret_cast<const uint4 *>(bx + r1 * 128 + (((cp + hf) ^ (r1 & 7)) << 4));
+                        const uint4 w0 = *reinterpret_cast<const uint4 *>(bx + r0 * 128 + (((2 * q + hf) ^ (r0 & 7)) << 4));
+                        const uint4 w1 = *reinterpret_cast<const uint4 *>(bx + r1 * 128 + (((2 * q + hf) ^ (r1 & 7)) << 4));
                         const uint32_t cw0[4] = {w0.x, w0.y, w0.z, w0.w}, cw1[4] = {w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const uint2 bf = fragw[(G * 8 + 4 * hf + q) * 32 + lane];
-                            mma16816(C, cw0[q] & mask, cw1[q] & mask, (cw0[q] >> 8) & mask, (cw1[q] >> 8) & mask, bf.x,
-                                     bf.y);
+                        for (int qq = 0; qq < 4; ++qq) {
+                            const uint2 bf = bfr[q][4 * hf + qq];
+                            mma16816(C, cw0[qq] & mask, cw1[qq] & mask, (cw0[qq] >> 8) & mask, (cw1[qq] >> 8) & mask,
+                                     bf.x, bf.y);
                         }
                     }
                     // scale box: row r at r * 16 bytes holds the item's 8 scales
                     const float s0 = __half2float(*reinterpret_cast<const __half *>(sa + 2 * kBoxBytes + r0 * 16 + 2 * gl));
                     const float s1 = __half2float(*reinterpret_cast<const __half *>(sa + 2 * kBoxBytes + r1 * 16 + 2 * gl));
                     const float2 f0 = fx[G * 8 + 2 * c], f1 = fx[G * 8 + 2 * c + 1];
-                    acc[0] = fmaf(s0 * f0.x, fmaf(C[0], 16777216.f, -f0.y), acc[0]);
-                    acc[1] = fmaf(s0 * f1.x, fmaf(C[1], 16777216.f, -f1.y), acc[1]);
-                    acc[2] = fmaf(s1 * f0.x, fmaf(C[2], 16777216.f, -f0.y), acc[2]);
-                    acc[3] = fmaf(s1 * f1.x, fmaf(C[3], 16777216.f, -f1.y), acc[3]);
+                    a4[0] = fmaf(s0 * f0.x, fmaf(C[0], 16777216.f, -f0.y), a4[0]);
+                    a4[1] = fmaf(s0 * f1.x, fmaf(C[1], 16777216.f, -f1.y), a4[1]);
+                    a4[2] = fmaf(s1 * f0.x, fmaf(C[2], 16777216.f, -f0.y), a4[2]);
+                    a4[3] = fmaf(s1 * f1.x, fmaf(C[3], 16777216.f, -f1.y), a4[3]);
                 }
-            }
-            if (refill) {
-                // release the slot; the last of the sixteen readers re-arms it with item + nslots
-                __syncwarp();
-                if (lane == 0) {
-                    if (!ok) *failed = 1;
-                    __threadfence_block();
-                    const uint32_t seen = atomicAdd(&cnt[slot], 1u);
-                    if (seen == kWarps - 1) {
-                        cnt[slot] = 0;
-                        if (ok && !*(volatile uint32_t *)failed && item + p.nslots < nitems) {
-                            fence_proxy_async();
-                            issue_item(p, smem, item + p.nslots, last_cta);
-                            atomicAdd(issued, 1u);
-                        }
-                    }
-                }
-                __syncwarp();
-            } else if (!ok && lane == 0) {
-                *failed = 1;
-            }
-            if (++slot == p.nslots) {
-                slot = 0;
-                phase ^= 1u;
             }
         }
-        // the two warps of a slice hold complementary group halves: add them and store
-        part[warp * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-        __syncthreads();
-        if (gh == 0) {
-            const float4 o = part[(warp + 1) * 32 + lane];
-            const float sum[4] = {acc[0] + o.x, acc[1] + o.y, acc[2] + o.z, acc[3] + o.w};
-            const uint64_t row[2] = {r_begin + (uint64_t)tile * kRows + r0, r_begin + (uint64_t)tile * kRows + r1};
+        if (refill) {
+            // release the slot; the last of the sixteen readers re-arms it with item + nslots
+            __syncwarp();
+            if (lane == 0) {
+                if (!ok) *failed = 1;
+                __threadfence_block();
+                const uint32_t seen = atomicAdd(&cnt[slot], 1u);
+                if (seen == kWarps - 1) {
+                    cnt[slot] = 0;
+                    if (ok && !*(volatile uint32_t *)failed && it + p.nslots < nitems) {
+                        fence_proxy_async();
+                        issue_item(p, smem, it + p.nslots, ntile, last_cta);
+                        atomicAdd(issued, 1u);
+                    }
+                }
+            }
+            __syncwarp();
+        } else if (!ok && lane == 0) {
+            *failed = 1;
+        }
+        if (++slot == p.nslots) {
+            slot = 0;
+            phase ^= 1u;
+        }
+        // the two warps of a slice hold complementary group halves: the even warp
+        // adds them into the tile's sums
+        float4 *pb = part + ((it & 1) * 8 + slice) * 32 + lane;
+        if (gh) *pb = make_float4(a4[0], a4[1], a4[2], a4[3]);
+        named_barrier(1 + slice, 64);
+        if (!gh) {
+            const float4 o = *pb;
+            float4 *as = acc_s + (tile * 8 + slice) * 32 + lane;
+            float4 v = make_float4(a4[0] + o.x, a4[1] + o.y, a4[2] + o.z, a4[3] + o.w);
+            if (j) {
+                const float4 prev = *as;
+                v = make_float4(prev.x + v.x, prev.y + v.y, prev.z + v.z, prev.w + v.w);
+            }
+            *as = v;
+        }
+        if (++tile == ntile) {
+            tile = 0;
+            ++j;
+        }
+    }
+    if (!gh) {
+        // this warp's rows of every tile, activation rows 2c and 2c + 1
+        for (uint32_t t = 0; t < ntile; ++t) {
+            const float4 v = acc_s[(t * 8 + slice) * 32 + lane];
+            const float sum[4] = {v.x, v.y, v.z, v.w};
+            const uint64_t row[2] = {r_begin + (uint64_t)t * kRows + r0, r_begin + (uint64_t)t * kRows + r1};
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const uint64_t r = row[i >> 1];
@@ -268,15 +337,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_pq2_mma_kernel(const __grid_
                 if (r < r_end && m < p.M) store1(p.y, (uint64_t)m * p.n + r, p.y_dtype, sum[i]);
             }
         }
-        __syncthreads();
     }
     // after a timed-out wait: let the copies still in flight land (at most one
     // per slot, the last one issued into it) before the CTA's memory is freed
+    __syncthreads();
     if (tid == 0 && *(volatile uint32_t *)failed) {
         const uint32_t n_issued = *(volatile uint32_t *)issued;
         for (uint32_t i = n_issued > p.nslots ? n_issued - p.nslots : 0; i < n_issued; ++i)
             mbar_wait(bar0 + 8 * (i % p.nslots), (i / p.nslots) & 1, p.err, 200000000ll);
-        mbar_wait(frag_bar, 0, p.err, 200000000ll);
+        mbar_wait(fx_bar, 0, p.err, 200000000ll);
+        for (uint32_t b = 0; b < 2; ++b) {
+            const uint32_t jl = *(volatile uint32_t *)&col_last[b];
+            if (jl != 0xffffffffu) mbar_wait(col_bar + 8 * b, (jl >> 1) & 1, p.err, 200000000ll);
+        }
     }
 }
 
@@ -291,31 +364,44 @@ bool gemv_pq2_mma_plan(const ninfer_row_split_geometry &g, uint64_t M, bool rota
     if (g.scale_row_bytes % 16 || g.base_row_bytes % 16 || g.payload_bytes % 16) return false;
     if (g.k > (1u << 24) || g.n > (1ull << 31)) return false;
     const uint32_t groups = (uint32_t)g.groups_per_row;
-    const uint32_t frag_bytes = groups * 8 * kWordFrag + groups * 8 * 8;
-    const uint32_t part_bytes = kWarps * 32 * 16;
-    const uint32_t bar_bytes = (kMaxSlots + 1) * 8;
-    const uint32_t cnt_bytes = (kMaxSlots + 4) * 4;
-    const uint32_t fixed = frag_bytes + part_bytes + bar_bytes + cnt_bytes;
+    // one CTA per SM with ~n / SMs rows each, at most kMaxTiles tiles of sums per CTA
+    const uint64_t grid0 = std::max<uint64_t>(1, std::min<uint64_t>((uint64_t)sms, g.n / 64));
+    uint64_t R = (g.n + grid0 - 1) / grid0;
+    R = std::min<uint64_t>(R, (uint64_t)kMaxTiles * kRows);
+    const uint64_t grid = (g.n + R - 1) / R;
+    const uint32_t ntile = (uint32_t)((R + kRows - 1) / kRows);
+    const uint32_t fx_bytes = groups * 8 * 8;
+    const uint32_t acc_bytes = ntile * kTileAcc;
+    const uint32_t part_bytes = 2 * 8 * 32 * 16;
+    const uint32_t bar_bytes = (kMaxSlots + 3) * 8;
+    const uint32_t cnt_bytes = (kMaxSlots + 8) * 4;
+    const uint32_t fixed = 2 * kColFrag + fx_bytes + acc_bytes + part_bytes + bar_bytes + cnt_bytes;
     if ((int64_t)fixed + 2 * (int64_t)kItemBytes > smem_limit) return false;
     const uint32_t nslots = std::min<uint32_t>(kMaxSlots, (uint32_t)((smem_limit - (int)fixed) / (int)kItemBytes));
-    // one CTA per SM with ~n / SMs rows each
-    const uint64_t grid0 = std::max<uint64_t>(1, std::min<uint64_t>((uint64_t)sms, g.n / 64));
-    const uint64_t R = (g.n + grid0 - 1) / grid0;
-    const uint64_t grid = (g.n + R - 1) / R;
     plan->ok = true;
     plan->grid = (uint32_t)grid;
     plan->rows_per_cta = (uint32_t)R;
     plan->nitem = (groups + 7) / 8;
     plan->nslots = nslots;
     plan->pre_issue = std::min<uint32_t>(1, nslots);
-    plan->frag_bytes = frag_bytes;
-    plan->off_ring = 0;
-    plan->off_frag = nslots * kItemBytes;
-    plan->off_part = plan->off_frag + frag_bytes;
-    plan->off_bar = plan->off_part + part_bytes;
-    plan->off_cnt = plan->off_bar + bar_bytes;
-    plan->smem = plan->off_cnt + cnt_bytes;
-    plan->workspace = frag_bytes;
+    plan->fx_bytes = fx_bytes;
+    uint32_t off = 0;
+    plan->off_ring = off;
+    off += nslots * kItemBytes;
+    plan->off_frag = off;
+    off += 2 * kColFrag;
+    plan->off_fx = off;
+    off += fx_bytes;
+    plan->off_acc = off;
+    off += acc_bytes;
+    plan->off_part = off;
+    off += part_bytes;
+    plan->off_bar = off;
+    off += bar_bytes;
+    plan->off_cnt = off;
+    off += cnt_bytes;
+    plan->smem = off;
+    plan->workspace = (uint64_t)groups * 8 * kWordFrag + fx_bytes;
     return true;
 }
 
@@ -341,7 +427,7 @@ int gemv_pq2_mma_launch(const MmaPlan &plan, const uint8_t *payload, const ninfe
     std::memset(&p, 0, sizeof p);
     const uint8_t *base = payload + g.base_offset, *scale = payload + g.scale_offset;
     p.frag = static_cast<const uint8_t *>(workspace);
-    p.frag_bytes = plan.frag_bytes;
+    p.fx_bytes = plan.fx_bytes;
     p.y = y;
     p.n = g.n;
     p.M = (uint32_t)M;
@@ -353,6 +439,8 @@ int gemv_pq2_mma_launch(const MmaPlan &plan, const uint8_t *payload, const ninfe
     p.pre_issue = plan.pre_issue;
     p.off_ring = plan.off_ring;
     p.off_frag = plan.off_frag;
+    p.off_fx = plan.off_fx;
+    p.off_acc = plan.off_acc;
     p.off_part = plan.off_part;
     p.off_bar = plan.off_bar;
     p.off_cnt = plan.off_cnt;
