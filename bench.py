@@ -23,6 +23,7 @@ import re
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -119,10 +120,10 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, out_dir: str | None = None):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        self.path = os.path.join(out_dir or tempfile.gettempdir(), f"bench_clocks_rank{gpu_index}.csv")
 
     def start(self):
         os.makedirs(os.path.dirname(self.path), exist_ok=True)
@@ -254,7 +255,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         return ms
 
     warm_replays = max(1, -(-args.warmup // per_graph))
-    clocks = ClockSampler(local_rank)
+    clocks = ClockSampler(local_rank, args.clocks_dir)
     clocks.start()
     ms_total = timed(g_main, g_rem, warm_replays)
     clock_info = clocks.stop()
@@ -404,6 +405,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="gateup", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clocks-dir", default=None, help="where to keep the raw nvidia-smi samples (default: temp dir)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -15,7 +15,7 @@
 //    code * 4^c * 2^-24 (exact); the word shifted right by 8 gives codes c + 4 and
 //    c + 12 the same way. Lane c of a quad therefore feeds K slots (c, c + 8,
 //    c + 4, c + 12) of every 16-weight word.
-//  * B (activations): ptq-free binary16 of xr * 2^E / 4^c (E per 1024-block and
+//  * B (activations): binary16 of xr * 2^E / 4^c (E per 1024-block and
 //    row, so that max |xr * 2^E| < 2^11), written once per call by
 //    mma_prep_kernel in the fragment order of the MMA, plus per group and row
 //    {2^-E, X} with X the sum of the group's B values times 4^c.
