@@ -99,7 +99,7 @@ def dominant_kernel(w):
         return "gemv_ptq1", ["bit_gemv_gb300/csrc/gemv_ptq1_int.cu", "bit_gemv_gb300/csrc/act16.cuh"] + _COMMON
     if w.M <= 8:
         return "gemv_ptq1_mma", ["bit_gemv_gb300/csrc/gemv_ptq1_mma.cu", "bit_gemv_gb300/csrc/act16.cuh"] + _COMMON
-    return "gemm_simple", ["bit_gemv_gb300/csrc/gemm_simple.cu", "bit_gemv_gb300/csrc/plane.cuh"] + _COMMON
+    return "gemm_tc", ["bit_gemv_gb300/csrc/gemm_tc.cu", "bit_gemv_gb300/csrc/transcode.cu"] + _COMMON
 
 
 def measured_tensor_peak():
@@ -307,9 +307,7 @@ def path_dtype(w) -> str:
     """Arithmetic type of the path that serves workload w."""
     if w.M == 1:
         return "int16*ternary->int32->f32"
-    if w.M <= 8 or w.fmt == "PQ2_0_G128":
-        return "f16*f16->f32"
-    return "f32"
+    return "f16*f16->f32"
 
 
 def tensor_roofline(M, n, k, s_step, traffic):
@@ -330,6 +328,8 @@ def kernels_per_step(w) -> int:
         return 2 if (w.fmt == "PTQ1_0_G128" and w.k > 8192) else 1
     if w.fmt == "PTQ1_0_G128" and w.M <= 8:
         return 2 if w.k > 1024 else 1
+    if w.fmt == "PTQ1_0_G128":
+        return 3     # planes rewritten as PQ2_0, rotation to binary16, tensor-core GEMM
     return 2
 
 

@@ -90,6 +90,10 @@ int gemv_ptq1_mma_launch(const Ptq1MmaPlan &plan, const uint8_t *payload, const 
                          const void *x, int x_dtype, const uint16_t *signs, void *y, int y_dtype, uint64_t M,
                          void *workspace, cudaStream_t stream, bool pdl);
 
+// PTQ1_0 planes rewritten exactly as PQ2_0 planes (transcode.cu), for the prefill path.
+int ptq1_to_pq2_launch(const uint8_t *payload, const ninfer_row_split_geometry &g, uint8_t *out,
+                       const ninfer_row_split_geometry &q, cudaStream_t stream, bool pdl);
+
 // Prefill (M > 8) tensor-core path for PQ2_0_G128 (gemm_tc.cu).
 struct TcPlan {
     bool ok;

@@ -38,7 +38,7 @@ static bool g_pdl = true;
 using namespace ninfer;
 
 namespace {
-enum class Path { kIntPq2, kIntPtq1, kMmaPq2, kMmaPtq1, kTcPq2, kTiled };
+enum class Path { kIntPq2, kIntPtq1, kMmaPq2, kMmaPtq1, kTcPq2, kTcPtq1, kTiled };
 
 struct MatmulPlan {
     Path path;
@@ -47,6 +47,8 @@ struct MatmulPlan {
     MmaPlan gmma;
     Ptq1MmaPlan gpm;
     TcPlan gtc;
+    ninfer_row_split_geometry q;     // PQ2_0 geometry of the transcoded planes (kTcPtq1)
+    uint64_t q_bytes;                // their bytes in the workspace, 256-aligned
     uint64_t workspace;
 };
 
@@ -78,6 +80,15 @@ int plan_matmul(int fmt, const ninfer_row_split_geometry &g, uint64_t M, bool ro
     if (fmt == NINFER_PQ2_0_G128 && gemm_tc_plan(g, M, d.smem_optin, &mp->gtc)) {
         mp->path = Path::kTcPq2;
         mp->workspace = mp->gtc.workspace;     // xr as binary16
+        return NINFER_OK;
+    }
+    if (fmt == NINFER_PTQ1_0_G128 && M > 8 && geometry(NINFER_PQ2_0_G128, g.n, g.k, &mp->q) == NINFER_OK &&
+        gemm_tc_plan(mp->q, M, d.smem_optin, &mp->gtc)) {
+        // prefill: the planes are rewritten as PQ2_0 planes in the workspace, then the
+        // same tensor-core GEMM runs on them
+        mp->path = Path::kTcPtq1;
+        mp->q_bytes = (mp->q.payload_bytes + 255) / 256 * 256;
+        mp->workspace = mp->q_bytes + mp->gtc.workspace;
         return NINFER_OK;
     }
     mp->path = Path::kTiled;
@@ -147,6 +158,12 @@ extern "C" int ninfer_ternary_matmul(int fmt, const uint8_t *payload, uint64_t p
         return gemv_ptq1_mma_launch(mp.gpm, payload, g, x, x_dtype, signs_bf16, y, y_dtype, M, workspace, s, g_pdl);
     if (mp.path == Path::kTcPq2)
         return gemm_tc_launch(mp.gtc, payload, g, x, x_dtype, signs_bf16, y, y_dtype, M, workspace, s);
+    if (mp.path == Path::kTcPtq1) {
+        uint8_t *qp = static_cast<uint8_t *>(workspace);
+        st = ptq1_to_pq2_launch(payload, g, qp, mp.q, s, g_pdl);
+        if (st) return st;
+        return gemm_tc_launch(mp.gtc, qp, mp.q, x, x_dtype, signs_bf16, y, y_dtype, M, qp + mp.q_bytes, s);
+    }
     const PlaneView p = make_view(payload, g, fmt);
     const void *a = x;
     int a_dtype = x_dtype;

@@ -121,6 +121,8 @@ WORKLOADS = {
                         description="FFN down decode GEMV, PTQ1_0_G128 n=5120 k=17408, M=8"),
     "prefill": Workload("prefill", "PQ2_0_G128", 17408, 5120, 2048, "bf16", 3,
                         description="prefill GEMM, PQ2_0_G128 n=17408 k=5120, M=2048 token rows"),
+    "prefill_down": Workload("prefill_down", "PTQ1_0_G128", 5120, 17408, 2048, "bf16", 5,
+                             description="prefill GEMM, PTQ1_0_G128 n=5120 k=17408 (FFN down), M=2048 token rows"),
     "head": Workload("head", "PQ2_0_G128", 248320, 5120, 1, "bf16", 4,
                      description="output head, PQ2_0_G128 n=248320 k=5120, M=1"),
     "head_m8": Workload("head_m8", "PQ2_0_G128", 248320, 5120, 8, "bf16", 4,

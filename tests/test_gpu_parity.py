@@ -176,14 +176,34 @@ def test_embed_head_rows(head_case):
     assert oracle.max_rel_error(out.cpu().numpy(), ref) <= TOL_DECODE
 
 
+@pytest.mark.parametrize("fmt", ["PQ2_0_G128", "PTQ1_0_G128"])
 @pytest.mark.parametrize("preset,n,k,M", [("prefill", 300, 1024, 200), ("prefill", 129, 2048, 130),
                                            ("tiny", 256, 1024, 17), ("prefill", 1000, 5120, 300)])
-def test_matmul_prefill_small(preset, n, k, M):
+def test_matmul_prefill_small(fmt, preset, n, k, M):
     """Tensor-core prefill path: partial token and weight-row tiles, fp32 and
-    bf16 activations, every output compared."""
+    bf16 activations, every output compared. PTQ1_0 runs through its planes
+    rewritten as PQ2_0 planes on the device."""
     c = synth.make_case(preset, n=n, k=k, M=M, seed=n + k + M)
-    y = run_matmul("PQ2_0_G128", c)
-    ref = oracle_matmul_rows("PQ2_0_G128", c, np.arange(n))
+    y = run_matmul(fmt, c)
+    ref = oracle_matmul_rows(fmt, c, np.arange(n))
+    assert oracle.max_rel_error(y, ref) <= TOL_PREFILL
+
+
+def test_matmul_prefill_ptq1_invalid_trits():
+    """Base bytes >= 243 and high bytes >= 81 are not produced by the packer;
+    every decoder follows the digit definition (byte / 3^i) % 3 for them too, so
+    the rewritten PQ2_0 planes must give the oracle's result on such payloads."""
+    c = synth.make_case("prefill", n=40, k=1024, M=24, seed=77)
+    payload = nt.ninfer_ternary_pack("PTQ1_0_G128", c.values, c.scales)
+    g = nt.ninfer_ternary_geometry("PTQ1_0_G128", 40, 1024)
+    rng = np.random.default_rng(3)
+    pay = payload.copy()
+    base = pay[g.base_offset:g.base_offset + g.base_bytes]
+    high = pay[g.high_offset:g.high_offset + g.high_bytes]
+    base[rng.integers(0, base.size, 60)] = rng.integers(243, 256, 60).astype(np.uint8)
+    high[rng.integers(0, high.size, 20)] = rng.integers(81, 256, 20).astype(np.uint8)
+    y = run_matmul("PTQ1_0_G128", c, payload_dev=dev_u8(pay))
+    ref = oracle.ternary_matmul("PTQ1_0_G128", pay, 40, 1024, c.x, signs_values(c))
     assert oracle.max_rel_error(y, ref) <= TOL_PREFILL
 
 
@@ -192,6 +212,16 @@ def test_matmul_prefill_unrotated_bf16_out():
     y = run_matmul("PQ2_0_G128", c, rotate=False, y_dtype=torch.bfloat16)
     ref = oracle_matmul_rows("PQ2_0_G128", c, np.arange(256), rotate=False)
     assert oracle.max_rel_error(y, ref) <= TOL_PREFILL
+
+
+@pytest.mark.slow
+def test_matmul_prefill_down_sampled():
+    c = synth.make_case("prefill_down")
+    y = run_matmul("PTQ1_0_G128", c)
+    rng = np.random.default_rng(8)
+    rows = np.unique(np.concatenate([[0, c.workload.n - 1], rng.integers(0, c.workload.n, 128)]))
+    ref = oracle_matmul_rows("PTQ1_0_G128", c, rows)
+    assert oracle.max_rel_error(y[:, rows], ref) <= TOL_PREFILL
 
 
 @pytest.mark.slow

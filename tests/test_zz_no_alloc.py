@@ -63,7 +63,7 @@ def test_noalloc_matches_workspace_entry_two_calls(fmt, n, k, M):
 
 
 def test_noalloc_rejects_problem_larger_than_scratch():
-    fmt, n, k, M = "PTQ1_0_G128", 64, 17408, 64
+    fmt, n, k, M = "PTQ1_0_G128", 64, 17408, 128
     need = nt.ninfer_ternary_matmul_workspace(fmt, n, k, M, True)
     assert need > nt.NOALLOC_SCRATCH_BYTES
     g = nt.ninfer_ternary_geometry(fmt, n, k)
