@@ -56,6 +56,8 @@ _sig = {
     "ninfer_ternary_unpack": (_int, [_int, _u64, _u64, _vp, _u64, _vp, _vp]),
     "ninfer_blocks_to_planes": (_int, [_int, _u64, _u64, _vp, _u64, _vp, _u64]),
     "ninfer_planes_to_blocks": (_int, [_int, _u64, _u64, _vp, _u64, _vp, _u64]),
+    "ninfer_blocks_to_planes_device": (_int, [_int, _u64, _u64, _vp, _u64, _vp, _u64, _vp]),
+    "ninfer_planes_to_blocks_device": (_int, [_int, _u64, _u64, _vp, _u64, _vp, _u64, _vp]),
     "ninfer_hadamard_fwd": (_int, [_vp, _int, _vp, _int, _vp, _u64, _u64, _vp]),
     "ninfer_hadamard_inv": (_int, [_vp, _int, _vp, _int, _vp, _u64, _u64, _vp]),
     "ninfer_ternary_matmul_workspace": (_int, [_int, _u64, _u64, _u64, _int, C.POINTER(_u64)]),
@@ -133,6 +135,29 @@ def ninfer_planes_to_blocks(fmt, n: int, k: int, payload: np.ndarray) -> np.ndar
     nb = 34 if _fmt(fmt) == PQ2_0_G128 else 28
     out = np.empty(n * g.groups_per_row * nb, dtype=np.uint8)
     _check(_lib.ninfer_planes_to_blocks(_fmt(fmt), n, k, _np_ptr(payload), payload.size, _np_ptr(out), out.size))
+    return out
+
+
+def ninfer_blocks_to_planes_device(fmt, n: int, k: int, blocks, out=None):
+    """Device version of ninfer_blocks_to_planes: blocks is a uint8 CUDA tensor;
+    returns (or fills) the uint8 CUDA payload tensor, on the current stream."""
+    torch = _torch()
+    g = ninfer_ternary_geometry(fmt, n, k)
+    if out is None:
+        out = torch.empty(g.payload_bytes, dtype=torch.uint8, device=blocks.device)
+    _check(_lib.ninfer_blocks_to_planes_device(_fmt(fmt), n, k, _dev(blocks, "blocks"), blocks.numel(),
+                                               _dev(out, "payload"), out.numel(), _stream(blocks)))
+    return out
+
+
+def ninfer_planes_to_blocks_device(fmt, n: int, k: int, payload, out=None):
+    torch = _torch()
+    g = ninfer_ternary_geometry(fmt, n, k)
+    nb = 34 if _fmt(fmt) == PQ2_0_G128 else 28
+    if out is None:
+        out = torch.empty(n * g.groups_per_row * nb, dtype=torch.uint8, device=payload.device)
+    _check(_lib.ninfer_planes_to_blocks_device(_fmt(fmt), n, k, _dev(payload, "payload"), payload.numel(),
+                                               _dev(out, "blocks"), out.numel(), _stream(payload)))
     return out
 
 

@@ -160,6 +160,26 @@ int ninfer_planes_to_blocks(int fmt, uint64_t n, uint64_t k, const uint8_t *payl
                             uint64_t blocks_bytes);
 
 /*
+ * ninfer_blocks_to_planes_device / ninfer_planes_to_blocks_device -- the same
+ * two conversions ([FMT] §3-§4 block slices) on device buffers, for a model
+ * whose block stream is already in device memory.
+ *   blocks: device, n * groups_per_row * 34 (PQ2_0) or 28 (PTQ1_0) bytes,
+ *     2-byte aligned; payload: device, payload_bytes of the geometry, 256-byte
+ *     aligned. Same bytes out as the host functions (to planes: the gaps between
+ *     planes are zero).
+ *   Asynchronous on `stream`; the caller keeps both buffers alive until it completes.
+ * Errors: UNKNOWN_FORMAT, SHAPE, INVALID_ARGUMENT, SIZE_MISMATCH, ALIGNMENT,
+ *   OVERFLOW, CUDA (launch failures), all before any device work is queued
+ *   except CUDA.
+ */
+int ninfer_blocks_to_planes_device(int fmt, uint64_t n, uint64_t k, const uint8_t *blocks,
+                                   uint64_t blocks_bytes, uint8_t *payload,
+                                   uint64_t payload_bytes, ninfer_stream stream);
+int ninfer_planes_to_blocks_device(int fmt, uint64_t n, uint64_t k, const uint8_t *payload,
+                                   uint64_t payload_bytes, uint8_t *blocks,
+                                   uint64_t blocks_bytes, ninfer_stream stream);
+
+/*
  * ninfer_hadamard_fwd -- [V3] §8 hadamard_signs, [TS] §4.2 forward transform:
  *   for every row m and 1024-block b: y_b = H (D_b * x_b) / sqrt(1024), with H
  *   the unnormalised Sylvester Hadamard matrix in natural order

@@ -278,3 +278,19 @@ def test_embed_unrotated():
 def test_no_device_errors_after_suite():
     torch.cuda.synchronize()
     assert nt.ninfer_device_errors(clear=True) == 0
+
+
+# --------------------------------------------------------- block <-> planes ---
+@pytest.mark.parametrize("fmt", ["PQ2_0_G128", "PTQ1_0_G128"])
+@pytest.mark.parametrize("n,k", [(1, 128), (37, 1000), (300, 5120)])
+def test_blocks_planes_device_matches_oracle(fmt, n, k):
+    """Device block-stream <-> plane conversion, bit-exact against the oracle's
+    own conversion of the same generator output (both directions)."""
+    c = synth.make_case("gateup", n=n, k=k, M=1, seed=n + k)
+    payload = oracle.pack_planes(fmt, c.values, c.scales)
+    blocks = oracle.planes_to_blocks(fmt, n, k, payload)
+    got_payload = nt.ninfer_blocks_to_planes_device(fmt, n, k, dev_u8(blocks))
+    got_blocks = nt.ninfer_planes_to_blocks_device(fmt, n, k, dev_u8(payload))
+    torch.cuda.synchronize()
+    assert np.array_equal(got_payload.cpu().numpy(), oracle.blocks_to_planes(fmt, n, k, blocks))
+    assert np.array_equal(got_blocks.cpu().numpy(), blocks)
