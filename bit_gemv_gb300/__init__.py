@@ -66,6 +66,9 @@ _sig = {
     "ninfer_device_errors": (_int, [C.POINTER(C.c_uint32), _int]),
     "ninfer_set_prefetch_before_dependency": (_int, [_int]),
     "ninfer_ternary_matmul_noalloc": (_int, [_int, _vp, _u64, _u64, _u64, _vp, _int, _vp, _vp, _int, _u64, _vp]),
+    "ninfer_ternary_gate_up_workspace": (_int, [_int, _u64, _u64, _u64, _int, _int, C.POINTER(_u64)]),
+    "ninfer_ternary_gate_up": (_int, [_int, _vp, _vp, _u64, _u64, _u64, _vp, _int, _vp, _vp, _vp, _int, _u64, _vp,
+                                      _u64, _vp]),
 }
 NOALLOC_SCRATCH_BYTES = 4 * 1024 * 1024
 for _name, (_res, _args) in _sig.items():
@@ -234,6 +237,36 @@ def ninfer_ternary_matmul(fmt, payload, n: int, k: int, x, signs=None, y=None, y
     _check(_lib.ninfer_ternary_matmul(
         _fmt(fmt), _dev(payload, "payload"), payload.numel(), n, k, _dev(x2, "x"), _dt(x2.dtype),
         _dev(signs, "signs") if signs is not None else None, _dev(y, "y"), _dt(y.dtype), M,
+        ws_ptr, ws_bytes, _stream(x)))
+    return y
+
+
+def ninfer_ternary_gate_up_workspace(fmt, n: int, k: int, M: int, rotate: bool, distinct_signs: bool) -> int:
+    v = _u64()
+    _check(_lib.ninfer_ternary_gate_up_workspace(_fmt(fmt), n, k, M, int(bool(rotate)), int(bool(distinct_signs)),
+                                                 C.byref(v)))
+    return v.value
+
+
+def ninfer_ternary_gate_up(fmt, payload_gate, payload_up, n: int, k: int, x, signs_gate=None, signs_up=None, y=None,
+                           y_dtype=None, workspace=None):
+    """y (M, n) = silu(gate projection) * (up projection) of x (M, k); each
+    projection rotates x with its own signs (both or neither given)."""
+    torch = _torch()
+    x2 = x.reshape(-1, k)
+    M = x2.shape[0]
+    if y is None:
+        y = torch.empty((M, n), dtype=y_dtype or torch.float32, device=x.device)
+    distinct = signs_gate is not None and signs_up is not None and signs_gate.data_ptr() != signs_up.data_ptr()
+    need = ninfer_ternary_gate_up_workspace(fmt, n, k, M, signs_gate is not None, distinct)
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    ws_ptr = _dev(workspace, "workspace") if need else None
+    ws_bytes = workspace.numel() * workspace.element_size() if need else 0
+    _check(_lib.ninfer_ternary_gate_up(
+        _fmt(fmt), _dev(payload_gate, "payload_gate"), _dev(payload_up, "payload_up"), payload_gate.numel(), n, k,
+        _dev(x2, "x"), _dt(x2.dtype), _dev(signs_gate, "signs_gate") if signs_gate is not None else None,
+        _dev(signs_up, "signs_up") if signs_up is not None else None, _dev(y, "y"), _dt(y.dtype), M,
         ws_ptr, ws_bytes, _stream(x)))
     return y
 

@@ -18,6 +18,9 @@ struct DeviceInfo {
 int device_info(DeviceInfo *out);
 // Device address of the library's error word on the current device.
 int device_error_word(uint32_t **out);
+// Whether decode kernels may request weights before the dependency wait
+// (ninfer_set_prefetch_before_dependency).
+bool prefetch_before_dependency();
 
 // Rows of a plane as a 2-D byte tensor {row_bytes, rows}, for 2-D box loads:
 // boxes of box_bytes x box_rows, optionally 128-byte swizzled.
@@ -34,17 +37,22 @@ int encode_row_tiles(CUtensorMap *map, const uint8_t *addr, uint64_t row_bytes, 
 int encode_2d(CUtensorMap *map, CUtensorMapDataType dtype, uint32_t elem_bytes, const void *addr, uint64_t inner,
               uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer, bool swizzle128);
 
-// M = 1 integer kernel (PQ2_0_G128), rotation fused in.
+// M = 1 integer kernel (PQ2_0_G128), rotation fused in. With mats = 2 it
+// streams two matrices of the same geometry (FFN gate and up) for the same rows
+// and stores silu(gate x) * (up x); two_rotations when their signs differ.
 struct IntPlan {
     bool ok;
+    int mats;
+    uint32_t act_one;
     uint32_t grid, rows_per_cta, nitem, nslots, pre_issue;
     uint32_t off_ring, off_act, off_part, off_bar, off_cnt, smem;
     uint64_t workspace;
 };
 bool gemv_pq2_int_plan(const ninfer_row_split_geometry &g, uint64_t M, bool rotate, int sms, int smem_limit,
-                       IntPlan *plan);
+                       IntPlan *plan, int mats = 1, bool two_rotations = false);
 int gemv_pq2_int_launch(const IntPlan &plan, const uint8_t *payload, const ninfer_row_split_geometry &g, const void *x,
-                        int x_dtype, const uint16_t *signs, void *y, int y_dtype, cudaStream_t stream, bool pdl);
+                        int x_dtype, const uint16_t *signs, void *y, int y_dtype, cudaStream_t stream, bool pdl,
+                        const uint8_t *payload2 = nullptr, const uint16_t *signs2 = nullptr);
 
 
 // M = 1 integer kernel (PTQ1_0_G128), rotation fused in.

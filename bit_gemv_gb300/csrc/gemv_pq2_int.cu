@@ -60,8 +60,11 @@ constexpr uint32_t kRotPairs = 8;     // warp pairs that rotate x (one 1024-bloc
 struct IntParams {
     CUtensorMap wmap_main, wmap_last;   // base rows: {row bytes, R rows, CTA} / last CTA {row bytes, rows}
     CUtensorMap smap_main, smap_last;   // scale rows, same views
+    CUtensorMap wmap2_main, wmap2_last, smap2_main, smap2_last;     // second matrix (fused gate/up: up)
     const void *x;
     const uint16_t *signs;              // bf16 +-1 per element, or null (no rotation)
+    const uint16_t *signs2;             // second matrix's signs (may equal signs)
+    uint32_t act_bytes;                 // operand words + group entries of one rotation
     void *y;
     uint64_t n;
     uint32_t k, groups, nblk, nitem, rows_per_cta;     // nitem: items per tile, ceil(groups / 8)
@@ -71,22 +74,28 @@ struct IntParams {
     uint32_t *err;
 };
 
-// Item i = tile * nitem + j (groups 8j .. 8j + 7 of the tile's rows): its two
-// weight boxes and its scale box into ring slot i % nslots (one thread).
+// Item i = tile * (kMats * nitem) + mat * nitem + j (groups 8j .. 8j + 7 of
+// the tile's rows of matrix mat): its two weight boxes and its scale box into
+// ring slot i % nslots (one thread).
+template <int kMats>
 __device__ __forceinline__ void issue_item(const IntParams &p, uint8_t *smem, uint32_t item, bool last_cta) {
-    const uint32_t tile = item / p.nitem, j = item % p.nitem, slot = item % p.nslots;
+    const uint32_t per_tile = kMats * p.nitem;
+    const uint32_t tile = item / per_tile, jj = item % per_tile, mat = kMats == 1 ? 0 : jj / p.nitem;
+    const uint32_t j = jj - mat * p.nitem, slot = item % p.nslots;
     const uint32_t dst = smem_u32(smem + p.off_ring) + slot * kItemBytes;
     const uint32_t bar = smem_u32(smem + p.off_bar) + 8 * slot;
     mbar_arrive_expect_tx(bar, kItemBytes);
     const int y0 = (int)(tile * kRows), xs = (int)(j * 16);
     if (last_cta) {
-        tma_load_2d(dst, &p.wmap_last, (int)(j * 256), y0, bar);
-        tma_load_2d(dst + kBoxBytes, &p.wmap_last, (int)(j * 256 + 128), y0, bar);
-        tma_load_2d(dst + 2 * kBoxBytes, &p.smap_last, xs, y0, bar);
+        const CUtensorMap *wm = mat ? &p.wmap2_last : &p.wmap_last, *sm = mat ? &p.smap2_last : &p.smap_last;
+        tma_load_2d(dst, wm, (int)(j * 256), y0, bar);
+        tma_load_2d(dst + kBoxBytes, wm, (int)(j * 256 + 128), y0, bar);
+        tma_load_2d(dst + 2 * kBoxBytes, sm, xs, y0, bar);
     } else {
-        tma_load_3d(dst, &p.wmap_main, (int)(j * 256), y0, (int)blockIdx.x, bar);
-        tma_load_3d(dst + kBoxBytes, &p.wmap_main, (int)(j * 256 + 128), y0, (int)blockIdx.x, bar);
-        tma_load_3d(dst + 2 * kBoxBytes, &p.smap_main, xs, y0, (int)blockIdx.x, bar);
+        const CUtensorMap *wm = mat ? &p.wmap2_main : &p.wmap_main, *sm = mat ? &p.smap2_main : &p.smap_main;
+        tma_load_3d(dst, wm, (int)(j * 256), y0, (int)blockIdx.x, bar);
+        tma_load_3d(dst + kBoxBytes, wm, (int)(j * 256 + 128), y0, (int)blockIdx.x, bar);
+        tma_load_3d(dst + 2 * kBoxBytes, sm, xs, y0, (int)blockIdx.x, bar);
     }
 }
 
@@ -124,6 +133,9 @@ __device__ __forceinline__ void pack_pq2(const int16_t *qs, uint8_t *act_s, uint
     named_barrier(bar, 64);      // qs is read before the next block reuses the tile
 }
 
+// kMats = 1: y = W x. kMats = 2 (fused FFN gate/up): y = silu(Wg x_g) * (Wu x_u)
+// for the same rows of both matrices, x_g and x_u rotated with each matrix's signs.
+template <int kMats>
 __global__ void __launch_bounds__(kThreads, 1) gemv_pq2_int_kernel(const __grid_constant__ IntParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -131,7 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_pq2_int_kernel(const __grid_
     const uint64_t r_end = r_begin + p.rows_per_cta < p.n ? r_begin + p.rows_per_cta : p.n;
     const bool last_cta = blockIdx.x == gridDim.x - 1;
     const uint32_t ntile = (uint32_t)((r_end - r_begin + kRows - 1) / kRows);
-    const uint32_t nitems = ntile * p.nitem;
+    const uint32_t nitems = ntile * kMats * p.nitem;
     const uint32_t bar0 = smem_u32(smem + p.off_bar);
     uint32_t *cnt = reinterpret_cast<uint32_t *>(smem + p.off_cnt);
     uint32_t *issued = cnt + kMaxSlots, *failed = cnt + kMaxSlots + 1;
@@ -139,6 +151,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_pq2_int_kernel(const __grid_
     if (tid == 0) {
         prefetch_tmap(last_cta ? &p.wmap_last : &p.wmap_main);
         prefetch_tmap(last_cta ? &p.smap_last : &p.smap_main);
+        if (kMats == 2) {
+            prefetch_tmap(last_cta ? &p.wmap2_last : &p.wmap2_main);
+            prefetch_tmap(last_cta ? &p.smap2_last : &p.smap2_main);
+        }
         for (uint32_t s = 0; s < p.nslots; ++s) {
             mbar_init(bar0 + 8 * s, 1);
             cnt[s] = 0;
@@ -151,36 +167,46 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_pq2_int_kernel(const __grid_
     const uint32_t pre = p.pre_issue < ring_to ? p.pre_issue : ring_to;
     if (tid == 0) {
         // weights are read-only parameters: a few items before the dependency wait
-        for (uint32_t i = 0; i < pre; ++i) issue_item(p, smem, i, last_cta);
+        for (uint32_t i = 0; i < pre; ++i) issue_item<kMats>(p, smem, i, last_cta);
     }
-    // rotation: warp pair pr = warp / 2 < nrot takes blocks pr, pr + nrot, ...
-    const uint32_t nrot = p.nblk < kRotPairs ? p.nblk : kRotPairs;
+    // rotation tasks (matrix, block): one rotation per block, or two when the
+    // fused matrices have different signs; warp pair pr takes tasks pr, pr + nrot, ...
+    const uint32_t nrmat = (kMats == 2 && p.signs2 != p.signs) ? 2 : 1;
+    const uint32_t ntask = nrmat * p.nblk;
+    const uint32_t nrot = ntask < kRotPairs ? ntask : kRotPairs;
     const uint32_t pr = warp >> 1;
     const int t = tid & 63;
-    const XSource xsrc{p.x, p.signs, p.k, p.x_dtype};
+    auto task_src = [&](uint32_t task) {
+        return XSource{p.x, task >= p.nblk ? p.signs2 : p.signs, p.k, p.x_dtype};
+    };
     float d[16];
-    if (p.signs && pr < nrot) load_signs16(xsrc, pr, t, d);     // also read-only
+    if (pr < nrot) {
+        const XSource xs0 = task_src(pr);
+        if (xs0.signs) load_signs16(xs0, pr % p.nblk, t, d);     // also read-only
+    }
     pdl_launch_dependents();
     pdl_wait();          // x may come from the preceding kernel
 
     float v[16];
-    if (pr < nrot) load_run16(xsrc, pr, t, v);
+    if (pr < nrot) load_run16(task_src(pr), pr % p.nblk, t, v);
     __syncthreads();     // every warp's x request is out: the rest of the ring queues behind them
     if (tid == 0) {
-        for (uint32_t i = pre; i < ring_to; ++i) issue_item(p, smem, i, last_cta);
+        for (uint32_t i = pre; i < ring_to; ++i) issue_item<kMats>(p, smem, i, last_cta);
         *issued = ring_to;
     }
     uint8_t *act_s = smem + p.off_act;
     if (pr < nrot) {
         float *tile = reinterpret_cast<float *>(smem + p.off_part + pr * kRotScratch);
-        for (uint32_t b = pr; b < p.nblk; b += nrot) {
-            if (b != pr) {
-                if (p.signs) load_signs16(xsrc, b, t, d);
-                load_run16(xsrc, b, t, v);
+        for (uint32_t task = pr; task < ntask; task += nrot) {
+            const XSource xs = task_src(task);
+            const uint32_t b = task % p.nblk;
+            if (task != pr) {
+                if (xs.signs) load_signs16(xs, b, t, d);
+                load_run16(xs, b, t, v);
             }
             int E;
-            const int16_t *qs = rotate_quantize16(p.signs != nullptr, t, v, d, tile, 1 + pr, &E);
-            pack_pq2(qs, act_s, p.groups, b, t, E, 1 + pr);
+            const int16_t *qs = rotate_quantize16(xs.signs != nullptr, t, v, d, tile, 1 + pr, &E);
+            pack_pq2(qs, act_s + (task / p.nblk) * p.act_bytes, p.groups, b, t, E, 1 + pr);
         }
     }
     __syncthreads();
@@ -190,13 +216,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_pq2_int_kernel(const __grid_
     // line; this warp reads chunk 2gi + half (words 4 half .. 4 half + 3), swizzled by row % 8
     const uint32_t gw = warp & 7, half = warp >> 3, h = gw >> 2, gi = gw & 3;
     const uint32_t ch = ((2 * gi + half) ^ (lane & 7)) << 4;
-    const float2 *gs = reinterpret_cast<const float2 *>(act_s + p.groups * 256);
     float *part = reinterpret_cast<float *>(smem + p.off_part);
     const bool refill = nitems > p.nslots;    // otherwise the whole slice sits in the ring
     uint32_t slot = 0, phase = 0, item = 0;
     for (uint32_t tile = 0; tile < ntile; ++tile) {
-        float y[4] = {0.f, 0.f, 0.f, 0.f};      // rows lane + 32q of the tile
-        for (uint32_t j = 0; j < p.nitem; ++j, ++item) {
+        float y[kMats][4];      // rows lane + 32q of the tile, per matrix
+#pragma unroll
+        for (int mt = 0; mt < kMats; ++mt)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) y[mt][q] = 0.f;
+        for (uint32_t jj = 0; jj < kMats * p.nitem; ++jj, ++item) {
+            const uint32_t mat = kMats == 1 ? 0 : (jj >= p.nitem), j = jj - mat * p.nitem;
+            const uint8_t *act_m = act_s + (mat < nrmat ? mat : 0) * p.act_bytes;
+            const float2 *gs = reinterpret_cast<const float2 *>(act_m + p.groups * 256);
             ok = ok && mbar_wait(bar0 + 8 * slot, phase, p.err);
             const uint32_t G = j * 8 + gw;
             if (ok && G < p.groups) {
@@ -208,7 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_pq2_int_kernel(const __grid_
                     const uint4 a = *reinterpret_cast<const uint4 *>(wr + q * 4096);
                     w[q][0] = a.x; w[q][1] = a.y; w[q][2] = a.z; w[q][3] = a.w;
                 }
-                const uint4 *aw = reinterpret_cast<const uint4 *>(act_s + (uint64_t)G * 256 + half * 128);
+                const uint4 *aw = reinterpret_cast<const uint4 *>(act_m + (uint64_t)G * 256 + half * 128);
                 int acc[4][4];
 #pragma unroll
                 for (int q = 0; q < 4; ++q)
@@ -234,7 +266,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_pq2_int_kernel(const __grid_
                 for (int q = 0; q < 4; ++q) {
                     const int t = acc[q][0] + (acc[q][1] >> 2) + (acc[q][2] >> 4) + (acc[q][3] >> 6) - off;
                     const float s = __half2float(*reinterpret_cast<const __half *>(sc + q * 512));
-                    y[q] = fmaf(s * f.x, (float)t, y[q]);
+                    if (kMats == 1 || mat == 0) y[0][q] = fmaf(s * f.x, (float)t, y[0][q]);
+                    else y[kMats - 1][q] = fmaf(s * f.x, (float)t, y[kMats - 1][q]);
                 }
             }
             if (refill) {
@@ -248,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_pq2_int_kernel(const __grid_
                         cnt[slot] = 0;
                         if (ok && !*(volatile uint32_t *)failed && item + p.nslots < nitems) {
                             fence_proxy_async();
-                            issue_item(p, smem, item + p.nslots, last_cta);
+                            issue_item<kMats>(p, smem, item + p.nslots, last_cta);
                             atomicAdd(issued, 1u);
                         }
                     }
@@ -263,15 +296,23 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_pq2_int_kernel(const __grid_
             }
         }
 #pragma unroll
-        for (int q = 0; q < 4; ++q) part[warp * kRows + 32 * q + lane] = y[q];
+        for (int mt = 0; mt < kMats; ++mt)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) part[(mt * kWarps + warp) * kRows + 32 * q + lane] = y[mt][q];
         __syncthreads();
         if (warp < kRows / 32) {
             const uint32_t rl = warp * 32 + lane;
             const uint64_t r = r_begin + (uint64_t)tile * kRows + rl;
-            float acc = 0.f;
+            float acc[kMats];
 #pragma unroll
-            for (int w = 0; w < kWarps; ++w) acc += part[w * kRows + rl];
-            if (r < r_end) store1(p.y, r, p.y_dtype, acc);
+            for (int mt = 0; mt < kMats; ++mt) {
+                acc[mt] = 0.f;
+#pragma unroll
+                for (int w = 0; w < kWarps; ++w) acc[mt] += part[(mt * kWarps + w) * kRows + rl];
+            }
+            // fused gate/up: SwiGLU, silu(g) * u with silu(g) = g / (1 + e^-g)
+            const float out = kMats == 1 ? acc[0] : acc[0] / (1.f + expf(-acc[0])) * acc[kMats - 1];
+            if (r < r_end) store1(p.y, r, p.y_dtype, out);
         }
         __syncthreads();
     }
@@ -287,18 +328,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_pq2_int_kernel(const __grid_
 }  // namespace
 
 bool gemv_pq2_int_plan(const ninfer_row_split_geometry &g, uint64_t M, bool rotate, int sms, int smem_limit,
-                       IntPlan *plan) {
+                       IntPlan *plan, int mats, bool two_rotations) {
     *plan = IntPlan{};
-    if (M != 1) return false;
+    if (M != 1 || mats < 1 || mats > 2) return false;
     if (rotate && g.k % 1024) return false;
     // scale rows must be whole 16-byte units (8 groups) for the scale boxes
     if (g.scale_row_bytes % 16 || g.base_row_bytes % 16 || g.payload_bytes % 16) return false;
     if (g.k > (1u << 24) || g.n > (1ull << 31)) return false;
     const uint32_t groups = (uint32_t)g.groups_per_row;
-    const uint32_t act_bytes = ((groups * 264 + 15) / 16) * 16;
+    const uint32_t act_one = ((groups * 264 + 15) / 16) * 16;
+    const uint32_t nrmat = (mats == 2 && two_rotations) ? 2 : 1;
+    const uint32_t act_bytes = nrmat * act_one;
     // tile partial sums, and before them the rotation's scratch (one padded tile per rotating warp pair)
-    const uint32_t nrot = std::min<uint32_t>((uint32_t)((g.k + 1023) / 1024), kRotPairs);
-    const uint32_t part_bytes = std::max<uint32_t>(kWarps * kRows * 4, nrot * kRotScratch);
+    const uint32_t nrot = std::min<uint32_t>(nrmat * (uint32_t)((g.k + 1023) / 1024), kRotPairs);
+    const uint32_t part_bytes = std::max<uint32_t>(mats * kWarps * kRows * 4, nrot * kRotScratch);
     const uint32_t bar_bytes = kMaxSlots * 8;
     const uint32_t cnt_bytes = (kMaxSlots + 4) * 4;
     const uint32_t fixed = act_bytes + part_bytes + bar_bytes + cnt_bytes;
@@ -309,6 +352,8 @@ bool gemv_pq2_int_plan(const ninfer_row_split_geometry &g, uint64_t M, bool rota
     const uint64_t R = (g.n + grid0 - 1) / grid0;
     const uint64_t grid = (g.n + R - 1) / R;
     plan->ok = true;
+    plan->mats = mats;
+    plan->act_one = act_one;
     plan->grid = (uint32_t)grid;
     plan->rows_per_cta = (uint32_t)R;
     plan->nitem = (groups + 7) / 8;
@@ -325,12 +370,15 @@ bool gemv_pq2_int_plan(const ninfer_row_split_geometry &g, uint64_t M, bool rota
 }
 
 int gemv_pq2_int_launch(const IntPlan &plan, const uint8_t *payload, const ninfer_row_split_geometry &g, const void *x,
-                        int x_dtype, const uint16_t *signs, void *y, int y_dtype, cudaStream_t stream, bool pdl) {
+                        int x_dtype, const uint16_t *signs, void *y, int y_dtype, cudaStream_t stream, bool pdl,
+                        const uint8_t *payload2, const uint16_t *signs2) {
     IntParams p;
     std::memset(&p, 0, sizeof p);
     const uint8_t *base = payload + g.base_offset, *scale = payload + g.scale_offset;
     p.x = x;
     p.signs = signs;
+    p.signs2 = plan.mats == 2 ? signs2 : signs;
+    p.act_bytes = plan.act_one;
     p.y = y;
     p.n = g.n;
     p.k = (uint32_t)g.k;
@@ -361,7 +409,23 @@ int gemv_pq2_int_launch(const IntPlan &plan, const uint8_t *payload, const ninfe
         st = encode_rows(&p.smap_last, scale + (G - 1) * R * g.scale_row_bytes, g.scale_row_bytes, last_rows, 16,
                          kRows, false);
     if (st) return st;
-    cudaError_t e = cudaFuncSetAttribute(gemv_pq2_int_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.smem);
+    if (plan.mats == 2) {
+        // the second matrix: same geometry, its own payload
+        const uint8_t *base2 = payload2 + g.base_offset, *scale2 = payload2 + g.scale_offset;
+        if (G > 1) {
+            st = encode_row_tiles(&p.wmap2_main, base2, g.base_row_bytes, R, G - 1, 128, kRows, true);
+            if (!st) st = encode_row_tiles(&p.smap2_main, scale2, g.scale_row_bytes, R, G - 1, 16, kRows, false);
+            if (st) return st;
+        }
+        st = encode_rows(&p.wmap2_last, base2 + (G - 1) * R * g.base_row_bytes, g.base_row_bytes, last_rows, 128,
+                         kRows, true);
+        if (!st)
+            st = encode_rows(&p.smap2_last, scale2 + (G - 1) * R * g.scale_row_bytes, g.scale_row_bytes, last_rows,
+                             16, kRows, false);
+        if (st) return st;
+    }
+    auto kernel = plan.mats == 2 ? gemv_pq2_int_kernel<2> : gemv_pq2_int_kernel<1>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.smem);
     if (e != cudaSuccess) return fail(NINFER_ERR_CUDA, "gemv: smem attribute: %s", cudaGetErrorString(e));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(plan.grid);
@@ -373,7 +437,7 @@ int gemv_pq2_int_launch(const IntPlan &plan, const uint8_t *payload, const ninfe
     attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, gemv_pq2_int_kernel, p);
+    e = cudaLaunchKernelEx(&cfg, kernel, p);
     if (e != cudaSuccess) return fail(NINFER_ERR_CUDA, "gemv launch: %s", cudaGetErrorString(e));
     return NINFER_OK;
 }

@@ -33,6 +33,7 @@ int device_info(DeviceInfo *out) {
 }
 
 static bool g_pdl = true;
+bool prefetch_before_dependency() { return g_pdl; }
 }  // namespace ninfer
 
 using namespace ninfer;

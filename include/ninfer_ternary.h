@@ -244,6 +244,33 @@ int ninfer_ternary_matmul(int fmt, const uint8_t *payload, uint64_t payload_byte
                           ninfer_stream stream);
 
 /*
+ * ninfer_ternary_gate_up -- the FFN gate and up projections of one activation
+ * with the SwiGLU product ([TS] §4.2: fused gate/up weights keep each original
+ * projection's transform; §4.4: the dense gated FFN, read as SwiGLU):
+ *   y[m][r] = silu(g[m][r]) * u[m][r],  silu(a) = a / (1 + e^-a),
+ *   g = ninfer_ternary_matmul(payload_gate, x, signs_gate),
+ *   u = ninfer_ternary_matmul(payload_up, x, signs_up).
+ *   payload_gate, payload_up: device, the same format and shape n x k
+ *     (payload_bytes each, 256-byte aligned).
+ *   signs_gate_bf16, signs_up_bf16: both device bfloat16[k], or both NULL (no
+ *     rotation); they may be the same pointer (one rotation serves both).
+ *   x, y, x_dtype, y_dtype, M, stream: as ninfer_ternary_matmul.
+ *   workspace: device scratch of at least ninfer_ternary_gate_up_workspace()
+ *     bytes, 256-byte aligned (NULL allowed when that is 0). PQ2_0 with M = 1
+ *     runs both projections and the product in one kernel and needs none;
+ *     other cases keep fp32 g and u in the workspace.
+ * Errors: as ninfer_ternary_matmul; INVALID_ARGUMENT when exactly one sign
+ *   vector is given.
+ */
+int ninfer_ternary_gate_up_workspace(int fmt, uint64_t n, uint64_t k, uint64_t M,
+                                     int rotate, int distinct_signs, uint64_t *bytes);
+int ninfer_ternary_gate_up(int fmt, const uint8_t *payload_gate, const uint8_t *payload_up,
+                           uint64_t payload_bytes, uint64_t n, uint64_t k,
+                           const void *x, int x_dtype, const uint16_t *signs_gate_bf16,
+                           const uint16_t *signs_up_bf16, void *y, int y_dtype, uint64_t M,
+                           void *workspace, uint64_t workspace_bytes, ninfer_stream stream);
+
+/*
  * ninfer_ternary_embed -- embedding rows ([TS] §4.4: token id -> low-bit
  * embedding row -> inverse signed Hadamard transform; [V3] §7.3: a row range of
  * a row-split matrix spans intervals of the base, high and scale planes):

@@ -17,7 +17,8 @@ codec), written step by step from the source pages:
   §8 the ``hadamard_signs`` auxiliary input.
 * "从 TensorSharp 视角解读 Ternary Bonsai 2 27B" (TensorSharp article): §4.2 the
   transform contract H(D.x)/sqrt(block) and its inverse D.(H.x)/sqrt(block),
-  §4.4 where the transforms apply.
+  §4.4 where the transforms apply (and the dense gated FFN, read as SwiGLU;
+  §4.2: fused gate/up weights keep each projection's own transform).
 
 Pins (tests/test_oracle_pins.py) tie each function to something outside the
 oracle: the byte counts the format page prints, a library Hadamard matrix,
@@ -37,6 +38,7 @@ from .ternary import (  # noqa: F401
     hadamard_forward,
     hadamard_inverse,
     ternary_matmul,
+    gate_up_swiglu,
     embed_rows,
     max_rel_error,
 )

@@ -367,6 +367,18 @@ def ternary_matmul(fmt, payload, n: int, k: int, x, signs=None, rows=None) -> np
     return xr @ W.T
 
 
+def gate_up_swiglu(fmt, payload_gate, payload_up, n: int, k: int, x, signs_gate=None, signs_up=None,
+                   rows=None) -> np.ndarray:
+    """FFN gate/up with the SwiGLU product, fp64: y = silu(g) * u with
+    g = ternary_matmul(gate, x, signs_gate), u = ternary_matmul(up, x, signs_up)
+    and silu(a) = a / (1 + e^-a). Fused gate/up weights keep each original
+    projection's transform (TensorSharp article section 4.2); the layers' dense
+    gated FFN (section 4.4) is read as SwiGLU."""
+    g = ternary_matmul(fmt, payload_gate, n, k, x, signs_gate, rows)
+    u = ternary_matmul(fmt, payload_up, n, k, x, signs_up, rows)
+    return g / (1.0 + np.exp(-g)) * u
+
+
 def embed_rows(fmt, payload, n: int, k: int, ids, signs) -> np.ndarray:
     """out_i = inverse transform of dequantised row ids[i] (count x k, fp64)."""
     ids = np.asarray(ids, dtype=np.int64).reshape(-1)

@@ -387,4 +387,33 @@ def pin_padding_bytes():
     assert np.all(t[g.high_offset + 2:g.high_offset + 4] == 40)
 
 
+def pin_gate_up_limits():
+    """SwiGLU of the gate and up projections at points where silu has a closed
+    limit: silu(a) -> a for large a, -> 0 for large -a, silu(0) = 0. With x a
+    unit vector and every weight +1 the projections are the scales themselves
+    (no rotation), or 32 * D[0] * scale (rotation: H's first column is all ones),
+    which also tells whether each projection used its own sign vector."""
+    n, k = 3, 1024
+    ones = np.ones((n, k), np.int8)
+    def payload(scale_f16):
+        return oracle.pack_planes("PQ2_0_G128", ones, np.full((n, k // 128), scale_f16, np.uint16))
+    x = np.zeros((1, k))
+    x[0, 0] = 1.0             # unrotated: only column 0 contributes, g = scale
+    f16 = lambda v: int(np.array([v], np.float16).view(np.uint16)[0])
+    y = oracle.gate_up_swiglu("PQ2_0_G128", payload(f16(20.0)), payload(f16(0.5)), n, k, x)
+    assert np.allclose(y, 10.0, rtol=1e-7)                 # silu(20) * 0.5 = 10 (1 - 2e-9)
+    y = oracle.gate_up_swiglu("PQ2_0_G128", payload(f16(-20.0)), payload(f16(0.5)), n, k, x)
+    assert np.all(np.abs(y) < 1e-6)                        # silu(-20) * 0.5 ~ -2e-8
+    y = oracle.gate_up_swiglu("PQ2_0_G128", payload(0), payload(f16(3.0)), n, k, x)
+    assert np.all(y == 0.0)                                # silu(0) = 0
+    # rotation with different signs: xr = D[0] / 32 everywhere, g = 32 D_g[0] s_g, u = 32 D_u[0] s_u
+    Dg = np.ones(k)
+    Du = np.ones(k)
+    Du[0] = -1.0
+    x1 = np.zeros((1, k))
+    x1[0, 0] = 1.0
+    y = oracle.gate_up_swiglu("PQ2_0_G128", payload(f16(1.0)), payload(f16(1.0 / 32)), n, k, x1, Dg, Du)
+    assert np.allclose(y, -32.0, rtol=1e-7)                # silu(32) * (-1)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -294,3 +294,69 @@ def test_blocks_planes_device_matches_oracle(fmt, n, k):
     torch.cuda.synchronize()
     assert np.array_equal(got_payload.cpu().numpy(), oracle.blocks_to_planes(fmt, n, k, blocks))
     assert np.array_equal(got_blocks.cpu().numpy(), blocks)
+
+
+# ------------------------------------------------------- fused FFN gate/up ---
+def _up_inputs(seed, n, k):
+    """The up projection's values, scales and signs, from their own generator."""
+    rng = np.random.default_rng(seed)
+    groups = -(-k // 128)
+    return synth.ternary_values(rng, n, k), synth.group_scales(rng, n, groups), synth.sign_vector(rng, k)
+
+
+@pytest.mark.parametrize("fmt,n,k,M,same_signs", [
+    ("PQ2_0_G128", 300, 2048, 1, False), ("PQ2_0_G128", 300, 2048, 1, True), ("PQ2_0_G128", 150, 5120, 1, False),
+    ("PQ2_0_G128", 1, 1024, 1, False), ("PTQ1_0_G128", 300, 2048, 1, False), ("PQ2_0_G128", 77, 3072, 4, False),
+    ("PTQ1_0_G128", 129, 2048, 40, True)])
+def test_gate_up_swiglu(fmt, n, k, M, same_signs):
+    """silu(gate x) * (up x), each projection with its own signs (or one shared
+    vector): PQ2_0 at M = 1 runs the fused two-matrix kernel, the other cases
+    the two projections and the SwiGLU kernel."""
+    c = synth.make_case("gateup", n=n, k=k, M=M, seed=n + k + M)
+    vu, su, du = _up_inputs(n + 2 * k + M, n, k)
+    if same_signs:
+        du = c.signs
+    pay_g = dev_u8(nt.ninfer_ternary_pack(fmt, c.values, c.scales))
+    pay_u = dev_u8(nt.ninfer_ternary_pack(fmt, vu, su))
+    sg = dev_signs(c.signs)
+    su_dev = sg if same_signs else dev_signs(du)
+    y = nt.ninfer_ternary_gate_up(fmt, pay_g, pay_u, n, k, dev_x(c), sg, su_dev)
+    torch.cuda.synchronize()
+    ref = oracle.gate_up_swiglu(fmt, oracle.pack_planes(fmt, c.values, c.scales), oracle.pack_planes(fmt, vu, su), n, k,
+                                c.x, signs_values(c), synth.bf16_bits_to_f32(du).astype(np.float64))
+    tol = TOL_DECODE if M <= 8 else TOL_PREFILL
+    assert oracle.max_rel_error(y.cpu().numpy().astype(np.float64), ref) <= tol
+
+
+def test_gate_up_unrotated_and_errors():
+    c = synth.make_case("gateup", n=64, k=1000, M=1, seed=3)
+    vu, su, _ = _up_inputs(4, 64, 1000)
+    pay_g = dev_u8(nt.ninfer_ternary_pack("PQ2_0_G128", c.values, c.scales))
+    pay_u = dev_u8(nt.ninfer_ternary_pack("PQ2_0_G128", vu, su))
+    y = nt.ninfer_ternary_gate_up("PQ2_0_G128", pay_g, pay_u, 64, 1000, dev_x(c))
+    torch.cuda.synchronize()
+    ref = oracle.gate_up_swiglu("PQ2_0_G128", oracle.pack_planes("PQ2_0_G128", c.values, c.scales),
+                                oracle.pack_planes("PQ2_0_G128", vu, su), 64, 1000, c.x)
+    assert oracle.max_rel_error(y.cpu().numpy().astype(np.float64), ref) <= TOL_DECODE
+    with pytest.raises(nt.NinferError):          # one sign vector without the other
+        nt.ninfer_ternary_gate_up("PQ2_0_G128", pay_g, pay_u, 64, 1024, dev_x(synth.make_case("gateup", n=64, k=1024, M=1, seed=3)),
+                                  dev_signs(synth.make_case("gateup", n=64, k=1024, M=1, seed=3).signs), None)
+
+
+@pytest.mark.slow
+def test_gate_up_full_sampled():
+    """The gate/up shape (17408 x 5120 per projection), M = 1, fused kernel;
+    sampled rows of both projections from the oracle."""
+    c = synth.make_case("gateup")
+    n, k = c.values.shape
+    vu, su, du = _up_inputs(11, n, k)
+    pay_g = dev_u8(nt.ninfer_ternary_pack("PQ2_0_G128", c.values, c.scales))
+    pay_u = dev_u8(nt.ninfer_ternary_pack("PQ2_0_G128", vu, su))
+    y = nt.ninfer_ternary_gate_up("PQ2_0_G128", pay_g, pay_u, n, k, dev_x(c), dev_signs(c.signs), dev_signs(du))
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(5)
+    rows = np.unique(np.concatenate([[0, n - 1], rng.integers(0, n, 2000)]))
+    ref = oracle.gate_up_swiglu("PQ2_0_G128", oracle.pack_planes("PQ2_0_G128", c.values[rows], c.scales[rows]),
+                                oracle.pack_planes("PQ2_0_G128", vu[rows], su[rows]), rows.size, k, c.x,
+                                signs_values(c), synth.bf16_bits_to_f32(du).astype(np.float64))
+    assert oracle.max_rel_error(y.cpu().numpy()[:, rows].astype(np.float64), ref) <= TOL_DECODE

@@ -171,6 +171,28 @@ def m_pack_pad_minus_one(mp):
     _patch(mp, "pack_planes", pk)
 
 
+def m_swiglu_sigmoid_gate(mp):
+    def f(fmt, pg, pu, n, k, x, sg=None, su=None, rows=None):
+        g = T.ternary_matmul(fmt, pg, n, k, x, sg, rows)
+        u = T.ternary_matmul(fmt, pu, n, k, x, su, rows)
+        return 1.0 / (1.0 + np.exp(-g)) * u
+    _patch(mp, "gate_up_swiglu", f)
+
+
+def m_swiglu_operands_swapped(mp):
+    orig = _orig("gate_up_swiglu")
+    def f(fmt, pg, pu, n, k, x, sg=None, su=None, rows=None):
+        return orig(fmt, pu, pg, n, k, x, su, sg, rows)
+    _patch(mp, "gate_up_swiglu", f)
+
+
+def m_swiglu_one_sign_vector(mp):
+    orig = _orig("gate_up_swiglu")
+    def f(fmt, pg, pu, n, k, x, sg=None, su=None, rows=None):
+        return orig(fmt, pg, pu, n, k, x, sg, sg, rows)
+    _patch(mp, "gate_up_swiglu", f)
+
+
 MUTATIONS = [v for k, v in sorted(globals().items()) if k.startswith("m_")]
 
 
