@@ -42,9 +42,9 @@ def algorithmic_bytes(w, M: int) -> dict:
     """Bytes the method must move per call: packed planes + activations + signs + fp32 output."""
     groups = -(-w.k // 128)
     per_group = 34 if w.fmt == "PQ2_0_G128" else 28
-    weights = w.n * groups * per_group
+    weights = w.mats * w.n * groups * per_group
     xb = M * w.k * (4 if w.x_dtype == "f32" else 2)
-    sb = w.k * 2
+    sb = w.mats * w.k * 2
     yb = M * w.n * 4
     return {"weights": weights, "x": xb, "signs": sb, "y": yb, "total": weights + xb + sb + yb}
 
@@ -89,6 +89,8 @@ KERNEL_TAG = "gemv"
 
 def dominant_kernel(w):
     """(profile tag, source files) of the kernel that dominates one step of workload w."""
+    if w.mats == 2 and w.fmt == "PQ2_0_G128" and w.M == 1:
+        return KERNEL_TAG, GEMV_SOURCES + ["bit_gemv_gb300/csrc/ffn.cu"]
     if w.fmt == "PQ2_0_G128" and w.M == 1:
         return KERNEL_TAG, GEMV_SOURCES
     if w.fmt == "PQ2_0_G128" and w.M <= 8:
@@ -181,22 +183,33 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     nbytes = algorithmic_bytes(w, M)
     payload_host = nt.ninfer_ternary_pack(w.fmt, c.values, c.scales)
     del c.values
+    up_host = nt.ninfer_ternary_pack(w.fmt, c.up[0], c.up[1]) if w.mats == 2 else None
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    pool = max(2, -(-3 * l2 // payload_host.size))
+    pool = max(2, -(-3 * l2 // (w.mats * payload_host.size)))
     payloads = [torch.from_numpy(payload_host).to(dev) for _ in range(pool)]
     signs = torch.from_numpy(c.signs.view(np.int16)).to(dev)
+    if w.mats == 2:
+        payloads_up = [torch.from_numpy(up_host).to(dev) for _ in range(pool)]
+        signs_up = torch.from_numpy(c.up[2].view(np.int16)).to(dev)
     if w.x_dtype == "bf16":
         x_host = torch.from_numpy(c.x_raw.view(np.int16)).view(torch.bfloat16)
     else:
         x_host = torch.from_numpy(c.x)
     x = x_host.to(dev)
     y = torch.empty((M, n), dtype=torch.float32, device=dev)
-    ws_bytes = nt.ninfer_ternary_matmul_workspace(w.fmt, n, k, M, True)
+    if w.mats == 2:
+        ws_bytes = nt.ninfer_ternary_gate_up_workspace(w.fmt, n, k, M, True, True)
+    else:
+        ws_bytes = nt.ninfer_ternary_matmul_workspace(w.fmt, n, k, M, True)
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(dev)
 
     def step(i):
-        nt.ninfer_ternary_matmul(w.fmt, payloads[i % pool], n, k, x, signs, y=y, workspace=ws)
+        if w.mats == 2:
+            nt.ninfer_ternary_gate_up(w.fmt, payloads[i % pool], payloads_up[i % pool], n, k, x, signs, signs_up, y=y,
+                                      workspace=ws)
+        else:
+            nt.ninfer_ternary_matmul(w.fmt, payloads[i % pool], n, k, x, signs, y=y, workspace=ws)
 
     # e2e buffers: pinned host activations in, pinned host result out
     x_pin = [x_host.clone().pin_memory() for _ in range(pool)]
@@ -285,8 +298,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         "dtype": path_dtype(w),
         "data": "synthetic",
         "config": {"workload": args.workload, "format": w.fmt, "n": n, "k": k, "M": M, "x_dtype": w.x_dtype,
-                   "seed": w.seed, "rotate": True,
-                   "l2": f"rotating pool of {pool} payload copies ({pool * payload_host.size / 1e6:.0f} MB > 3x L2 "
+                   "seed": w.seed, "rotate": True, "projections": w.mats,
+                   "l2": f"rotating pool of {pool} payload copies ({pool * w.mats * payload_host.size / 1e6:.0f} MB > 3x L2 "
                          f"{l2 / 1e6:.0f} MB)",
                    "parallelism": f"replicas x{world}"},
         "tokens_per_s": round(world * M / s_step, 1),
@@ -323,7 +336,12 @@ def kernels_per_step(w) -> int:
     themselves (PTQ1_0 with k > 8192 also runs its prep kernel); the PTQ1_0
     M <= 8 kernel rotates x itself and, with more than one 1024-block, is
     followed by the block reduction; the PQ2_0 M <= 8, prefill and general
-    paths run a prep or transform kernel and then the main one."""
+    paths run a prep or transform kernel and then the main one. The fused
+    gate/up pair at PQ2_0, M = 1 is one kernel."""
+    if w.mats == 2 and w.fmt == "PQ2_0_G128" and w.M == 1:
+        return 1
+    if w.mats == 2:
+        return 2 * kernels_per_step(synth.WORKLOADS["gateup"] if w.fmt == "PQ2_0_G128" else w) + 1
     if w.M == 1:
         return 2 if (w.fmt == "PTQ1_0_G128" and w.k > 8192) else 1
     if w.fmt == "PTQ1_0_G128" and w.M <= 8:
@@ -342,12 +360,18 @@ def cpu_oracle_sample(workload: str, rows: int, reps: int) -> dict:
     c = synth.make_case(w, n=rows)
     payload = oracle.pack_planes(w.fmt, c.values, c.scales)
     D = synth.bf16_bits_to_f32(c.signs)
+    if w.mats == 2:
+        payload_up = oracle.pack_planes(w.fmt, c.up[0], c.up[1])
+        D_up = synth.bf16_bits_to_f32(c.up[2])
     t0 = time.perf_counter()
     for _ in range(reps):
-        oracle.ternary_matmul(w.fmt, payload, rows, w.k, c.x, D)
+        if w.mats == 2:
+            oracle.gate_up_swiglu(w.fmt, payload, payload_up, rows, w.k, c.x, D, D_up)
+        else:
+            oracle.ternary_matmul(w.fmt, payload, rows, w.k, c.x, D)
     dt = (time.perf_counter() - t0) / reps
     groups = -(-w.k // 128)
-    wbytes = rows * groups * (34 if w.fmt == "PQ2_0_G128" else 28)
+    wbytes = w.mats * rows * groups * (34 if w.fmt == "PQ2_0_G128" else 28)
     return {"seconds_per_call": dt, "weight_bytes": wbytes, "rows": rows}
 
 

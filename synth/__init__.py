@@ -108,6 +108,7 @@ class Workload:
     seed: int
     rotate: bool = True
     description: str = ""
+    mats: int = 1            # 2: FFN gate and up projections of one activation (SwiGLU product)
 
 
 WORKLOADS = {
@@ -123,6 +124,9 @@ WORKLOADS = {
                         description="prefill GEMM, PQ2_0_G128 n=17408 k=5120, M=2048 token rows"),
     "prefill_down": Workload("prefill_down", "PTQ1_0_G128", 5120, 17408, 2048, "bf16", 5,
                              description="prefill GEMM, PTQ1_0_G128 n=5120 k=17408 (FFN down), M=2048 token rows"),
+    "ffn_gate_up": Workload("ffn_gate_up", "PQ2_0_G128", 17408, 5120, 1, "bf16", 6,
+                            description="FFN gate and up projections, PQ2_0_G128 17408x5120 each with its own "
+                                        "sign vector, SwiGLU product, M=1", mats=2),
     "head": Workload("head", "PQ2_0_G128", 248320, 5120, 1, "bf16", 4,
                      description="output head, PQ2_0_G128 n=248320 k=5120, M=1"),
     "head_m8": Workload("head_m8", "PQ2_0_G128", 248320, 5120, 8, "bf16", 4,
@@ -142,6 +146,14 @@ class Case:
     x: np.ndarray            # M x k float32 values (exactly representable in x_dtype)
     x_raw: np.ndarray        # M x k storage array (uint16 bf16 bits or float32)
     ids: np.ndarray = field(default_factory=lambda: np.zeros(0, np.int32))
+    up: tuple | None = None  # (values, scales, signs) of the up projection when workload.mats == 2
+
+
+def up_projection(seed: int, n: int, k: int):
+    """The second projection of a gate/up pair: values, scales and signs drawn
+    in that order from default_rng(seed), with the distributions above."""
+    rng = np.random.default_rng(seed)
+    return ternary_values(rng, n, k), group_scales(rng, n, -(-k // GROUP)), sign_vector(rng, k)
 
 
 def make_case(w: Workload | str, n: int | None = None, k: int | None = None,
@@ -149,7 +161,8 @@ def make_case(w: Workload | str, n: int | None = None, k: int | None = None,
     """Draw every input of a workload in a fixed order from default_rng(seed).
 
     Order: values, scales, signs, activations, ids. n/k/M/seed override the
-    preset (smaller shapes with the same distributions for parity tests).
+    preset (smaller shapes with the same distributions for parity tests). A
+    two-projection workload also draws the up projection from up_projection(seed + 1000).
     """
     if isinstance(w, str):
         w = WORKLOADS[w]
@@ -164,4 +177,5 @@ def make_case(w: Workload | str, n: int | None = None, k: int | None = None,
     signs = sign_vector(rng, k) if w.rotate else np.zeros(0, np.uint16)
     x, x_raw = activations(rng, M, k, w.x_dtype)
     ids = token_ids(rng, EMBED_COUNT, n) if with_ids else np.zeros(0, np.int32)
-    return Case(w, values, scales, signs, x, x_raw, ids)
+    up = up_projection(seed + 1000, n, k) if w.mats == 2 else None
+    return Case(w, values, scales, signs, x, x_raw, ids, up)

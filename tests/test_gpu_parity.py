@@ -297,11 +297,7 @@ def test_blocks_planes_device_matches_oracle(fmt, n, k):
 
 
 # ------------------------------------------------------- fused FFN gate/up ---
-def _up_inputs(seed, n, k):
-    """The up projection's values, scales and signs, from their own generator."""
-    rng = np.random.default_rng(seed)
-    groups = -(-k // 128)
-    return synth.ternary_values(rng, n, k), synth.group_scales(rng, n, groups), synth.sign_vector(rng, k)
+_up_inputs = synth.up_projection     # the up projection's values, scales and signs, from their own generator
 
 
 @pytest.mark.parametrize("fmt,n,k,M,same_signs", [
