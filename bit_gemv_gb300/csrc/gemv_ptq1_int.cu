@@ -12,9 +12,13 @@
 // Arithmetic: the rotated activation is 16-bit fixed point per 1024-block
 // (act16.cuh). A 256-entry table maps a code byte to its digits as bytes
 // (t0 | t1 << 8 | t2 << 16 | t3 << 24, with t4 in bits 2-3 of byte 0); the
-// table is replicated 32 times so that lane l always reads bank l. Per base
-// byte, dp2a multiplies (t0, t1) and (t2, t3) by int16 activation pairs and
-// 4 * t4 by the fifth activation, exactly in int32. Per group:
+// table is replicated 32 times so that lane l always reads bank l (entry B of
+// lane l at B * 128 + 4 l, from the start of shared memory). Per base byte,
+// dp2a multiplies (t0, t1) and
+// (t2, t3) by int16 activation pairs; the t4 fields of four consecutive bytes
+// are gathered into one word by byte permutes and multiplied by two pairs of
+// fifth activations (times 4, removed at the end), all exactly in int32. Per
+// group:
 //   y += scale * 2^-E * (sum t x16 - sum x16)                    (value = t - 1)
 //
 // Data movement: one CTA per SM owns a contiguous range of rows, processed as
@@ -51,8 +55,8 @@ constexpr uint32_t kItemBytes = 3 * kBaseBox + 2 * 32 * kRows;
 constexpr uint32_t kMaxSlots = 12;
 constexpr uint32_t kRotPairs = 8;
 constexpr uint32_t kMaxRem = 2;   // extra rows beyond whole row blocks handled per (row, group)
-constexpr uint32_t kActWords = 76; // per group: 24 base bytes x 3 words + 2 high bytes x 2 words
-constexpr uint32_t kLutBytes = 256 * 32 * 4;
+constexpr uint32_t kActWords = 64; // per group: 24 base bytes x 2 words + 6 t4 quads x 2 words + 2 high bytes x 2 words
+constexpr uint32_t kLutBytes = 256 * 128; // entry B at B * 128: 32 lane copies
 
 struct Ptq1Params {
     CUtensorMap bmap_main, bmap_last;   // base rows {row bytes, R rows, CTA} / last CTA, boxes 128 B x 32 rows
@@ -69,7 +73,7 @@ struct Ptq1Params {
     uint32_t k, groups, nblk, nch, rows_per_cta;
     int x_dtype, y_dtype;
     uint32_t nslots, pre_issue;
-    uint32_t off_ring, off_act, off_lut, off_rot, off_rem, off_part, off_bar, off_cnt;
+    uint32_t off_ring, off_act, off_rot, off_rem, off_part, off_bar, off_cnt;     // the table is at offset 0
     uint32_t *err;
 };
 
@@ -119,8 +123,9 @@ __device__ __forceinline__ void issue_item(const Ptq1Params &p, uint8_t *smem, u
 }
 
 // Operand words of block b from its x16 (rotate_quantize16): per group G,
-//   word 3j + c (j < 24): c = 0 -> (x16[5j], x16[5j+1]), 1 -> (x16[5j+2], x16[5j+3]), 2 -> (x16[5j+4], 0)
-//   word 72 + 2h + c (h < 2): (x16[120+4h+2c], x16[121+4h+2c])
+//   word 2j + c (j < 24): c = 0 -> (x16[5j], x16[5j+1]), 1 -> (x16[5j+2], x16[5j+3])
+//   word 48 + 2q + c (q < 6): (x16[5(4q+2c)+4], x16[5(4q+2c+1)+4])   (the t4 weights of bytes 4q .. 4q+3)
+//   word 60 + 2h + c (h < 2): (x16[120+4h+2c], x16[121+4h+2c])
 // and gs[G] = {2^-E, sum of the group's x16 (as int bits)}. The block's 8
 // groups have 208 code bytes (192 base, 16 high); thread t of the pair takes
 // bytes t, t + 64, t + 128 and t + 192.
@@ -137,14 +142,14 @@ __device__ __forceinline__ void pack_ptq1(const int16_t *qs, uint8_t *act_s, uin
         if (u < 192) {
             const uint32_t j = u % 24;
             const int16_t *e = qs + 128 * gl + 5 * j;
-            dst[3 * j] = (uint32_t)(uint16_t)e[0] | ((uint32_t)(uint16_t)e[1] << 16);
-            dst[3 * j + 1] = (uint32_t)(uint16_t)e[2] | ((uint32_t)(uint16_t)e[3] << 16);
-            dst[3 * j + 2] = (uint32_t)(uint16_t)e[4];
+            dst[2 * j] = (uint32_t)(uint16_t)e[0] | ((uint32_t)(uint16_t)e[1] << 16);
+            dst[2 * j + 1] = (uint32_t)(uint16_t)e[2] | ((uint32_t)(uint16_t)e[3] << 16);
+            reinterpret_cast<int16_t *>(dst + 48 + 2 * (j >> 2) + ((j >> 1) & 1))[j & 1] = e[4];
         } else {
             const uint32_t hh = (u - 192) & 1;
             const int16_t *e = qs + 128 * gl + 120 + 4 * hh;
-            dst[72 + 2 * hh] = (uint32_t)(uint16_t)e[0] | ((uint32_t)(uint16_t)e[1] << 16);
-            dst[73 + 2 * hh] = (uint32_t)(uint16_t)e[2] | ((uint32_t)(uint16_t)e[3] << 16);
+            dst[60 + 2 * hh] = (uint32_t)(uint16_t)e[0] | ((uint32_t)(uint16_t)e[1] << 16);
+            dst[61 + 2 * hh] = (uint32_t)(uint16_t)e[2] | ((uint32_t)(uint16_t)e[3] << 16);
         }
     }
     // group sums: thread t sums elements 16t .. 16t + 15 (group t / 8)
@@ -179,34 +184,41 @@ __global__ void __launch_bounds__(64) ptq1_prep_kernel(const XSource xsrc, uint3
 }
 
 // sum_j t_j x16_j of one group: 24 base bytes (six words) and 2 high bytes,
-// table lookups in lane-private copies, operand words from shared memory.
-__device__ __forceinline__ int group_dot(const uint32_t (&bw)[6], uint32_t hb, const uint32_t *lut, int lane,
+// table lookups in lane-private copies, operand words from shared memory: the
+// lane's copy of entry B sits at lut + (B << 7 | lane4), lane4 = 4 * lane.
+__device__ __forceinline__ int group_dot(const uint32_t (&bw)[6], uint32_t hb, uint32_t lut, uint32_t lane4,
                                          const uint4 *aw) {
-    uint4 a[19];
+    uint4 a[16];
 #pragma unroll
-    for (int i = 0; i < 19; ++i) a[i] = aw[i];
+    for (int i = 0; i < 16; ++i) a[i] = aw[i];
     const uint32_t *av = reinterpret_cast<const uint32_t *>(a);
     int acc[4] = {0, 0, 0, 0}, acc4 = 0;
-    const uint8_t *lutb = reinterpret_cast<const uint8_t *>(lut) + 4 * lane;
 #pragma unroll
-    for (int j = 0; j < 24; ++j) {
-        // byte (j & 3) of word j >> 2, times 128 (one table row of 32 copies)
-        const int sh = 8 * (j & 3) - 7;
-        const uint32_t off = (sh >= 0 ? bw[j >> 2] >> sh : bw[j >> 2] << (-sh)) & 0x7F80u;
-        const uint32_t W = *reinterpret_cast<const uint32_t *>(lutb + off);
-        const uint32_t m = W & 0x03030303u;
-        acc[j & 3] = dp2a_lo(av[3 * j], m, acc[j & 3]);
-        acc[j & 3] = dp2a_hi(av[3 * j + 1], m, acc[j & 3]);
-        acc4 = dp2a_lo(av[3 * j + 2], W & 0x0000000Cu, acc4);
+    for (int q = 0; q < 6; ++q) {
+        uint32_t W[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const int sh = 8 * c - 7;
+            const uint32_t off = ((sh >= 0 ? bw[q] >> sh : bw[q] << (-sh)) & 0x7F80u) | lane4;
+            W[c] = lds32(lut + off);
+            const uint32_t m = W[c] & 0x03030303u;
+            const int j = 4 * q + c;
+            acc[c] = dp2a_lo(av[2 * j], m, acc[c]);
+            acc[c] = dp2a_hi(av[2 * j + 1], m, acc[c]);
+        }
+        // byte 0 of each entry holds 4 * t4 in bits 2-3: gather the four
+        const uint32_t g = __byte_perm(__byte_perm(W[0], W[1], 0x0040u), __byte_perm(W[2], W[3], 0x0040u), 0x5410u) &
+                           0x0C0C0C0Cu;
+        acc4 = dp2a_lo(av[48 + 2 * q], g, acc4);
+        acc4 = dp2a_hi(av[49 + 2 * q], g, acc4);
     }
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
         const int sh = 8 * hh - 7;
-        const uint32_t off = (sh >= 0 ? hb >> sh : hb << (-sh)) & 0x7F80u;
-        const uint32_t W = *reinterpret_cast<const uint32_t *>(lutb + off);
-        const uint32_t m = W & 0x03030303u;
-        acc[hh] = dp2a_lo(av[72 + 2 * hh], m, acc[hh]);
-        acc[hh] = dp2a_hi(av[73 + 2 * hh], m, acc[hh]);
+        const uint32_t off = ((sh >= 0 ? hb >> sh : hb << (-sh)) & 0x7F80u) | lane4;
+        const uint32_t m = lds32(lut + off) & 0x03030303u;
+        acc[hh] = dp2a_lo(av[60 + 2 * hh], m, acc[hh]);
+        acc[hh] = dp2a_hi(av[61 + 2 * hh], m, acc[hh]);
     }
     return acc[0] + acc[1] + acc[2] + acc[3] + (acc4 >> 2);
 }
@@ -221,7 +233,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ptq1_int_kernel(const __grid
     const uint32_t rem_bar = bar0 + 8 * kMaxSlots;
     uint32_t *cnt = reinterpret_cast<uint32_t *>(smem + p.off_cnt);
     uint32_t *issued = cnt + kMaxSlots, *failed = cnt + kMaxSlots + 1;
-    uint32_t *lut = reinterpret_cast<uint32_t *>(smem + p.off_lut);
+    uint32_t *lut = reinterpret_cast<uint32_t *>(smem);      // the table starts the dynamic shared memory
+    const uint32_t lut_s = smem_u32(smem), lane4 = 4u * (uint32_t)lane;
     uint8_t *rem_s = smem + p.off_rem;
 
     if (tid == 0) {
@@ -256,8 +269,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ptq1_int_kernel(const __grid
             }
         }
     }
-    // digit table, replicated per bank: entry (B, l) at 32 B + l; thread tid
-    // computes entry tid / 2 and writes 16 of its copies
+    // digit table, replicated per bank: entry (B, l) at word 32 B + l; thread
+    // tid computes entry tid / 2 and writes 16 of its copies
     {
         uint32_t B = (uint32_t)tid >> 1, W = 0;
 #pragma unroll
@@ -291,10 +304,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ptq1_int_kernel(const __grid
         bulk_g2s(smem_u32(act_s), p.act_g, p.act_bytes, act_bar);
     }
     __syncthreads();     // every warp's x request is out: the rest of the ring queues behind them
-    if (tid == 0) {
-        for (uint32_t i = pre; i < ring_to; ++i) issue_item(p, smem, i, last_cta);
-        *issued = ring_to;
-    }
+    // the rest of the ring, one item per warp (lane 0 of warp w: items pre + w, pre + w + 16, ...)
+    if (lane == 0)
+        for (uint32_t i = pre + warp; i < ring_to; i += kWarps) issue_item(p, smem, i, last_cta);
+    if (tid == 0) *issued = ring_to;
     if (pr < nrot) {
         float *tile = reinterpret_cast<float *>(smem + p.off_rot + pr * kRotScratch);
         for (uint32_t b = pr; b < p.nblk; b += nrot) {
@@ -307,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ptq1_int_kernel(const __grid
             pack_ptq1(qs, act_s, p.groups, b, t, E, 1 + pr);
         }
     }
-    __syncthreads();
+    if (nrot) __syncthreads();      // the rotated operand words are complete (else they arrive on act_bar)
 
     bool ok = true;
     if (p.act_g) ok = mbar_wait(act_bar, 0, p.err);
@@ -332,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ptq1_int_kernel(const __grid
                 const uint32_t hb = *reinterpret_cast<const uint16_t *>(row + p.base_row + 2 * G);
                 const float s = __half2float(*reinterpret_cast<const __half *>(row + p.base_row + p.high_row + 2 * G));
                 const float2 f = gs[G];
-                const int dot = group_dot(bw, hb, lut, lane, reinterpret_cast<const uint4 *>(act_w + G * kActWords));
+                const int dot = group_dot(bw, hb, lut_s, lane4, reinterpret_cast<const uint4 *>(act_w + G * kActWords));
                 part_rem[rr * p.groups + G] = s * f.x * (float)(dot - __float_as_int(f.y));
             }
         }
@@ -363,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ptq1_int_kernel(const __grid
                 const float s =
                     __half2float(*reinterpret_cast<const __half *>(sa + 3 * kBaseBox + 32 * kRows + lane * 32 + 2 * warp));
                 const float2 f = gs[G];
-                const int dot = group_dot(bw, hb, lut, lane, reinterpret_cast<const uint4 *>(act_w + G * kActWords));
+                const int dot = group_dot(bw, hb, lut_s, lane4, reinterpret_cast<const uint4 *>(act_w + G * kActWords));
                 y = fmaf(s * f.x, (float)(dot - __float_as_int(f.y)), y);
             }
             if (refill) {
@@ -458,10 +471,10 @@ bool gemv_ptq1_int_plan(const ninfer_row_split_geometry &g, uint64_t M, bool rot
     plan->nslots = nslots;
     plan->pre_issue = std::min<uint32_t>(1, nslots);
     uint32_t off = 0;
+    plan->off_lut = off;         // fixed at 0: the kernel addresses the table from the start of its shared memory
+    off += kLutBytes;
     plan->off_ring = off;
     off += nslots * kItemBytes;
-    plan->off_lut = off;
-    off += kLutBytes;
     plan->off_act = off;
     off += act_bytes;
     plan->off_rot = off;
@@ -509,7 +522,6 @@ int gemv_ptq1_int_launch(const Ptq1Plan &plan, const uint8_t *payload, const nin
     p.pre_issue = plan.pre_issue;
     p.off_ring = plan.off_ring;
     p.off_act = plan.off_act;
-    p.off_lut = plan.off_lut;
     p.off_rot = plan.off_rot;
     p.off_rem = plan.off_rem;
     p.off_part = plan.off_part;
