@@ -18,18 +18,22 @@
 //    every run of 16 elements it stores the order 0,8,1,9,...,7,15, which is the
 //    order in which one 32-bit word of codes decodes with one mask per pair
 //    (codes j and j+8 sit at bits 2j and 2j+16).
-//  * gemm_tc_kernel computes one 128 (tokens) x 128 (weight rows) output tile per
-//    CTA, two CTAs per SM, K in stages of 64:
-//      warp 0       TMA producer: xr tile (128 x 64 binary16, 128-byte swizzle),
-//                   the tile's 64 codes per weight row (16 bytes) and the 8
-//                   scales that cover them (16 bytes);
+//  * gemm_tc_kernel computes one 128 (weight rows) x 128 (tokens) output tile per
+//    CTA, two CTAs per SM, K in stages of 64. The expanded weights are the MMA's
+//    A operand and live in tensor memory, so they never pass through shared
+//    memory; xr is the B operand, in shared memory:
+//      warp 0       TMA producer: xr tile (128 tokens x 64 binary16, 128-byte
+//                   swizzle), the tile's 64 codes per weight row (16 bytes) and
+//                   the 8 scales that cover them (16 bytes);
 //      warp 1       TMEM owner and MMA issuer (one thread): four K=16 MMAs per stage;
-//      warps 2..5   decode: thread t expands weight row t's 64 codes to binary16
-//                   (code - 1) * scale and writes them in the canonical K-major
-//                   128-byte-swizzled layout; after the K loop they read the
-//                   accumulators out of tensor memory and store y.
-//    Stages are handed over with mbarriers (TMA transaction counts, 128 decoder
-//    arrivals, and tcgen05.commit for "stage consumed"); every wait is bounded.
+//      warps 2..5   decode: lane l of warp w expands weight row 32 (w % 4) + l
+//                   (its tensor-memory lane) to binary16 (code - 1) * scale and
+//                   stores the stage's 32 binary16 pairs into the stage's A
+//                   columns; after the K loop they read the accumulators (lane =
+//                   weight row, column = token) and store y.
+//    Stages are handed over with mbarriers (TMA transaction counts, one arrival
+//    per decode warp, and tcgen05.commit for "stage consumed", which frees the
+//    shared-memory stage and its A columns together); every wait is bounded.
 #include <cstring>
 
 #include <cuda.h>
@@ -44,17 +48,20 @@
 namespace ninfer {
 namespace {
 
-constexpr int kBM = 128, kBN = 128, kBK = 64;      // tokens, weight rows, k per stage
-constexpr int kStages = 3;
-constexpr uint32_t kABytes = kBM * kBK * 2;        // 16 KB of xr
-constexpr uint32_t kBBytes = kBN * kBK * 2;        // 16 KB of expanded weights
+constexpr int kBM = 128, kBN = 128, kBK = 64;      // tokens (MMA N), weight rows (MMA M), k per stage
+constexpr int kStages = 4;
+constexpr uint32_t kXBytes = kBM * kBK * 2;        // 16 KB of xr
 constexpr uint32_t kCodeBytes = kBN * 16;          // 64 codes per weight row
 constexpr uint32_t kScaleBytes = kBN * 16;         // 8 scales per weight row
-constexpr uint32_t kStageBytes = kABytes + kBBytes + kCodeBytes + kScaleBytes;     // 36 KB, 1024-aligned
+constexpr uint32_t kStageBytes = kXBytes + kCodeBytes + kScaleBytes;     // 20 KB, 1024-aligned
 constexpr uint32_t kBarBytes = 8 * (3 * kStages + 1);
 constexpr uint32_t kSmemBytes = ((kStages * kStageBytes + kBarBytes + 16 + 1023) / 1024) * 1024;
 constexpr int kThreads = 192;
-constexpr uint32_t kTmemCols = 128;                // fp32 accumulators, one column per weight row
+constexpr uint32_t kAccCols = kBM;                 // fp32 accumulators: lane = weight row, column = token
+constexpr uint32_t kACols = kBK / 2;               // a stage's weights per row, as binary16 pairs
+constexpr uint32_t kTmemCols = 256;                // accumulators + the A stages, a power of two
+static_assert(kAccCols + kStages * kACols <= kTmemCols, "tensor memory plan");
+static_assert(kStageBytes % 1024 == 0, "swizzled xr tiles need 1024-byte alignment");
 
 struct TcParams {
     CUtensorMap amap, cmap, smap;
@@ -72,14 +79,16 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
            (2ull << 61);
 }
 
-// Instruction descriptor of kind::f16: fp32 D, binary16 A and B, both K-major, M = 128, N = 128.
-constexpr uint32_t kIdesc = (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+// Instruction descriptor of kind::f16: fp32 D, binary16 A and B, both K-major,
+// M = 128 (weight rows), N = 128 (tokens).
+constexpr uint32_t kIdesc = (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(kBM >> 3) << 17) | ((uint32_t)(kBN >> 4) << 24);
 
-__device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+// D (tensor memory) += A (tensor memory, M x 16) * B (shared memory descriptor, 16 x N).
+__device__ __forceinline__ void mma_f16_tmem_a(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc, uint32_t accumulate) {
     asm volatile(
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(tmem_d),
-        "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(tmem_d),
+        "r"(tmem_a), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
         : "memory");
 }
 
@@ -105,6 +114,19 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 32 consecutive 32-bit columns of this warp's 32 TMEM lanes, from registers.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+        "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+        "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 // Codes j and j+8 of a 32-bit code word as a binary16 pair ((c - 1) * s):
@@ -181,7 +203,8 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_tc_kernel(const __grid_const
     const uint32_t accum_bar = bar + 8 * 3 * kStages;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kStages * kStageBytes + kBarBytes);
     const uint64_t n0 = (uint64_t)blockIdx.x * kBN, m0 = (uint64_t)blockIdx.y * kBM;
-    // full_a[s]: xr, codes and scales landed; full_b[s]: weights expanded; empty[s]: stage consumed
+    // full_a[s]: xr, codes and scales landed; full_b[s]: weights expanded into the
+    // stage's A columns; empty[s]: stage consumed (shared memory and A columns)
 #define FULL_A(s) (bar + 8 * (s))
 #define FULL_B(s) (bar + 8 * (kStages + (s)))
 #define EMPTY(s) (bar + 8 * (2 * kStages + (s)))
@@ -198,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_tc_kernel(const __grid_const
         prefetch_tmap(&p.smap);
         for (int s = 0; s < kStages; ++s) {
             mbar_init(FULL_A(s), 1);
-            mbar_init(FULL_B(s), 128);
+            mbar_init(FULL_B(s), 4);
             mbar_init(EMPTY(s), 1);
         }
         mbar_init(accum_bar, 1);
@@ -215,10 +238,10 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_tc_kernel(const __grid_const
                 const uint32_t s = kt % kStages, round = kt / kStages;
                 if (round > 0 && !mbar_wait(EMPTY(s), (round - 1) & 1, p.err)) break;
                 const uint32_t st = base + s * kStageBytes;
-                mbar_arrive_expect_tx(FULL_A(s), kABytes + kCodeBytes + kScaleBytes);
+                mbar_arrive_expect_tx(FULL_A(s), kXBytes + kCodeBytes + kScaleBytes);
                 tma_load_2d(st, &p.amap, (int)(kt * kBK), (int)m0, FULL_A(s));
-                tma_load_2d(st + kABytes + kBBytes, &p.cmap, (int)(kt * 16), (int)n0, FULL_A(s));
-                tma_load_2d(st + kABytes + kBBytes + kCodeBytes, &p.smap, (int)((kt / 16) * 16), (int)n0, FULL_A(s));
+                tma_load_2d(st + kXBytes, &p.cmap, (int)(kt * 16), (int)n0, FULL_A(s));
+                tma_load_2d(st + kXBytes + kCodeBytes, &p.smap, (int)((kt / 16) * 16), (int)n0, FULL_A(s));
             }
         }
     } else if (warp == 1) {
@@ -227,66 +250,63 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_tc_kernel(const __grid_const
                 const uint32_t s = kt % kStages, par = (kt / kStages) & 1;
                 if (!mbar_wait(FULL_A(s), par, p.err) || !mbar_wait(FULL_B(s), par, p.err)) break;
                 tc_fence_after();
-                const uint32_t st = base + s * kStageBytes;
-                const uint64_t adesc = sw128_desc(st), bdesc = sw128_desc(st + kABytes);
+                const uint64_t bdesc = sw128_desc(base + s * kStageBytes);
+                const uint32_t acol = tmem + kAccCols + kACols * s;
 #pragma unroll
-                for (int kk = 0; kk < kBK / 16; ++kk)      // +32 bytes along K per MMA (16-byte units: +2)
-                    mma_f16(tmem, adesc + 2 * kk, bdesc + 2 * kk, (kt | kk) != 0);
+                for (int kk = 0; kk < kBK / 16; ++kk)      // A: +8 columns, B: +32 bytes (16-byte units: +2) per K=16
+                    mma_f16_tmem_a(tmem, acol + 8 * kk, bdesc + 2 * kk, (kt | kk) != 0);
                 mma_commit(EMPTY(s));
             }
             mma_commit(accum_bar);
         }
     } else {
-        const int t = tid - 64;     // weight row of the tile
+        // warp w may touch TMEM lanes 32 (w % 4) .. 32 (w % 4) + 31: its lane l is weight row 32 (w % 4) + l
+        const uint32_t q = warp & 3;
+        const uint32_t r = 32 * q + lane;
+        const uint32_t lane_addr = tmem + ((32u * q) << 16);
         for (uint32_t kt = 0; kt < p.nk; ++kt) {
             const uint32_t s = kt % kStages, par = (kt / kStages) & 1;
-            if (!mbar_wait(FULL_A(s), par, p.err)) break;
-            uint8_t *st = smem + s * kStageBytes;
-            const uint4 cw = *reinterpret_cast<const uint4 *>(st + kABytes + kBBytes + t * 16);
+            // warp-uniform: the tensor-memory store below is a warp-wide instruction
+            if (!__all_sync(0xffffffffu, mbar_wait(FULL_A(s), par, p.err))) break;
+            const uint8_t *st = smem + s * kStageBytes;
+            const uint4 cw = *reinterpret_cast<const uint4 *>(st + kXBytes + r * 16);
             const __half sc =
-                *reinterpret_cast<const __half *>(st + kABytes + kBBytes + kCodeBytes + t * 16 + 2 * ((kt / 2) % 8));
+                *reinterpret_cast<const __half *>(st + kXBytes + kCodeBytes + r * 16 + 2 * ((kt / 2) % 8));
             const __half2 s2 = __halves2half2(sc, sc);
-            uint8_t *brow = st + kABytes + t * 128;
             const uint32_t w[4] = {cw.x, cw.y, cw.z, cw.w};
+            // column 8 i + j holds the pair (code 16 i + j, code 16 i + j + 8): the
+            // K order 0,8,1,9,... of every run of 16, as xr is stored
+            uint32_t a[32];
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    uint4 o;
-                    o.x = expand_pair(w[i], 4 * hh + 0, s2);
-                    o.y = expand_pair(w[i], 4 * hh + 1, s2);
-                    o.z = expand_pair(w[i], 4 * hh + 2, s2);
-                    o.w = expand_pair(w[i], 4 * hh + 3, s2);
-                    *reinterpret_cast<uint4 *>(brow + ((((2 * i + hh) ^ (t & 7))) << 4)) = o;
-                }
-            fence_proxy_async();      // generic-proxy writes, read by the tensor core
-            mbar_arrive(FULL_B(s));
+                for (int j = 0; j < 8; ++j) a[8 * i + j] = expand_pair(w[i], j, s2);
+            tmem_st32(lane_addr + kAccCols + kACols * s, a);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(FULL_B(s));
         }
-        // epilogue: TMEM lanes 32q .. 32q + 31 are this warp's token rows
+        // epilogue: lane = weight row n0 + r, columns = the tile's tokens
         const bool done = __all_sync(0xffffffffu, mbar_wait(accum_bar, 0, p.err));
         tc_fence_after();
-        const uint32_t q = warp & 3;
-        const uint64_t m = m0 + 32 * q + lane;
+        const uint64_t row = n0 + r;
         if (done) {
 #pragma unroll 1
-            for (int cb = 0; cb < kBN / 32; ++cb) {
+            for (int cb = 0; cb < kBM / 32; ++cb) {
                 float v[32];
-                tmem_ld32(tmem + ((32 * q) << 16) + 32 * cb, v);
-                const uint64_t nc = n0 + 32 * cb;
-                if (m >= p.M || nc >= p.n) continue;
-                const uint64_t off = m * p.n + nc;
-                const bool full = nc + 32 <= p.n;
+                tmem_ld32(lane_addr + 32 * cb, v);
+                const uint64_t mb = m0 + 32 * cb;
+                if (row >= p.n || mb >= p.M) continue;
+                const int cnt = p.M - mb < 32 ? (int)(p.M - mb) : 32;
                 if (p.y_dtype == NINFER_F32) {
-                    float *yp = static_cast<float *>(p.y) + off;
-                    if (full && (off % 4) == 0) {
+                    float *yp = static_cast<float *>(p.y) + mb * p.n + row;
 #pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            reinterpret_cast<float4 *>(yp)[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-                    } else {
-                        for (int i = 0; i < 32 && nc + i < p.n; ++i) yp[i] = v[i];
-                    }
+                    for (int i = 0; i < 32; ++i)
+                        if (i < cnt) yp[(uint64_t)i * p.n] = v[i];
                 } else {
-                    for (int i = 0; i < 32 && nc + i < p.n; ++i) store1(p.y, off + i, p.y_dtype, v[i]);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (i < cnt) store1(p.y, (mb + i) * p.n + row, p.y_dtype, v[i]);
                 }
             }
         }
