@@ -18,22 +18,26 @@
 //    every run of 16 elements it stores the order 0,8,1,9,...,7,15, which is the
 //    order in which one 32-bit word of codes decodes with one mask per pair
 //    (codes j and j+8 sit at bits 2j and 2j+16).
-//  * gemm_tc_kernel computes one 128 (weight rows) x 128 (tokens) output tile per
-//    CTA, two CTAs per SM, K in stages of 64. The expanded weights are the MMA's
-//    A operand and live in tensor memory, so they never pass through shared
-//    memory; xr is the B operand, in shared memory:
-//      warp 0       TMA producer: xr tile (128 tokens x 64 binary16, 128-byte
+//  * gemm_tc_kernel is persistent: one CTA per SM walks the output tiles
+//    (128 weight rows x 192 tokens) t = blockIdx.x, blockIdx.x + gridDim.x, ...,
+//    K in stages of 64. The expanded weights are the MMA's A operand and live in
+//    tensor memory, so they never pass through shared memory; xr is the B
+//    operand, in shared memory. Two accumulator buffers in tensor memory let the
+//    epilogue of one tile run under the main loop of the next:
+//      warp 0       TMA producer: xr tile (192 tokens x 64 binary16, 128-byte
 //                   swizzle), the tile's 64 codes per weight row (16 bytes) and
 //                   the 8 scales that cover them (16 bytes);
-//      warp 1       TMEM owner and MMA issuer (one thread): four K=16 MMAs per stage;
+//      warp 1       TMEM owner and MMA issuer (one thread): four K=16 MMAs per
+//                   stage into the tile's accumulator buffer;
 //      warps 2..5   decode: lane l of warp w expands weight row 32 (w % 4) + l
 //                   (its tensor-memory lane) to binary16 (code - 1) * scale and
-//                   stores the stage's 32 binary16 pairs into the stage's A
-//                   columns; after the K loop they read the accumulators (lane =
-//                   weight row, column = token) and store y.
-//    Stages are handed over with mbarriers (TMA transaction counts, one arrival
-//    per decode warp, and tcgen05.commit for "stage consumed", which frees the
-//    shared-memory stage and its A columns together); every wait is bounded.
+//                   stores the stage's 32 binary16 pairs into the stage's A columns;
+//      warps 6..9   epilogue: read a finished accumulator buffer (lane = weight
+//                   row, column = token), store y, hand the buffer back.
+//    Stages and buffers are handed over with mbarriers (TMA transaction counts,
+//    one arrival per decode or epilogue warp, and tcgen05.commit for "stage
+//    consumed" and "tile accumulated"); every wait is bounded.
+#include <algorithm>
 #include <cstring>
 
 #include <cuda.h>
@@ -48,26 +52,27 @@
 namespace ninfer {
 namespace {
 
-constexpr int kBM = 128, kBN = 128, kBK = 64;      // tokens (MMA N), weight rows (MMA M), k per stage
+constexpr int kBM = 192, kBN = 128, kBK = 64;      // tokens (MMA N), weight rows (MMA M), k per stage
 constexpr int kStages = 4;
-constexpr uint32_t kXBytes = kBM * kBK * 2;        // 16 KB of xr
+constexpr uint32_t kXBytes = kBM * kBK * 2;        // 24 KB of xr
 constexpr uint32_t kCodeBytes = kBN * 16;          // 64 codes per weight row
 constexpr uint32_t kScaleBytes = kBN * 16;         // 8 scales per weight row
-constexpr uint32_t kStageBytes = kXBytes + kCodeBytes + kScaleBytes;     // 20 KB, 1024-aligned
-constexpr uint32_t kBarBytes = 8 * (3 * kStages + 1);
+constexpr uint32_t kStageBytes = kXBytes + kCodeBytes + kScaleBytes;     // 28 KB, 1024-aligned
+constexpr uint32_t kBarBytes = 8 * (3 * kStages + 4);
 constexpr uint32_t kSmemBytes = ((kStages * kStageBytes + kBarBytes + 16 + 1023) / 1024) * 1024;
-constexpr int kThreads = 192;
-constexpr uint32_t kAccCols = kBM;                 // fp32 accumulators: lane = weight row, column = token
+constexpr int kThreads = 320;
+constexpr uint32_t kAccCols = kBM;                 // one fp32 accumulator buffer: lane = weight row, column = token
 constexpr uint32_t kACols = kBK / 2;               // a stage's weights per row, as binary16 pairs
-constexpr uint32_t kTmemCols = 256;                // accumulators + the A stages, a power of two
-static_assert(kAccCols + kStages * kACols <= kTmemCols, "tensor memory plan");
+constexpr uint32_t kAColBase = 2 * kAccCols;       // A stages after the two accumulator buffers
+constexpr uint32_t kTmemCols = 512;                // a power of two; one CTA per SM
+static_assert(kAColBase + kStages * kACols <= kTmemCols, "tensor memory plan");
 static_assert(kStageBytes % 1024 == 0, "swizzled xr tiles need 1024-byte alignment");
 
 struct TcParams {
     CUtensorMap amap, cmap, smap;
     void *y;
     uint64_t M, n;
-    uint32_t nk;
+    uint32_t nk, gn, tiles;     // K stages, weight tiles, tiles (weight tile fastest)
     int y_dtype;
     uint32_t *err;
 };
@@ -80,7 +85,7 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
 }
 
 // Instruction descriptor of kind::f16: fp32 D, binary16 A and B, both K-major,
-// M = 128 (weight rows), N = 128 (tokens).
+// M = 128 (weight rows), N = 192 (tokens).
 constexpr uint32_t kIdesc = (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(kBM >> 3) << 17) | ((uint32_t)(kBN >> 4) << 24);
 
 // D (tensor memory) += A (tensor memory, M x 16) * B (shared memory descriptor, 16 x N).
@@ -141,57 +146,80 @@ __device__ __forceinline__ uint32_t expand_pair(uint32_t w, int j, __half2 s2) {
 __global__ void __launch_bounds__(128) tc_prep_kernel(const void *__restrict__ x, int x_dtype,
                                                       const uint16_t *__restrict__ signs, __half *__restrict__ out,
                                                       uint64_t M, uint64_t K) {
+    // per warp: its 1024-block, element e at e + 8 (e >> 8) (padding keeps the
+    // transposed reads conflict-free)
+    __shared__ __align__(16) float tile_s[4][1024 + 32];
     const uint64_t nblk = K / 1024;
     const uint64_t task = (uint64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
     if (task >= M * nblk) return;
     const int lane = threadIdx.x & 31;
+    float *t = tile_s[threadIdx.x >> 5];
     const uint64_t m = task / nblk, b = task % nblk;
     const uint64_t row = m * K, col0 = b * 1024;
+    // lane l holds v[8 i + e] = element 256 i + 8 l + e: index bits 0-2 and 8-9 in registers
     float v[32];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        float t[8];
+        float tv[8];
         const uint64_t c = col0 + 256 * i + 8 * lane;
-        load8(x, row + c, x_dtype, t);
+        load8(x, row + c, x_dtype, tv);
         if (signs) {
             float d[8];
             load_signs8(signs, c, d);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) t[e] *= d[e];
+            for (int e = 0; e < 8; ++e) tv[e] *= d[e];
         }
 #pragma unroll
-        for (int e = 0; e < 8; ++e) v[8 * i + e] = t[e];
+        for (int e = 0; e < 8; ++e) v[8 * i + e] = tv[e];
     }
     if (signs) {
-        wht1024_warp(v, lane);
 #pragma unroll
-        for (int r = 0; r < 32; ++r) v[r] *= 0.03125f;
+        for (int bit = 0; bit < 5; ++bit)
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                if (j & (1 << bit)) continue;
+                const float a = v[j], c = v[j | (1 << bit)];
+                v[j] = a + c;
+                v[j | (1 << bit)] = a - c;
+            }
     }
-    // lane holds elements 8*lane + e of each 256-run: half h = lane & 1 of the
-    // 16-element run 16i + lane/2. Output order in the run: 0,8,1,9,...,7,15.
-    const int h = lane & 1;
+    // transpose through shared memory: lane l' = (i', e') = (l' >> 3, l' & 7)
+    // then holds w[r] = element 256 i' + 8 r + e', index bits 3-7 in registers
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        float send[4], other[4];
+        float4 *dst = reinterpret_cast<float4 *>(t + 264 * i + 8 * lane);
+        dst[0] = make_float4(v[8 * i], v[8 * i + 1], v[8 * i + 2], v[8 * i + 3]);
+        dst[1] = make_float4(v[8 * i + 4], v[8 * i + 5], v[8 * i + 6], v[8 * i + 7]);
+    }
+    __syncwarp();
+    const int ip = lane >> 3, ep = lane & 7;
+    float w[32];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) send[q] = h ? v[8 * i + q] : v[8 * i + 4 + q];
+    for (int r = 0; r < 32; ++r) w[r] = t[264 * ip + 8 * r + ep];
+    if (signs) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) other[q] = __shfl_xor_sync(0xffffffffu, send[q], 1);
-        uint32_t pk[4];
+        for (int bit = 0; bit < 5; ++bit)
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            // h = 0: (old q, old q + 8); h = 1: (old 4 + q, old 12 + q)
-            const float lo = h ? other[q] : v[8 * i + q];
-            const float hi = h ? v[8 * i + 4 + q] : other[q];
-            __half2 p2 = __floats2half2_rn(lo, hi);
-            pk[q] = *reinterpret_cast<uint32_t *>(&p2);
-        }
-        const uint64_t dst = row + col0 + 256 * i + 8 * lane;     // = run start + 8h
-        *reinterpret_cast<uint4 *>(out + dst) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            for (int j = 0; j < 32; ++j) {
+                if (j & (1 << bit)) continue;
+                const float a = w[j], c = w[j | (1 << bit)];
+                w[j] = a + c;
+                w[j | (1 << bit)] = a - c;
+            }
+#pragma unroll
+        for (int r = 0; r < 32; ++r) w[r] *= 0.03125f;
+    }
+    // output order inside every run of 16: 0,8,1,9,...,7,15. The pair at
+    // positions 2e', 2e' + 1 of run 16 s + 256 i' is (w[2 s], w[2 s + 1]).
+    uint32_t *o = reinterpret_cast<uint32_t *>(out + row + col0 + 256 * ip + 2 * ep);
+#pragma unroll
+    for (int s = 0; s < 16; ++s) {
+        __half2 p2 = __floats2half2_rn(w[2 * s], w[2 * s + 1]);
+        o[8 * s] = *reinterpret_cast<uint32_t *>(&p2);
     }
 }
 
-__global__ void __launch_bounds__(kThreads, 2) gemm_tc_kernel(const __grid_constant__ TcParams p) {
+__global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ TcParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t base = smem_u32(smem);
@@ -200,14 +228,15 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_tc_kernel(const __grid_const
         return;
     }
     const uint32_t bar = base + kStages * kStageBytes;
-    const uint32_t accum_bar = bar + 8 * 3 * kStages;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kStages * kStageBytes + kBarBytes);
-    const uint64_t n0 = (uint64_t)blockIdx.x * kBN, m0 = (uint64_t)blockIdx.y * kBM;
     // full_a[s]: xr, codes and scales landed; full_b[s]: weights expanded into the
-    // stage's A columns; empty[s]: stage consumed (shared memory and A columns)
+    // stage's A columns; empty[s]: stage consumed (shared memory and A columns);
+    // acc_full[b]: buffer b holds a finished tile; acc_empty[b]: buffer b read out
 #define FULL_A(s) (bar + 8 * (s))
 #define FULL_B(s) (bar + 8 * (kStages + (s)))
 #define EMPTY(s) (bar + 8 * (2 * kStages + (s)))
+#define ACC_FULL(b) (bar + 8 * (3 * kStages + (b)))
+#define ACC_EMPTY(b) (bar + 8 * (3 * kStages + 2 + (b)))
 
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
@@ -224,7 +253,10 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_tc_kernel(const __grid_const
             mbar_init(FULL_B(s), 4);
             mbar_init(EMPTY(s), 1);
         }
-        mbar_init(accum_bar, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(ACC_FULL(b), 1);
+            mbar_init(ACC_EMPTY(b), 4);
+        }
         fence_mbar_init();
     }
     tc_fence_before();
@@ -234,67 +266,100 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_tc_kernel(const __grid_const
 
     if (warp == 0) {
         if (lane == 0) {
-            for (uint32_t kt = 0; kt < p.nk; ++kt) {
-                const uint32_t s = kt % kStages, round = kt / kStages;
-                if (round > 0 && !mbar_wait(EMPTY(s), (round - 1) & 1, p.err)) break;
-                const uint32_t st = base + s * kStageBytes;
-                mbar_arrive_expect_tx(FULL_A(s), kXBytes + kCodeBytes + kScaleBytes);
-                tma_load_2d(st, &p.amap, (int)(kt * kBK), (int)m0, FULL_A(s));
-                tma_load_2d(st + kXBytes, &p.cmap, (int)(kt * 16), (int)n0, FULL_A(s));
-                tma_load_2d(st + kXBytes + kCodeBytes, &p.smap, (int)((kt / 16) * 16), (int)n0, FULL_A(s));
+            uint32_t g = 0;     // stage counter over all of this CTA's tiles
+            bool ok = true;
+            for (uint32_t tile = blockIdx.x; ok && tile < p.tiles; tile += gridDim.x) {
+                const int n0 = (int)((tile % p.gn) * kBN), m0 = (int)((tile / p.gn) * kBM);
+                for (uint32_t kt = 0; kt < p.nk; ++kt, ++g) {
+                    const uint32_t s = g % kStages, round = g / kStages;
+                    if (round > 0 && !mbar_wait(EMPTY(s), (round - 1) & 1, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t st = base + s * kStageBytes;
+                    mbar_arrive_expect_tx(FULL_A(s), kXBytes + kCodeBytes + kScaleBytes);
+                    tma_load_2d(st, &p.amap, (int)(kt * kBK), m0, FULL_A(s));
+                    tma_load_2d(st + kXBytes, &p.cmap, (int)(kt * 16), n0, FULL_A(s));
+                    tma_load_2d(st + kXBytes + kCodeBytes, &p.smap, (int)((kt / 16) * 16), n0, FULL_A(s));
+                }
             }
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            for (uint32_t kt = 0; kt < p.nk; ++kt) {
-                const uint32_t s = kt % kStages, par = (kt / kStages) & 1;
-                if (!mbar_wait(FULL_A(s), par, p.err) || !mbar_wait(FULL_B(s), par, p.err)) break;
+            uint32_t g = 0, j = 0;
+            bool ok = true;
+            for (uint32_t tile = blockIdx.x; ok && tile < p.tiles; tile += gridDim.x, ++j) {
+                const uint32_t b = j & 1;
+                // the buffer's previous tile (two tiles back) has been read out
+                if (j >= 2 && !mbar_wait(ACC_EMPTY(b), ((j >> 1) - 1) & 1, p.err)) break;
                 tc_fence_after();
-                const uint64_t bdesc = sw128_desc(base + s * kStageBytes);
-                const uint32_t acol = tmem + kAccCols + kACols * s;
+                const uint32_t dcol = tmem + b * kAccCols;
+                for (uint32_t kt = 0; kt < p.nk; ++kt, ++g) {
+                    const uint32_t s = g % kStages, par = (g / kStages) & 1;
+                    if (!mbar_wait(FULL_A(s), par, p.err) || !mbar_wait(FULL_B(s), par, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t bdesc = sw128_desc(base + s * kStageBytes);
+                    const uint32_t acol = tmem + kAColBase + kACols * s;
 #pragma unroll
-                for (int kk = 0; kk < kBK / 16; ++kk)      // A: +8 columns, B: +32 bytes (16-byte units: +2) per K=16
-                    mma_f16_tmem_a(tmem, acol + 8 * kk, bdesc + 2 * kk, (kt | kk) != 0);
-                mma_commit(EMPTY(s));
+                    for (int kk = 0; kk < kBK / 16; ++kk)      // A: +8 columns, B: +32 bytes (16-byte units: +2) per K=16
+                        mma_f16_tmem_a(dcol, acol + 8 * kk, bdesc + 2 * kk, (kt | kk) != 0);
+                    mma_commit(EMPTY(s));
+                }
+                if (ok) mma_commit(ACC_FULL(b));
             }
-            mma_commit(accum_bar);
         }
-    } else {
+    } else if (warp < 6) {
         // warp w may touch TMEM lanes 32 (w % 4) .. 32 (w % 4) + 31: its lane l is weight row 32 (w % 4) + l
         const uint32_t q = warp & 3;
         const uint32_t r = 32 * q + lane;
         const uint32_t lane_addr = tmem + ((32u * q) << 16);
-        for (uint32_t kt = 0; kt < p.nk; ++kt) {
-            const uint32_t s = kt % kStages, par = (kt / kStages) & 1;
-            // warp-uniform: the tensor-memory store below is a warp-wide instruction
-            if (!__all_sync(0xffffffffu, mbar_wait(FULL_A(s), par, p.err))) break;
-            const uint8_t *st = smem + s * kStageBytes;
-            const uint4 cw = *reinterpret_cast<const uint4 *>(st + kXBytes + r * 16);
-            const __half sc =
-                *reinterpret_cast<const __half *>(st + kXBytes + kCodeBytes + r * 16 + 2 * ((kt / 2) % 8));
-            const __half2 s2 = __halves2half2(sc, sc);
-            const uint32_t w[4] = {cw.x, cw.y, cw.z, cw.w};
-            // column 8 i + j holds the pair (code 16 i + j, code 16 i + j + 8): the
-            // K order 0,8,1,9,... of every run of 16, as xr is stored
-            uint32_t a[32];
+        uint32_t g = 0;
+        bool ok = true;
+        for (uint32_t tile = blockIdx.x; ok && tile < p.tiles; tile += gridDim.x) {
+            for (uint32_t kt = 0; kt < p.nk; ++kt, ++g) {
+                const uint32_t s = g % kStages, par = (g / kStages) & 1;
+                // warp-uniform: the tensor-memory store below is a warp-wide instruction
+                if (!__all_sync(0xffffffffu, mbar_wait(FULL_A(s), par, p.err))) {
+                    ok = false;
+                    break;
+                }
+                const uint8_t *st = smem + s * kStageBytes;
+                const uint4 cw = *reinterpret_cast<const uint4 *>(st + kXBytes + r * 16);
+                const __half sc =
+                    *reinterpret_cast<const __half *>(st + kXBytes + kCodeBytes + r * 16 + 2 * ((kt / 2) % 8));
+                const __half2 s2 = __halves2half2(sc, sc);
+                const uint32_t w[4] = {cw.x, cw.y, cw.z, cw.w};
+                // column 8 i + j holds the pair (code 16 i + j, code 16 i + j + 8): the
+                // K order 0,8,1,9,... of every run of 16, as xr is stored
+                uint32_t a[32];
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+                for (int i = 0; i < 4; ++i)
 #pragma unroll
-                for (int j = 0; j < 8; ++j) a[8 * i + j] = expand_pair(w[i], j, s2);
-            tmem_st32(lane_addr + kAccCols + kACols * s, a);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(FULL_B(s));
+                    for (int jj = 0; jj < 8; ++jj) a[8 * i + jj] = expand_pair(w[i], jj, s2);
+                tmem_st32(lane_addr + kAColBase + kACols * s, a);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(FULL_B(s));
+            }
         }
-        // epilogue: lane = weight row n0 + r, columns = the tile's tokens
-        const bool done = __all_sync(0xffffffffu, mbar_wait(accum_bar, 0, p.err));
-        tc_fence_after();
-        const uint64_t row = n0 + r;
-        if (done) {
+    } else {
+        // epilogue: lane = weight row n0 + r of the tile, columns = its tokens
+        const uint32_t q = warp & 3;
+        const uint32_t r = 32 * q + lane;
+        const uint32_t lane_addr = tmem + ((32u * q) << 16);
+        uint32_t j = 0;
+        for (uint32_t tile = blockIdx.x; tile < p.tiles; tile += gridDim.x, ++j) {
+            const uint32_t b = j & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(ACC_FULL(b), (j >> 1) & 1, p.err))) break;
+            tc_fence_after();
+            const uint64_t row = (uint64_t)(tile % p.gn) * kBN + r, m0 = (uint64_t)(tile / p.gn) * kBM;
 #pragma unroll 1
             for (int cb = 0; cb < kBM / 32; ++cb) {
                 float v[32];
-                tmem_ld32(lane_addr + 32 * cb, v);
+                tmem_ld32(lane_addr + b * kAccCols + 32 * cb, v);
                 const uint64_t mb = m0 + 32 * cb;
                 if (row >= p.n || mb >= p.M) continue;
                 const int cnt = p.M - mb < 32 ? (int)(p.M - mb) : 32;
@@ -309,11 +374,16 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_tc_kernel(const __grid_const
                         if (i < cnt) store1(p.y, (mb + i) * p.n + row, p.y_dtype, v[i]);
                 }
             }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(ACC_EMPTY(b));
         }
     }
 #undef FULL_A
 #undef FULL_B
 #undef EMPTY
+#undef ACC_FULL
+#undef ACC_EMPTY
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -324,17 +394,20 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_tc_kernel(const __grid_const
 
 }  // namespace
 
-bool gemm_tc_plan(const ninfer_row_split_geometry &g, uint64_t M, int smem_limit, TcPlan *plan) {
+bool gemm_tc_plan(const ninfer_row_split_geometry &g, uint64_t M, int sms, int smem_limit, TcPlan *plan) {
     *plan = TcPlan{};
     if (M < 9 || g.k % 1024 || g.k > (1u << 24)) return false;
     if (g.scale_row_bytes % 16 || g.base_row_bytes % 16) return false;
-    if ((int)kSmemBytes > smem_limit) return false;
+    if (120 * 1024 > smem_limit || (int)kSmemBytes > smem_limit) return false;
     const uint64_t gm = (M + kBM - 1) / kBM, gn = (g.n + kBN - 1) / kBN;
-    if (gm > 65535 || gn > 0x7fffffffull) return false;
+    if (sms < 1 || gm * gn > 0x7fffffffull || g.n > 0x7fffffffull || M > 0x7fffffffull) return false;
     plan->ok = true;
     plan->grid_n = (uint32_t)gn;
     plan->grid_m = (uint32_t)gm;
-    plan->smem = kSmemBytes;
+    plan->grid = (uint32_t)std::min<uint64_t>((uint64_t)sms, gm * gn);     // persistent: one CTA per SM
+    // more than half of an SM's shared memory, so that the persistent CTAs never share an SM
+    // (each holds all 512 tensor-memory columns)
+    plan->smem = std::max<uint32_t>(kSmemBytes, 120 * 1024);
     plan->workspace = M * g.k * 2;      // xr, binary16
     return true;
 }
@@ -354,6 +427,8 @@ int gemm_tc_launch(const TcPlan &plan, const uint8_t *payload, const ninfer_row_
     p.M = M;
     p.n = g.n;
     p.nk = (uint32_t)(g.k / kBK);
+    p.gn = plan.grid_n;
+    p.tiles = plan.grid_n * plan.grid_m;
     p.y_dtype = y_dtype;
     int st = device_error_word(&p.err);
     if (st) return st;
@@ -363,7 +438,7 @@ int gemm_tc_launch(const TcPlan &plan, const uint8_t *payload, const ninfer_row_
     if (st) return st;
     e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.smem);
     if (e != cudaSuccess) return fail(NINFER_ERR_CUDA, "prefill: smem attribute: %s", cudaGetErrorString(e));
-    gemm_tc_kernel<<<dim3(plan.grid_n, plan.grid_m), kThreads, plan.smem, stream>>>(p);
+    gemm_tc_kernel<<<plan.grid, kThreads, plan.smem, stream>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return fail(NINFER_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
     return NINFER_OK;

@@ -105,10 +105,10 @@ int ptq1_to_pq2_launch(const uint8_t *payload, const ninfer_row_split_geometry &
 // Prefill (M > 8) tensor-core path for PQ2_0_G128 (gemm_tc.cu).
 struct TcPlan {
     bool ok;
-    uint32_t grid_n, grid_m, smem;
+    uint32_t grid_n, grid_m, grid, smem;     // weight tiles, token tiles, persistent CTAs
     uint64_t workspace;
 };
-bool gemm_tc_plan(const ninfer_row_split_geometry &g, uint64_t M, int smem_limit, TcPlan *plan);
+bool gemm_tc_plan(const ninfer_row_split_geometry &g, uint64_t M, int sms, int smem_limit, TcPlan *plan);
 int gemm_tc_launch(const TcPlan &plan, const uint8_t *payload, const ninfer_row_split_geometry &g, const void *x,
                    int x_dtype, const uint16_t *signs, void *y, int y_dtype, uint64_t M, void *workspace,
                    cudaStream_t stream);

@@ -78,13 +78,13 @@ int plan_matmul(int fmt, const ninfer_row_split_geometry &g, uint64_t M, bool ro
         mp->workspace = mp->gpm.workspace;      // per-block partial sums
         return NINFER_OK;
     }
-    if (fmt == NINFER_PQ2_0_G128 && gemm_tc_plan(g, M, d.smem_optin, &mp->gtc)) {
+    if (fmt == NINFER_PQ2_0_G128 && gemm_tc_plan(g, M, d.sms, d.smem_optin, &mp->gtc)) {
         mp->path = Path::kTcPq2;
         mp->workspace = mp->gtc.workspace;     // xr as binary16
         return NINFER_OK;
     }
     if (fmt == NINFER_PTQ1_0_G128 && M > 8 && geometry(NINFER_PQ2_0_G128, g.n, g.k, &mp->q) == NINFER_OK &&
-        gemm_tc_plan(mp->q, M, d.smem_optin, &mp->gtc)) {
+        gemm_tc_plan(mp->q, M, d.sms, d.smem_optin, &mp->gtc)) {
         // prefill: the planes are rewritten as PQ2_0 planes in the workspace, then the
         // same tensor-core GEMM runs on them
         mp->path = Path::kTcPtq1;
