@@ -29,10 +29,11 @@
 //                   the 8 scales that cover them (16 bytes);
 //      warp 1       TMEM owner and MMA issuer (one thread): four K=16 MMAs per
 //                   stage into the tile's accumulator buffer;
-//      warps 2..5   decode: lane l of warp w expands weight row 32 (w % 4) + l
+//      warps 2..9   decode: lane l of warp w expands weight row 32 (w % 4) + l
 //                   (its tensor-memory lane) to binary16 (code - 1) * scale and
-//                   stores the stage's 32 binary16 pairs into the stage's A columns;
-//      warps 6..9   epilogue: read a finished accumulator buffer (lane = weight
+//                   stores 16 of the stage's 32 binary16 pairs into the stage's
+//                   A columns (warps 2..5 the first 16, warps 6..9 the rest);
+//      warps 10..13 epilogue: read a finished accumulator buffer (lane = weight
 //                   row, column = token), store y, hand the buffer back.
 //    Stages and buffers are handed over with mbarriers (TMA transaction counts,
 //    one arrival per decode or epilogue warp, and tcgen05.commit for "stage
@@ -60,7 +61,7 @@ constexpr uint32_t kScaleBytes = kBN * 16;         // 8 scales per weight row
 constexpr uint32_t kStageBytes = kXBytes + kCodeBytes + kScaleBytes;     // 28 KB, 1024-aligned
 constexpr uint32_t kBarBytes = 8 * (3 * kStages + 4);
 constexpr uint32_t kSmemBytes = ((kStages * kStageBytes + kBarBytes + 16 + 1023) / 1024) * 1024;
-constexpr int kThreads = 320;
+constexpr int kThreads = 448;
 constexpr uint32_t kAccCols = kBM;                 // one fp32 accumulator buffer: lane = weight row, column = token
 constexpr uint32_t kACols = kBK / 2;               // a stage's weights per row, as binary16 pairs
 constexpr uint32_t kAColBase = 2 * kAccCols;       // A stages after the two accumulator buffers
@@ -121,15 +122,13 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// 32 consecutive 32-bit columns of this warp's 32 TMEM lanes, from registers.
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+// 16 consecutive 32-bit columns of this warp's 32 TMEM lanes, from registers.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
     asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16};" ::"r"(taddr),
         "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
-        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
-        "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
-        "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
         : "memory");
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -250,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         prefetch_tmap(&p.smap);
         for (int s = 0; s < kStages; ++s) {
             mbar_init(FULL_A(s), 1);
-            mbar_init(FULL_B(s), 4);
+            mbar_init(FULL_B(s), 8);
             mbar_init(EMPTY(s), 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -311,9 +310,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 if (ok) mma_commit(ACC_FULL(b));
             }
         }
-    } else if (warp < 6) {
-        // warp w may touch TMEM lanes 32 (w % 4) .. 32 (w % 4) + 31: its lane l is weight row 32 (w % 4) + l
-        const uint32_t q = warp & 3;
+    } else if (warp < 10) {
+        // warp w may touch TMEM lanes 32 (w % 4) .. 32 (w % 4) + 31: its lane l is weight row 32 (w % 4) + l;
+        // warps 2..5 expand code words 0, 1 of every stage, warps 6..9 words 2, 3
+        const uint32_t q = warp & 3, hf = (warp - 2) >> 2;
         const uint32_t r = 32 * q + lane;
         const uint32_t lane_addr = tmem + ((32u * q) << 16);
         uint32_t g = 0;
@@ -331,15 +331,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 const __half sc =
                     *reinterpret_cast<const __half *>(st + kXBytes + kCodeBytes + r * 16 + 2 * ((kt / 2) % 8));
                 const __half2 s2 = __halves2half2(sc, sc);
-                const uint32_t w[4] = {cw.x, cw.y, cw.z, cw.w};
+                const uint32_t w[2] = {hf ? cw.z : cw.x, hf ? cw.w : cw.y};
                 // column 8 i + j holds the pair (code 16 i + j, code 16 i + j + 8): the
                 // K order 0,8,1,9,... of every run of 16, as xr is stored
-                uint32_t a[32];
+                uint32_t a[16];
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
+                for (int i = 0; i < 2; ++i)
 #pragma unroll
                     for (int jj = 0; jj < 8; ++jj) a[8 * i + jj] = expand_pair(w[i], jj, s2);
-                tmem_st32(lane_addr + kAColBase + kACols * s, a);
+                tmem_st16(lane_addr + kAColBase + kACols * s + 16 * hf, a);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(FULL_B(s));
