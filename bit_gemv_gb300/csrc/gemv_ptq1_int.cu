@@ -56,6 +56,12 @@ constexpr uint32_t kMaxSlots = 12;
 constexpr uint32_t kRotPairs = 8;
 constexpr uint32_t kMaxRem = 2;   // extra rows beyond whole row blocks handled per (row, group)
 constexpr uint32_t kActWords = 64; // per group: 24 base bytes x 2 words + 6 t4 quads x 2 words + 2 high bytes x 2 words
+// Groups sit kActStride words apart: the 4-word pad moves consecutive groups 16
+// bytes along the banks, so the remainder-row path (lanes = 16 groups) reads
+// its operand words with at most two-way conflicts; the row-block path reads
+// one group per warp (a broadcast) either way.
+constexpr uint32_t kActStride = 68;
+static_assert(kActStride >= kActWords && kActStride % 4 == 0, "operand words: 16-byte aligned groups");
 constexpr uint32_t kLutBytes = 256 * 128; // entry B at B * 128: 32 lane copies
 
 struct Ptq1Params {
@@ -138,7 +144,7 @@ __device__ __forceinline__ void pack_ptq1(const int16_t *qs, uint8_t *act_s, uin
         if (u >= 208) break;
         const uint32_t gl = u < 192 ? u / 24 : (u - 192) >> 1, G = b * 8 + gl;
         if (G >= groups) continue;
-        uint32_t *dst = act + (uint64_t)G * kActWords;
+        uint32_t *dst = act + (uint64_t)G * kActStride;
         if (u < 192) {
             const uint32_t j = u % 24;
             const int16_t *e = qs + 128 * gl + 5 * j;
@@ -160,7 +166,7 @@ __device__ __forceinline__ void pack_ptq1(const int16_t *qs, uint8_t *act_s, uin
     for (int sh = 4; sh > 0; sh >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, sh);
     const uint32_t G = b * 8 + (t >> 3);
     if ((t & 7) == 0 && G < groups)
-        reinterpret_cast<float2 *>(act_s + (uint64_t)groups * kActWords * 4)[G] =
+        reinterpret_cast<float2 *>(act_s + (uint64_t)groups * kActStride * 4)[G] =
             make_float2(ldexpf(1.f, -E), __int_as_float(sum));
     named_barrier(bar, 64);      // qs is read before the next block reuses the tile
 }
@@ -325,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ptq1_int_kernel(const __grid
     bool ok = true;
     if (p.act_g) ok = mbar_wait(act_bar, 0, p.err);
     const uint32_t *act_w = reinterpret_cast<const uint32_t *>(act_s);
-    const float2 *gs = reinterpret_cast<const float2 *>(act_s + (uint64_t)p.groups * kActWords * 4);
+    const float2 *gs = reinterpret_cast<const float2 *>(act_s + (uint64_t)p.groups * kActStride * 4);
     float *part = reinterpret_cast<float *>(smem + p.off_part);
     float *part_rem = part + kWarps * kRows;      // [kMaxRem][groups]
 
@@ -345,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ptq1_int_kernel(const __grid
                 const uint32_t hb = *reinterpret_cast<const uint16_t *>(row + p.base_row + 2 * G);
                 const float s = __half2float(*reinterpret_cast<const __half *>(row + p.base_row + p.high_row + 2 * G));
                 const float2 f = gs[G];
-                const int dot = group_dot(bw, hb, lut_s, lane4, reinterpret_cast<const uint4 *>(act_w + G * kActWords));
+                const int dot = group_dot(bw, hb, lut_s, lane4, reinterpret_cast<const uint4 *>(act_w + G * kActStride));
                 part_rem[rr * p.groups + G] = s * f.x * (float)(dot - __float_as_int(f.y));
             }
         }
@@ -376,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ptq1_int_kernel(const __grid
                 const float s =
                     __half2float(*reinterpret_cast<const __half *>(sa + 3 * kBaseBox + 32 * kRows + lane * 32 + 2 * warp));
                 const float2 f = gs[G];
-                const int dot = group_dot(bw, hb, lut_s, lane4, reinterpret_cast<const uint4 *>(act_w + G * kActWords));
+                const int dot = group_dot(bw, hb, lut_s, lane4, reinterpret_cast<const uint4 *>(act_w + G * kActStride));
                 y = fmaf(s * f.x, (float)(dot - __float_as_int(f.y)), y);
             }
             if (refill) {
@@ -446,7 +452,7 @@ bool gemv_ptq1_int_plan(const ninfer_row_split_geometry &g, uint64_t M, bool rot
     if (g.k > (1u << 24) || g.n > (1ull << 31)) return false;
     const uint32_t groups = (uint32_t)g.groups_per_row;
     const uint32_t nblk = (uint32_t)((g.k + 1023) / 1024);
-    const uint32_t act_bytes = ((groups * (kActWords * 4 + 8) + 15) / 16) * 16;
+    const uint32_t act_bytes = ((groups * (kActStride * 4 + 8) + 15) / 16) * 16;
     const bool split = nblk > kRotPairs;       // rotate in a separate kernel, once for the grid
     const uint32_t nrot = split ? 0 : std::min<uint32_t>(nblk, kRotPairs);
     const uint32_t rot_bytes = nrot * kRotScratch;
