@@ -84,6 +84,18 @@ def test_matmul_ptq1_block_split(n, k, M):
     assert oracle.max_rel_error(y, ref) <= TOL_DECODE
 
 
+@pytest.mark.parametrize("n,k,rotate", [(40, 16384, True), (300, 17408, True), (200, 32768, True),
+                                        (150, 34816, True), (90, 33700, False), (70, 20400, False)])
+def test_matmul_ptq1_m1_wide_k(n, k, rotate):
+    """PTQ1_0 at M = 1 with 16 to 34 1024-blocks (rotated, and raw with a
+    ragged last block): the activation is rotated once for the grid by the
+    prep kernel and bulk-copied into every CTA."""
+    c = synth.make_case("down", n=n, k=k, M=1, seed=n + k)
+    y = run_matmul("PTQ1_0_G128", c, rotate=rotate)
+    ref = oracle_matmul_rows("PTQ1_0_G128", c, np.arange(n), rotate=rotate)
+    assert oracle.max_rel_error(y, ref) <= TOL_DECODE
+
+
 @pytest.mark.slow
 def test_matmul_ptq1_ring_refill():
     """Row tiles longer than the shared-memory ring (more than six items of 128
