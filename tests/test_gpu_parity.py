@@ -201,6 +201,17 @@ def test_matmul_prefill_small(fmt, preset, n, k, M):
     assert oracle.max_rel_error(y, ref) <= TOL_PREFILL
 
 
+@pytest.mark.parametrize("fmt", ["PQ2_0_G128", "PTQ1_0_G128"])
+def test_matmul_prefill_multi_tile(fmt):
+    """60 x 8 output tiles (the last of each ragged) on one persistent CTA per
+    SM: every CTA walks three or four tiles, so both tensor-memory accumulator
+    buffers are reused and handed back by the epilogue. Every output compared."""
+    c = synth.make_case("prefill", n=7601, k=1024, M=1500, seed=7)
+    y = run_matmul(fmt, c)
+    ref = oracle_matmul_rows(fmt, c, np.arange(7601))
+    assert oracle.max_rel_error(y, ref) <= TOL_PREFILL
+
+
 def test_matmul_prefill_ptq1_invalid_trits():
     """Base bytes >= 243 and high bytes >= 81 are not produced by the packer;
     every decoder follows the digit definition (byte / 3^i) % 3 for them too, so
