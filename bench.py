@@ -412,7 +412,7 @@ def run_reference(args, rank: int, world: int):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(r["seconds_per_call"] * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": args.workload, "format": w.fmt, "n": w.n, "k": w.k, "M": w.M, "x_dtype": w.x_dtype,
-                   "seed": w.seed, "rotate": True},
+                   "seed": w.seed, "rotate": True, "projections": w.mats},
         "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
         "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
