@@ -8,7 +8,8 @@ pool of weight-payload copies whose total size is more than 3x the L2 cache.
 Steps are captured in CUDA graphs and timed with CUDA events on the launching
 stream.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload gateup|down|down_m8|head|head_m8|tiny]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload gateup|ffn_gate_up|down|down_m8|head|head_m8|
+                                                                  prefill|prefill_down|tiny]
   python bench.py --impl reference ...   (the fp64 CPU oracle on the host cores)
 
 Prints one JSON line (rank 0).
@@ -261,10 +262,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1)
         if world > 1:
-            t = torch.tensor([ms], device=dev, dtype=torch.float64)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            ms = float(t.item())
-            torch.distributed.barrier()
+            ms = max_over_ranks(ms, dev)
         return ms
 
     warm_replays = max(1, -(-args.warmup // per_graph))
@@ -278,7 +276,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     torch.cuda.synchronize()
     ms_step = ms_total / args.steps
     s_step = ms_step / 1e3
-    value = world * nbytes["weights"] / s_step / 1e9
+    value = job_value(nbytes["weights"], world, s_step)
     achieved = nbytes["total"] / s_step / 1e9
     peak, peak_kind = measured_peaks()
     e2e_s = ms_e2e / args.steps / 1e3
@@ -307,13 +305,31 @@ def run_ours(args, rank: int, world: int, local_rank: int):
                       "frac": round(achieved / peak, 4), "traffic": traffic,
                       "peak_source": f"{peak_kind} hbm_gbs (copy)", "frac_of_8000_nominal": round(achieved / 8000, 4)}
                      if M <= 8 else tensor_roofline(M, n, k, s_step, traffic)),
-        "e2e": {"value": round(world * nbytes["weights"] / e2e_s / 1e9, 2), "unit": "GB/s",
+        "e2e": {"value": round(job_value(nbytes["weights"], world, e2e_s), 2), "unit": "GB/s",
                 "h2d_bytes_per_step": int(x_host.numel() * x_host.element_size()),
                 "d2h_bytes_per_step": int(M * n * 4), "ms_per_step": round(ms_e2e / args.steps, 6)},
         "clocks": clock_info,
         "gpu_launches": args.steps * kernels_per_step(w),
     }
     return res
+
+
+def max_over_ranks(ms: float, device) -> float:
+    """The slowest rank's time: every rank contributes its own and gets the
+    maximum (a collective on the process group; then a barrier)."""
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([ms], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.barrier()
+    return float(t.item())
+
+
+def job_value(weight_bytes_per_rank: int, world: int, s_step: float) -> float:
+    """Whole-job weight GB/s: every rank streams its own replica's weights once
+    per step, so the job moves world times the per-rank bytes in s_step."""
+    return world * weight_bytes_per_rank / s_step / 1e9
 
 
 def path_dtype(w) -> str:
