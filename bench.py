@@ -40,9 +40,15 @@ FALLBACK_HBM_GBS = 6800.0
 
 
 def algorithmic_bytes(w, M: int) -> dict:
-    """Bytes the method must move per call: packed planes + activations + signs + fp32 output."""
+    """Bytes the method must move per call: packed planes + activations + signs + fp32 output.
+    The embedding moves the gathered rows' planes, the ids, the signs and the fp32 rows."""
     groups = -(-w.k // 128)
     per_group = 34 if w.fmt == "PQ2_0_G128" else 28
+    if w.kind == "embed":
+        cnt = synth.EMBED_COUNT
+        weights = cnt * groups * per_group
+        return {"weights": weights, "x": cnt * 4, "signs": w.k * 2, "y": cnt * w.k * 4,
+                "total": weights + cnt * 4 + w.k * 2 + cnt * w.k * 4}
     weights = w.mats * w.n * groups * per_group
     xb = M * w.k * (4 if w.x_dtype == "f32" else 2)
     sb = w.mats * w.k * 2
@@ -90,6 +96,8 @@ KERNEL_TAG = "gemv"
 
 def dominant_kernel(w):
     """(profile tag, source files) of the kernel that dominates one step of workload w."""
+    if w.kind == "embed":
+        return "embed", ["bit_gemv_gb300/csrc/embed.cu"] + _COMMON
     if w.mats == 2 and w.fmt == "PQ2_0_G128" and w.M == 1:
         return KERNEL_TAG, GEMV_SOURCES + ["bit_gemv_gb300/csrc/ffn.cu"]
     if w.fmt == "PQ2_0_G128" and w.M == 1:
@@ -179,7 +187,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     w = synth.WORKLOADS[args.workload]
-    c = synth.make_case(w)
+    embed = w.kind == "embed"
+    c = synth.make_case(w, with_ids=embed)
     n, k, M = w.n, w.k, w.M
     nbytes = algorithmic_bytes(w, M)
     payload_host = nt.ninfer_ternary_pack(w.fmt, c.values, c.scales)
@@ -197,7 +206,8 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     else:
         x_host = torch.from_numpy(c.x)
     x = x_host.to(dev)
-    y = torch.empty((M, n), dtype=torch.float32, device=dev)
+    y = torch.empty((synth.EMBED_COUNT, k) if embed else (M, n), dtype=torch.float32, device=dev)
+    ids = torch.from_numpy(c.ids).to(dev) if embed else None
     if w.mats == 2:
         ws_bytes = nt.ninfer_ternary_gate_up_workspace(w.fmt, n, k, M, True, True)
     else:
@@ -206,18 +216,22 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     stream = torch.cuda.Stream(dev)
 
     def step(i):
-        if w.mats == 2:
+        if embed:
+            nt.ninfer_ternary_embed(w.fmt, payloads[i % pool], n, k, ids, signs, out=y)
+        elif w.mats == 2:
             nt.ninfer_ternary_gate_up(w.fmt, payloads[i % pool], payloads_up[i % pool], n, k, x, signs, signs_up, y=y,
                                       workspace=ws)
         else:
             nt.ninfer_ternary_matmul(w.fmt, payloads[i % pool], n, k, x, signs, y=y, workspace=ws)
 
-    # e2e buffers: pinned host activations in, pinned host result out
-    x_pin = [x_host.clone().pin_memory() for _ in range(pool)]
-    y_pin = [torch.empty((M, n), dtype=torch.float32).pin_memory() for _ in range(pool)]
+    # e2e buffers: pinned host inputs (activations, or token ids) in, pinned host result out
+    in_dev = ids if embed else x
+    in_host = torch.from_numpy(c.ids) if embed else x_host
+    x_pin = [in_host.clone().pin_memory() for _ in range(pool)]
+    y_pin = [torch.empty(tuple(y.shape), dtype=torch.float32).pin_memory() for _ in range(pool)]
 
     def step_e2e(i):
-        x.copy_(x_pin[i % pool], non_blocking=True)
+        in_dev.copy_(x_pin[i % pool], non_blocking=True)
         step(i)
         y_pin[i % pool].copy_(y, non_blocking=True)
 
@@ -297,17 +311,18 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         "data": "synthetic",
         "config": {"workload": args.workload, "format": w.fmt, "n": n, "k": k, "M": M, "x_dtype": w.x_dtype,
                    "seed": w.seed, "rotate": True, "projections": w.mats,
+                   **({"rows_gathered": synth.EMBED_COUNT} if embed else {}),
                    "l2": f"rotating pool of {pool} payload copies ({pool * w.mats * payload_host.size / 1e6:.0f} MB > 3x L2 "
                          f"{l2 / 1e6:.0f} MB)",
                    "parallelism": f"replicas x{world}"},
-        "tokens_per_s": round(world * M / s_step, 1),
+        "tokens_per_s": round(world * (synth.EMBED_COUNT if embed else M) / s_step, 1),
         "roofline": ({"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                       "frac": round(achieved / peak, 4), "traffic": traffic,
                       "peak_source": f"{peak_kind} hbm_gbs (copy)", "frac_of_8000_nominal": round(achieved / 8000, 4)}
                      if M <= 8 else tensor_roofline(M, n, k, s_step, traffic)),
         "e2e": {"value": round(job_value(nbytes["weights"], world, e2e_s), 2), "unit": "GB/s",
-                "h2d_bytes_per_step": int(x_host.numel() * x_host.element_size()),
-                "d2h_bytes_per_step": int(M * n * 4), "ms_per_step": round(ms_e2e / args.steps, 6)},
+                "h2d_bytes_per_step": int(in_host.numel() * in_host.element_size()),
+                "d2h_bytes_per_step": int(y.numel() * 4), "ms_per_step": round(ms_e2e / args.steps, 6)},
         "clocks": clock_info,
         "gpu_launches": args.steps * kernels_per_step(w),
     }
@@ -334,6 +349,8 @@ def job_value(weight_bytes_per_rank: int, world: int, s_step: float) -> float:
 
 def path_dtype(w) -> str:
     """Arithmetic type of the path that serves workload w."""
+    if w.kind == "embed":
+        return "f32"     # dequantised weights and the inverse transform in fp32
     if w.M == 1:
         return "int16*ternary->int32->f32"
     return "f16*f16->f32"
@@ -353,7 +370,9 @@ def kernels_per_step(w) -> int:
     M <= 8 kernel rotates x itself and, with more than one 1024-block, is
     followed by the block reduction; the PQ2_0 M <= 8, prefill and general
     paths run a prep or transform kernel and then the main one. The fused
-    gate/up pair at PQ2_0, M = 1 is one kernel."""
+    gate/up pair at PQ2_0, M = 1 is one kernel, and so is the embedding."""
+    if w.kind == "embed":
+        return 1
     if w.mats == 2 and w.fmt == "PQ2_0_G128" and w.M == 1:
         return 1
     if w.mats == 2:
@@ -373,6 +392,16 @@ def cpu_oracle_sample(workload: str, rows: int, reps: int) -> dict:
     import oracle
 
     w = synth.WORKLOADS[workload]
+    if w.kind == "embed":
+        # the same work per call: EMBED_COUNT rows gathered from a `rows`-row slice
+        c = synth.make_case(w, n=rows, with_ids=True)
+        payload = oracle.pack_planes(w.fmt, c.values, c.scales)
+        D = synth.bf16_bits_to_f32(c.signs)
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            oracle.embed_rows(w.fmt, payload, rows, w.k, c.ids, D)
+        dt = (time.perf_counter() - t0) / reps
+        return {"seconds_per_call": dt, "weight_bytes": algorithmic_bytes(w, 1)["weights"], "rows": rows}
     c = synth.make_case(w, n=rows)
     payload = oracle.pack_planes(w.fmt, c.values, c.scales)
     D = synth.bf16_bits_to_f32(c.signs)
@@ -405,6 +434,11 @@ def cpu_baseline(workload: str) -> dict:
     rows = min(w.n, 17408)
     r = run_cpu_child(workload, rows, 2)
     gbs = r["weight_bytes"] / r["seconds_per_call"] / 1e9
+    if w.kind == "embed":
+        return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                "sample": f"{synth.EMBED_COUNT} rows gathered from a {rows}-row slice of the {workload} matrix "
+                          f"(the same work per call), 2 calls, fp64 numpy, 1 thread",
+                "seconds_per_call": round(r["seconds_per_call"], 4)}
     return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"{rows} of {w.n} rows of the {workload} workload, 2 calls, fp64 numpy, 1 thread",
             "seconds_per_call": round(r["seconds_per_call"], 4),

@@ -109,6 +109,7 @@ class Workload:
     rotate: bool = True
     description: str = ""
     mats: int = 1            # 2: FFN gate and up projections of one activation (SwiGLU product)
+    kind: str = "matmul"     # "embed": gather EMBED_COUNT rows and inverse-rotate them
 
 
 WORKLOADS = {
@@ -127,6 +128,10 @@ WORKLOADS = {
     "ffn_gate_up": Workload("ffn_gate_up", "PQ2_0_G128", 17408, 5120, 1, "bf16", 6,
                             description="FFN gate and up projections, PQ2_0_G128 17408x5120 each with its own "
                                         "sign vector, SwiGLU product, M=1", mats=2),
+    "embed": Workload("embed", "PQ2_0_G128", 248320, 5120, 1, "bf16", 4,
+                      description="embedding: 64 token ids uniform in [0, 248320) gathered from the PQ2_0_G128 "
+                                  "head matrix 248320x5120, dequantised, inverse transform D*(H*e)/32",
+                      kind="embed"),
     "head": Workload("head", "PQ2_0_G128", 248320, 5120, 1, "bf16", 4,
                      description="output head, PQ2_0_G128 n=248320 k=5120, M=1"),
     "head_m8": Workload("head_m8", "PQ2_0_G128", 248320, 5120, 8, "bf16", 4,
