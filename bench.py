@@ -420,8 +420,9 @@ def cpu_oracle_sample(workload: str, rows: int, reps: int) -> dict:
     return {"seconds_per_call": dt, "weight_bytes": wbytes, "rows": rows}
 
 
-def run_cpu_child(workload: str, rows: int, reps: int) -> dict:
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+def run_cpu_child(workload: str, rows: int, reps: int, threads: int = 1) -> dict:
+    env = dict(os.environ, OMP_NUM_THREADS=str(threads), OPENBLAS_NUM_THREADS=str(threads),
+               MKL_NUM_THREADS=str(threads))
     out = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-child", workload, str(rows), str(reps)],
                          capture_output=True, text=True, env=env, timeout=900)
     if out.returncode != 0:
@@ -430,17 +431,29 @@ def run_cpu_child(workload: str, rows: int, reps: int) -> dict:
 
 
 def cpu_baseline(workload: str) -> dict:
+    res = _cpu_baseline_one(workload, 1)
+    cores = os.cpu_count() or 1
+    if cores > 1:
+        # the same sample with the host's BLAS on every core (the dense transform
+        # and contraction of the oracle are BLAS calls; its plane decode is not)
+        allc = _cpu_baseline_one(workload, cores)
+        res["all_cores"] = {"value": allc["value"], "unit": allc["unit"], "cores": cores,
+                            "seconds_per_call": allc["seconds_per_call"]}
+    return res
+
+
+def _cpu_baseline_one(workload: str, threads: int) -> dict:
     w = synth.WORKLOADS[workload]
     rows = min(w.n, 17408)
-    r = run_cpu_child(workload, rows, 2)
+    r = run_cpu_child(workload, rows, 2, threads)
     gbs = r["weight_bytes"] / r["seconds_per_call"] / 1e9
     if w.kind == "embed":
-        return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+        return {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
                 "sample": f"{synth.EMBED_COUNT} rows gathered from a {rows}-row slice of the {workload} matrix "
-                          f"(the same work per call), 2 calls, fp64 numpy, 1 thread",
+                          f"(the same work per call), 2 calls, fp64 numpy, {threads} thread(s)",
                 "seconds_per_call": round(r["seconds_per_call"], 4)}
-    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{rows} of {w.n} rows of the {workload} workload, 2 calls, fp64 numpy, 1 thread",
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{rows} of {w.n} rows of the {workload} workload, 2 calls, fp64 numpy, {threads} thread(s)",
             "seconds_per_call": round(r["seconds_per_call"], 4),
             "tokens_per_s_full_matrix": round(w.M / (r["seconds_per_call"] * w.n / rows), 4)}
 
