@@ -261,6 +261,10 @@ int ninfer_ternary_matmul(int fmt, const uint8_t *payload, uint64_t payload_byte
  *     other cases keep fp32 g and u in the workspace.
  * Errors: as ninfer_ternary_matmul; INVALID_ARGUMENT when exactly one sign
  *   vector is given.
+ * ninfer_ternary_gate_up_workspace: the workspace bytes of a call with these
+ *   fmt, n, k, M, with rotate != 0 when sign vectors are given and
+ *   distinct_signs != 0 when they are two different pointers (0 when the
+ *   single-kernel path applies). Errors: as ninfer_ternary_geometry, SHAPE for M = 0.
  */
 int ninfer_ternary_gate_up_workspace(int fmt, uint64_t n, uint64_t k, uint64_t M,
                                      int rotate, int distinct_signs, uint64_t *bytes);
