@@ -140,3 +140,31 @@ def test_device_entry_points_validate_before_launch():
     assert msg and b"dtype" in msg
     ws = u64()
     assert lib.ninfer_ternary_matmul_workspace(142, 256, 1024, 0, 1, ctypes.byref(ws)) == 3
+
+
+def test_gate_up_and_block_conversion_validate_before_launch():
+    """The fused gate/up and the device block conversion check their arguments
+    before any device work, so these run without a GPU (fake aligned addresses)."""
+    lib = nt._lib
+    fake = ctypes.c_void_p(1 << 20)
+    g = nt.ninfer_ternary_geometry("PQ2_0_G128", 256, 1024)
+    pb = g.payload_bytes
+
+    def gate_up(fmt=142, pg=fake, pu=fake, nbytes=pb, n=256, k=1024, sg=fake, su=fake, y_dtype=0, M=1):
+        return lib.ninfer_ternary_gate_up(fmt, pg, pu, nbytes, n, k, fake, 0, sg, su, fake, y_dtype, M, None, 0,
+                                          None)
+
+    assert gate_up(su=None) == 1                                      # one sign vector without the other
+    assert gate_up(y_dtype=2) == 1                                    # f16 output is not offered
+    assert gate_up(nbytes=pb - 2) == 4                                # payload size
+    assert gate_up(pu=ctypes.c_void_p((1 << 20) + 16)) == 5           # up payload not 256-byte aligned
+    assert gate_up(M=0) == 3
+    g2 = nt.ninfer_ternary_geometry("PQ2_0_G128", 256, 1000)
+    assert gate_up(nbytes=g2.payload_bytes, k=1000) == 3             # rotated input needs whole blocks
+    assert gate_up(fmt=9) == 2
+    # device block stream <-> planes: sizes and alignment
+    blocks = 256 * g.groups_per_row * 34
+    assert lib.ninfer_blocks_to_planes_device(142, 256, 1024, fake, blocks - 34, fake, pb, None) == 4
+    assert lib.ninfer_blocks_to_planes_device(142, 256, 1024, fake, blocks, fake, pb + 1, None) == 4
+    assert lib.ninfer_planes_to_blocks_device(142, 256, 1024, ctypes.c_void_p((1 << 20) + 8), pb, fake, blocks,
+                                              None) == 5
