@@ -58,6 +58,7 @@ _sig = {
     "ninfer_planes_to_blocks": (_int, [_int, _u64, _u64, _vp, _u64, _vp, _u64]),
     "ninfer_blocks_to_planes_device": (_int, [_int, _u64, _u64, _vp, _u64, _vp, _u64, _vp]),
     "ninfer_planes_to_blocks_device": (_int, [_int, _u64, _u64, _vp, _u64, _vp, _u64, _vp]),
+    "ninfer_validate_signs": (_int, [_vp, _u64]),
     "ninfer_hadamard_fwd": (_int, [_vp, _int, _vp, _int, _vp, _u64, _u64, _vp]),
     "ninfer_hadamard_inv": (_int, [_vp, _int, _vp, _int, _vp, _u64, _u64, _vp]),
     "ninfer_ternary_matmul_workspace": (_int, [_int, _u64, _u64, _u64, _int, C.POINTER(_u64)]),
@@ -194,6 +195,13 @@ def _dev(t, name):
     if not t.is_cuda or not t.is_contiguous():
         raise ValueError(f"{name} must be a contiguous CUDA tensor")
     return C.c_void_p(t.data_ptr())
+
+
+def ninfer_validate_signs(signs) -> None:
+    """Raise NinferError unless signs (host uint16/int16 bfloat16 bits, length K,
+    K % 1024 == 0) holds only +1 and -1."""
+    a = np.ascontiguousarray(np.asarray(signs).view(np.uint16).reshape(-1))
+    _check(_lib.ninfer_validate_signs(a.ctypes.data_as(C.c_void_p), a.size))
 
 
 def ninfer_hadamard_fwd(x, signs, out=None, out_dtype=None):

@@ -321,3 +321,15 @@ int ninfer_planes_to_blocks(int fmt, uint64_t n, uint64_t k, const uint8_t *payl
 }
 
 }  // extern "C"
+
+extern "C" int ninfer_validate_signs(const uint16_t *signs_bf16, uint64_t K) {
+    using namespace ninfer;
+    if (!signs_bf16) return fail(NINFER_ERR_INVALID_ARGUMENT, "validate signs: NULL vector");
+    if (K == 0 || K % 1024)
+        return fail(NINFER_ERR_SHAPE, "validate signs: K=%llu is not a positive multiple of 1024", (unsigned long long)K);
+    for (uint64_t i = 0; i < K; ++i)
+        if (signs_bf16[i] != 0x3F80u && signs_bf16[i] != 0xBF80u)
+            return fail(NINFER_ERR_INVALID_ARGUMENT, "validate signs: entry %llu is 0x%04x, not +1 (0x3F80) or -1 (0xBF80)",
+                        (unsigned long long)i, (unsigned)signs_bf16[i]);
+    return NINFER_OK;
+}

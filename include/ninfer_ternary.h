@@ -193,6 +193,17 @@ int ninfer_planes_to_blocks_device(int fmt, uint64_t n, uint64_t k, const uint8_
  *   Computed in fp32; y rounded to y_dtype.
  * Errors: INVALID_ARGUMENT, SHAPE (K % 1024 != 0), ALIGNMENT, CUDA.
  */
+/*
+ * ninfer_validate_signs -- load-time check of a hadamard_signs vector ([V3] §8:
+ *   bfloat16 [K], K a multiple of 1024, every entry +1 or -1). The device
+ *   entry points do not check sign values; validate a vector once with this
+ *   when it is loaded.
+ *   signs_bf16: host bfloat16[K] (bit patterns 0x3F80 = +1, 0xBF80 = -1).
+ * Errors: INVALID_ARGUMENT (NULL, or an entry other than +-1, named in the
+ *   message), SHAPE (K == 0 or K % 1024 != 0).
+ */
+int ninfer_validate_signs(const uint16_t *signs_bf16, uint64_t K);
+
 int ninfer_hadamard_fwd(const void *x, int x_dtype, void *y, int y_dtype,
                         const uint16_t *signs_bf16, uint64_t M, uint64_t K,
                         ninfer_stream stream);

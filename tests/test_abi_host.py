@@ -168,3 +168,21 @@ def test_gate_up_and_block_conversion_validate_before_launch():
     assert lib.ninfer_blocks_to_planes_device(142, 256, 1024, fake, blocks, fake, pb + 1, None) == 4
     assert lib.ninfer_planes_to_blocks_device(142, 256, 1024, ctypes.c_void_p((1 << 20) + 8), pb, fake, blocks,
                                               None) == 5
+
+
+def test_validate_signs():
+    """Load-time check of a sign vector: exactly +-1 in bfloat16, K % 1024 == 0."""
+    import synth
+
+    rng = np.random.default_rng(3)
+    s = synth.sign_vector(rng, 2048)
+    nt.ninfer_validate_signs(s)                            # valid
+    bad = s.copy()
+    bad[1500] = 0x3F00                                     # 0.5
+    with pytest.raises(nt.NinferError, match="entry 1500"):
+        nt.ninfer_validate_signs(bad)
+    bad[1500] = 0x0000                                     # +0
+    with pytest.raises(nt.NinferError):
+        nt.ninfer_validate_signs(bad)
+    with pytest.raises(nt.NinferError, match="multiple of 1024"):
+        nt.ninfer_validate_signs(s[:1000])
