@@ -96,6 +96,16 @@ def test_matmul_ptq1_m1_wide_k(n, k, rotate):
     assert oracle.max_rel_error(y, ref) <= TOL_DECODE
 
 
+@pytest.mark.parametrize("n,k,rotate", [(300, 16384, True), (130, 20480, True), (90, 20400, False)])
+def test_matmul_pq2_m1_wide_k(n, k, rotate):
+    """PQ2_0 at M = 1 with more than eight 1024-blocks: one warp rotates each
+    block (one round up to sixteen blocks, then a second)."""
+    c = synth.make_case("gateup", n=n, k=k, M=1, seed=n + k)
+    y = run_matmul("PQ2_0_G128", c, rotate=rotate)
+    ref = oracle_matmul_rows("PQ2_0_G128", c, np.arange(n), rotate=rotate)
+    assert oracle.max_rel_error(y, ref) <= TOL_DECODE
+
+
 @pytest.mark.slow
 def test_matmul_ptq1_ring_refill():
     """Row tiles longer than the shared-memory ring (more than six items of 128
