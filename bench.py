@@ -375,8 +375,9 @@ def kernels_per_step(w) -> int:
         return 1
     if w.mats == 2 and w.fmt == "PQ2_0_G128" and w.M == 1:
         return 1
-    if w.mats == 2:
-        return 2 * kernels_per_step(synth.WORKLOADS["gateup"] if w.fmt == "PQ2_0_G128" else w) + 1
+    if w.mats == 2:      # two projections, then the SwiGLU kernel
+        import dataclasses
+        return 2 * kernels_per_step(dataclasses.replace(w, mats=1)) + 1
     if w.M == 1:
         return 2 if (w.fmt == "PTQ1_0_G128" and w.k > 8192) else 1
     if w.fmt == "PTQ1_0_G128" and w.M <= 8:
