@@ -416,4 +416,31 @@ def pin_gate_up_limits():
     assert np.allclose(y, -32.0, rtol=1e-7)                # silu(32) * (-1)
 
 
+def pin_ptq1_0_every_byte_value():
+    """Every byte value 0..255 of a base and of a high byte decodes to its low
+    five (base) or four (high) base-3 digits minus one, the reading that also
+    covers bytes the packer never writes. The digits come from numpy's own
+    radix conversion (np.base_repr), independent of the oracle's arithmetic."""
+    n = 256
+    g = oracle.row_split_geometry("PTQ1_0_G128", n, 128)
+    payload = np.zeros(g.payload_bytes, np.uint8)
+    base = np.full((n, 24), 121, np.uint8)                # 121 = digits 1,1,1,1,1: value 0
+    base[:, 7] = np.arange(n)                              # weights 35 .. 39
+    high = np.full((n, 2), 40, np.uint8)                   # 40 = digits 1,1,1,1
+    high[:, 1] = np.arange(n)                              # weights 124 .. 127
+    payload[:g.base_bytes] = base.reshape(-1)
+    payload[g.high_offset:g.high_offset + g.high_bytes] = high.reshape(-1)
+    payload[g.scale_offset:] = np.tile(np.array([0, 0x3C], np.uint8), n)     # scale 1.0
+    W = oracle.dequantize("PTQ1_0_G128", payload, n, 128)
+
+    def digits(B, count):
+        r = np.base_repr(int(B), base=3)[::-1] + "0" * 8
+        return [int(ch) for ch in r[:count]]
+
+    for B in range(n):
+        assert list(W[B, 35:40]) == [d - 1 for d in digits(B, 5)], B
+        assert list(W[B, 124:128]) == [d - 1 for d in digits(B, 4)], B
+        assert np.all(W[B, :35] == 0) and np.all(W[B, 40:124] == 0)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

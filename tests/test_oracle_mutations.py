@@ -193,6 +193,28 @@ def m_swiglu_one_sign_vector(mp):
     _patch(mp, "gate_up_swiglu", f)
 
 
+def m_ptq1_invalid_bytes_to_zero(mp):
+    # bytes the packer never writes (>= 243 base, >= 81 high) read as all-zero values
+    orig = _orig("_decode_ptq1")
+    def dec(base_g, high_g):
+        v = orig(base_g, high_g)
+        lead = base_g.shape[:-1]
+        bad_lo = np.repeat(base_g >= 243, 5, axis=-1).reshape(lead + (120,))
+        bad_hi = np.repeat(high_g >= 81, 4, axis=-1).reshape(lead + (8,))
+        return np.where(np.concatenate([bad_lo, bad_hi], -1), 0, v)
+    _patch(mp, "_decode_ptq1", dec)
+
+
+def m_ptq1_fifth_digit_dropped(mp):
+    # t4 of every base byte read as 0 (value -1): a four-digit reading of five
+    orig = _orig("_decode_ptq1")
+    def dec(base_g, high_g):
+        v = orig(base_g, high_g).copy()
+        v[..., 4:120:5] = -1
+        return v
+    _patch(mp, "_decode_ptq1", dec)
+
+
 MUTATIONS = [v for k, v in sorted(globals().items()) if k.startswith("m_")]
 
 
