@@ -156,6 +156,13 @@ def m_blocks_scale_after(mp):
     mp.setattr(T, "BLOCK_PLANE_SLICES", monkeypatch_slices)
 
 
+def m_blocks_ptq1_high_first(mp):
+    # PTQ1_0 block read as [high 2][base 24][scale 2] instead of [base 24][high 2][scale 2]
+    monkeypatch_slices = dict(T.BLOCK_PLANE_SLICES)
+    monkeypatch_slices["PTQ1_0_G128"] = ((2, 26), (0, 2), (26, 28))
+    mp.setattr(T, "BLOCK_PLANE_SLICES", monkeypatch_slices)
+
+
 def m_pack_pad_minus_one(mp):
     orig = _orig("pack_planes")
     def pk(fmt, values, scales):
