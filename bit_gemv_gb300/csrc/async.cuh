@@ -1,6 +1,6 @@
-// Inline-PTX wrappers for mbarriers, 1-D bulk async copies (TMA engine),
-// programmatic dependent launch and fp8 tensor-core MMA on sm_103a, plus the
-// library's device error word. Every wait is bounded: a wait that runs out
+// Inline-PTX wrappers for mbarriers, bulk and tensor-map async copies (TMA
+// engine), programmatic dependent launch and shared-memory loads on sm_103a,
+// plus the bits of the library's device error word. Every wait is bounded: a wait that runs out
 // records an error code and returns false instead of spinning forever.
 #pragma once
 
@@ -94,17 +94,6 @@ __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepc
 
 __device__ __forceinline__ void named_barrier(uint32_t id, uint32_t threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
-
-// D = A (16x32 e4m3, row) * B (32x8 e4m3, col) + C, fp32 accumulate.
-__device__ __forceinline__ void mma_e4m3(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1,
-                                         const float (&c)[4]) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%10,%11,%12,%13};"
-        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]),
-          "f"(c[3]));
 }
 
 __device__ __forceinline__ uint2 lds64(uint32_t addr) {

@@ -1,6 +1,7 @@
 // Pieces shared by the fused decode kernels: the library's device error word
 // and tensor-map encoding for row-range views of a plane.
 #include <cstring>
+#include <mutex>
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -15,9 +16,11 @@ __device__ uint32_t g_device_error = 0;
 
 int device_error_word(uint32_t **out) {
     static uint32_t *cache[64];
+    static std::mutex mu;     // first calls from several host threads
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return fail(NINFER_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    std::lock_guard<std::mutex> lock(mu);
     if (dev >= 0 && dev < 64 && cache[dev]) {
         *out = cache[dev];
         return NINFER_OK;
@@ -37,6 +40,8 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_
 
 int encode_fn(EncodeTiledFn *out) {
     static EncodeTiledFn fn = nullptr;
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lock(mu);
     if (!fn) {
         void *ptr = nullptr;
         cudaDriverEntryPointQueryResult q;

@@ -1,4 +1,6 @@
 // ninfer_ternary_matmul: argument checks, workspace sizing and dispatch.
+#include <mutex>
+
 #include <cuda_runtime.h>
 
 #include "common.h"
@@ -13,9 +15,11 @@ int gemm_simple_launch(const PlaneView &p, uint64_t n, uint64_t k, const void *a
 int device_info(DeviceInfo *out) {
     static DeviceInfo cache[64];
     static bool have[64];
+    static std::mutex mu;     // first calls from several host threads
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return fail(NINFER_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    std::lock_guard<std::mutex> lock(mu);
     if (dev >= 0 && dev < 64 && have[dev]) {
         *out = cache[dev];
         return NINFER_OK;

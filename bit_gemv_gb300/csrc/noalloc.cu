@@ -13,7 +13,11 @@
 // Host code must not hand the array's name to a kernel: on the host that name
 // is only a stand-in symbol. Its device address is obtained once per device
 // with cudaGetSymbolAddress (on the first call made with that device current)
-// and cached.
+// and cached for the life of the process, so calls must not cross a
+// cudaDeviceReset (or any other teardown of the device's primary context): the
+// library is loaded again into the new context and the cached address would
+// be stale. The first call on a device should also come before any stream
+// capture, since it does this set-up.
 #include <mutex>
 
 #include <cuda_runtime.h>
@@ -70,8 +74,12 @@ extern "C" int ninfer_ternary_matmul_noalloc(int fmt, const uint8_t *payload, ui
     void *scratch = nullptr;
     st = scratch_address(&scratch);
     if (st) return st;
-    // The scratch only ever holds data a call writes in full before reading it
-    // (the rotated activations), so nothing has to be cleared between calls.
+    // Nothing is cleared between calls: every path writes each workspace byte
+    // it later reads, within the same call, before reading it. The users are
+    // the rotated or packed activations (all paths that stage them), the
+    // binary16 MMA fragments (PQ2_0, 2 <= M <= 8), the per-block fp32 partial
+    // sums (PTQ1_0, 2 <= M <= 8; padded rows that no block writes are never
+    // read back) and the PTQ1_0 planes rewritten as PQ2_0 planes (prefill).
     return ninfer_ternary_matmul(fmt, payload, payload_bytes, n, k, x, x_dtype, signs_bf16, y, y_dtype, M, scratch,
                                  kNoAllocScratchBytes, stream);
 }

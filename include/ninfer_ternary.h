@@ -240,12 +240,16 @@ int ninfer_ternary_matmul_workspace(int fmt, uint64_t n, uint64_t k, uint64_t M,
  * activations are rounded to 16-bit fixed point per 1024-block (|x16| < 2^14,
  * relative error <= 2^-14 of the block maximum); code x activation products
  * accumulate exactly in int32 per 128-weight group, then scale in fp32.
- * PQ2_0_G128 with 2 <= M <= 8: binary16 activations scaled per 1024-block
- * (relative error <= 2^-11 per element) with exact products and fp32
- * accumulation. PQ2_0_G128 with M > 8 (prefill): binary16 activations and the
- * exact binary16 weights (code - 1) * scale on the tensor cores, fp32
- * accumulation. Other shapes: fp32 throughout. Max relative error vs exact
- * (infinity norm over y) is well under 1e-3 for the decode paths.
+ * 2 <= M <= 8 (both formats): binary16 activations scaled per 1024-block
+ * (relative error <= 2^-11 per element), exact binary16 codes, products on the
+ * tensor cores (mma.sync) with fp32 accumulation. M > 8 (prefill, both
+ * formats): binary16 activations and the exact binary16 weights
+ * (code - 1) * scale on the tensor cores (tcgen05), fp32 accumulation; PTQ1_0
+ * planes are first rewritten exactly as PQ2_0 planes in the workspace. Inputs
+ * no fast path takes (raw x whose rows are not 16-byte aligned, M > 8 with
+ * k % 1024 != 0) run a general tiled kernel in fp32. The infinity-norm relative
+ * error against the exact result stays under 1e-3 on the decode paths and
+ * under 2e-2 on the prefill path.
  * Errors: INVALID_ARGUMENT, UNKNOWN_FORMAT, SHAPE, SIZE_MISMATCH, ALIGNMENT, CUDA.
  */
 int ninfer_ternary_matmul(int fmt, const uint8_t *payload, uint64_t payload_bytes,
@@ -344,7 +348,9 @@ int ninfer_set_prefetch_before_dependency(int enable);
  *     (use ninfer_ternary_matmul with your own workspace instead).
  *   - Set-up: the first call on a device (with that device current) looks up
  *     the array's device address once; make that first call before any stream
- *     capture.
+ *     capture. The address is kept for the life of the process, so calls must
+ *     not cross a cudaDeviceReset or any other teardown of the device's
+ *     primary context.
  *   - Sharing: all calls on a device share the one array and it keeps the last
  *     call's contents (every call overwrites what it reads, so no clearing is
  *     needed). Calls that may overlap on the GPU -- on different streams, or

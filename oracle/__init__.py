@@ -41,4 +41,5 @@ from .ternary import (  # noqa: F401
     gate_up_swiglu,
     embed_rows,
     max_rel_error,
+    significant_rel_error,
 )

@@ -22,6 +22,9 @@ beyond what the step's own definition states:
 * projection        -- y = W . transform(x) with W[r, c] = value(code) * scale
                        of the group (format page §3: one binary16 per group)
 * embedding         -- inverse transform of gathered rows (TensorSharp article §4.4)
+* error figures     -- the infinity-norm relative error the accuracy bounds are
+                       stated in, and a per-element relative error over the
+                       outputs that are not small (the pages fix no metric)
 
 Parity pins: all functions are pinned in tests/test_oracle_pins.py.
 """
@@ -389,9 +392,35 @@ def embed_rows(fmt, payload, n: int, k: int, ids, signs) -> np.ndarray:
 
 
 def max_rel_error(got, ref) -> float:
-    """max_i |got_i - ref_i| / max_i |ref_i| (infinity-norm relative error)."""
+    """Infinity-norm relative error, max_i |got_i - ref_i| / max_i |ref_i|: the
+    accuracy figure the decode, transform and embedding bounds (1e-3) and the
+    tensor-core prefill bound (2e-2) are stated in. The pages fix no metric; this
+    is the plain reading of "max relative error" for a vector result. The
+    denominator is always the reference's. With an all-zero (or empty)
+    reference the relative error is undefined and the absolute error
+    max_i |got_i - ref_i| is returned instead, so an exact zero output scores 0."""
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     den = np.max(np.abs(ref)) if ref.size else 0.0
     num = np.max(np.abs(got - ref)) if ref.size else 0.0
     return float(num / den) if den > 0 else float(num)
+
+
+def significant_rel_error(got, ref, floor: float = 0.1) -> float:
+    """Per-element relative error over the outputs that are not small:
+    max_i |got_i - ref_i| / |ref_i| over the i with |ref_i| >= floor * rms(ref),
+    rms(ref) = sqrt(mean(ref_i^2)). It catches a localised error on small
+    outputs (a wrong row or group with a small value) that the infinity-norm
+    figure hides under a large max |ref|. 0.0 when no element qualifies (an
+    empty or all-zero reference)."""
+    got = np.asarray(got, dtype=np.float64).reshape(-1)
+    ref = np.asarray(ref, dtype=np.float64).reshape(-1)
+    if got.shape != ref.shape:
+        raise ValueError("got and ref differ in size")
+    if ref.size == 0:
+        return 0.0
+    rms = np.sqrt(np.mean(ref * ref))
+    sel = (np.abs(ref) >= floor * rms) & (ref != 0)
+    if not np.any(sel):
+        return 0.0
+    return float(np.max(np.abs(got[sel] - ref[sel]) / np.abs(ref[sel])))

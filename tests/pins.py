@@ -443,4 +443,53 @@ def pin_ptq1_0_every_byte_value():
         assert np.all(W[B, :35] == 0) and np.all(W[B, 40:124] == 0)
 
 
+# ----------------------------------------------------------- error figures ---
+def pin_max_rel_error_worked():
+    """The infinity-norm relative error on hand-worked vectors. Each case is
+    chosen so that one plausible slip changes the answer: a dropped absolute
+    value (a negative largest difference), the denominator taken from got
+    instead of ref (max |got| > max |ref|), a mean in place of a max, and the
+    all-zero reference convention (absolute error)."""
+    f = oracle.max_rel_error
+    # |3 - 4| / 4: the largest difference is negative
+    assert f([1.0, 2.0, 3.0], [1.0, 2.0, 4.0]) == 0.25
+    # |5 - 4| / 4 = 0.25 as well (sign of the difference does not matter)
+    assert f([1.0, 2.0, 5.0], [1.0, 2.0, 4.0]) == 0.25
+    # max |got| = 8 > max |ref| = 4: normalised by the reference, 4 / 4 = 1
+    assert f([0.0, 0.0, 8.0], [0.0, 0.0, 4.0]) == 1.0
+    # largest difference (0.5 at index 0) and largest |ref| (-10 at index 2) differ
+    assert f([1.5, -3.0, -10.0], [1.0, -3.0, -10.0]) == 0.05
+    # 2-D arrays are compared element by element, whole-array maxima
+    assert f(np.array([[1.0, 2.0], [3.0, 4.5]]), np.array([[1.0, 2.0], [3.0, 4.0]])) == 0.125
+    # all-zero reference: the absolute error; identical zero vectors score 0
+    assert f([0.5, 0.0], [0.0, 0.0]) == 0.5
+    assert f([0.0, -0.25], [0.0, 0.0]) == 0.25
+    assert f([0.0, 0.0], [0.0, 0.0]) == 0.0
+    # identical vectors score exactly 0
+    assert f([3.0, -7.0, 1e-300], [3.0, -7.0, 1e-300]) == 0.0
+
+
+def pin_significant_rel_error_worked():
+    """The per-element relative error over |ref_i| >= 0.1 * rms(ref), on
+    hand-worked vectors. ref = (10, 0.8, 0.01, -5): rms = sqrt(125.6401 / 4)
+    = 5.6045.., so the threshold 0.56 keeps 10, 0.8 and -5 and drops 0.01
+    (a threshold of 0.1 * max = 1.0 would also drop 0.8)."""
+    f = oracle.significant_rel_error
+    ref = [10.0, 0.8, 0.01, -5.0]
+    # errors 0.1/10, 0.04/0.8, (0.49/0.01 dropped), 0.2/5 -> 0.05 from the 0.8 element
+    assert abs(f([10.1, 0.84, 0.5, -5.2], ref) - 0.05) < 1e-12
+    # the small element alone is wrong: it is below the threshold, so 0
+    assert f([10.0, 0.8, 0.5, -5.0], ref) == 0.0
+    # negative reference element, got on the far side of zero: |-4 - (-5)| / 5 = 0.2
+    assert abs(f([10.0, 0.8, 0.01, -4.0], ref) - 0.2) < 1e-12
+    # relative to |ref_i| (0.8), not to max |ref|: 0.4 / 0.8 = 0.5
+    assert abs(f([10.0, 1.2, 0.01, -5.0], ref) - 0.5) < 1e-12
+    # all elements equal in size: every one qualifies, 1/2
+    assert f([1.0, -1.0, 1.5], [1.0, -1.0, 1.0]) == 0.5
+    # empty and all-zero references
+    assert f([], []) == 0.0 and f([0.3, 0.0], [0.0, 0.0]) == 0.0
+    # a different floor: 0.5 * rms = 2.80 keeps only 10 and -5
+    assert abs(f([10.1, 1.2, 0.01, -5.2], ref, floor=0.5) - 0.04) < 1e-12
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

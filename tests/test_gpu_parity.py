@@ -4,7 +4,9 @@ Small shapes span several tiles and ragged tails and compare every output;
 the full-size workloads compare all outputs where the oracle finishes in
 seconds and sampled rows otherwise. Tolerance (infinity-norm relative error,
 max|y - y_ref| / max|y_ref|): 1e-3 for the decode projection, the transform
-and the embedding; 2e-2 for the 16-bit tensor-core prefill path.
+and the embedding; 2e-2 for the 16-bit tensor-core prefill path. The
+projections and the embedding also bound the per-element relative error over
+the outputs that are not small (|y_ref| >= 0.1 rms(y_ref)): 1e-2 and 2e-2.
 """
 import numpy as np
 import pytest
@@ -19,6 +21,26 @@ pytestmark = pytest.mark.gpu
 
 TOL_DECODE = 1e-3
 TOL_PREFILL = 2e-2
+# Per-element relative error over the outputs with |y_ref| >= 0.1 rms(y_ref).
+# The decode kernels round the rotated activation to 16 bits (integer path:
+# 14-bit magnitude per 1024-block; MMA path: binary16), which leaves an output
+# error of about 1e-4 rms(y); at 0.1 rms(y) that is a per-element error near
+# 1e-3 rms and a few times that at the maximum over ~1e4 such outputs. The
+# bounds below keep a margin of about three over that estimate.
+TOL_DECODE_ELEM = 1e-2
+TOL_PREFILL_ELEM = 2e-2
+
+
+def check_decode(y, ref):
+    """Both accuracy figures for a decode, transform or embedding result."""
+    e, s = oracle.max_rel_error(y, ref), oracle.significant_rel_error(y, ref)
+    assert e <= TOL_DECODE and s <= TOL_DECODE_ELEM, (e, s)
+
+
+def check_prefill(y, ref):
+    """Both accuracy figures for a tensor-core prefill result."""
+    e, s = oracle.max_rel_error(y, ref), oracle.significant_rel_error(y, ref)
+    assert e <= TOL_PREFILL and s <= TOL_PREFILL_ELEM, (e, s)
 
 
 # ---------------------------------------------------------------- transform ---
@@ -59,7 +81,7 @@ def test_matmul_tiny_workload():
     c = synth.make_case("tiny")
     y = run_matmul("PQ2_0_G128", c)
     ref = oracle_matmul_rows("PQ2_0_G128", c, np.arange(c.workload.n))
-    assert oracle.max_rel_error(y, ref) <= TOL_DECODE
+    check_decode(y, ref)
 
 
 @pytest.mark.parametrize("fmt", ["PQ2_0_G128", "PTQ1_0_G128"])
@@ -70,7 +92,7 @@ def test_matmul_small_shapes(fmt, n, k, M):
     c = synth.make_case("gateup", n=n, k=k, M=M, seed=n * 7 + k + M)
     y = run_matmul(fmt, c)
     ref = oracle_matmul_rows(fmt, c, np.arange(n))
-    assert oracle.max_rel_error(y, ref) <= TOL_DECODE
+    check_decode(y, ref)
 
 
 @pytest.mark.parametrize("n,k,M", [(4099, 3072, 7), (2100, 2048, 8), (63, 9216, 4), (16, 1024, 2)])
@@ -81,7 +103,7 @@ def test_matmul_ptq1_block_split(n, k, M):
     c = synth.make_case("down", n=n, k=k, M=M, seed=n + k + M)
     y = run_matmul("PTQ1_0_G128", c)
     ref = oracle_matmul_rows("PTQ1_0_G128", c, np.arange(n))
-    assert oracle.max_rel_error(y, ref) <= TOL_DECODE
+    check_decode(y, ref)
 
 
 @pytest.mark.parametrize("n,k,rotate", [(40, 16384, True), (300, 17408, True), (200, 32768, True),
@@ -93,7 +115,7 @@ def test_matmul_ptq1_m1_wide_k(n, k, rotate):
     c = synth.make_case("down", n=n, k=k, M=1, seed=n + k)
     y = run_matmul("PTQ1_0_G128", c, rotate=rotate)
     ref = oracle_matmul_rows("PTQ1_0_G128", c, np.arange(n), rotate=rotate)
-    assert oracle.max_rel_error(y, ref) <= TOL_DECODE
+    check_decode(y, ref)
 
 
 @pytest.mark.parametrize("n,k,rotate", [(300, 16384, True), (130, 20480, True), (90, 20400, False)])
@@ -103,7 +125,7 @@ def test_matmul_pq2_m1_wide_k(n, k, rotate):
     c = synth.make_case("gateup", n=n, k=k, M=1, seed=n + k)
     y = run_matmul("PQ2_0_G128", c, rotate=rotate)
     ref = oracle_matmul_rows("PQ2_0_G128", c, np.arange(n), rotate=rotate)
-    assert oracle.max_rel_error(y, ref) <= TOL_DECODE
+    check_decode(y, ref)
 
 
 @pytest.mark.slow
@@ -116,7 +138,7 @@ def test_matmul_ptq1_ring_refill():
     rng = np.random.default_rng(7)
     rows = np.unique(np.concatenate([np.arange(0, 8000, 97), [7999], rng.integers(0, 8000, 400)]))
     ref = oracle_matmul_rows("PTQ1_0_G128", c, rows)
-    assert oracle.max_rel_error(y[:, rows], ref) <= TOL_DECODE
+    check_decode(y[:, rows], ref)
 
 
 @pytest.mark.parametrize("fmt", ["PQ2_0_G128", "PTQ1_0_G128"])
@@ -129,7 +151,7 @@ def test_matmul_unrotated_ragged_k(fmt, n, k, M):
     c = synth.make_case("gateup", n=n, k=k, M=M, seed=n + k)
     y = run_matmul(fmt, c, rotate=False)
     ref = oracle_matmul_rows(fmt, c, np.arange(n), rotate=False)
-    assert oracle.max_rel_error(y, ref) <= TOL_DECODE
+    check_decode(y, ref)
 
 
 @pytest.mark.parametrize("fmt", ["PQ2_0_G128", "PTQ1_0_G128"])
@@ -139,7 +161,7 @@ def test_matmul_unrotated_padded_k(fmt):
     c = synth.make_case("gateup", n=129, k=300, M=2, seed=5)
     y = run_matmul(fmt, c, rotate=False)
     ref = oracle_matmul_rows(fmt, c, np.arange(129), rotate=False)
-    assert oracle.max_rel_error(y, ref) <= TOL_DECODE
+    check_decode(y, ref)
 
 
 def test_matmul_bf16_output():
@@ -154,7 +176,7 @@ def test_matmul_gateup_full():
     c = synth.make_case("gateup")
     y = run_matmul("PQ2_0_G128", c)
     ref = oracle_matmul_rows("PQ2_0_G128", c, np.arange(c.workload.n))
-    assert oracle.max_rel_error(y, ref) <= TOL_DECODE
+    check_decode(y, ref)
 
 
 @pytest.mark.slow
@@ -163,7 +185,7 @@ def test_matmul_down_full(M):
     c = synth.make_case("down", M=M)
     y = run_matmul("PTQ1_0_G128", c)
     ref = oracle_matmul_rows("PTQ1_0_G128", c, np.arange(c.workload.n))
-    assert oracle.max_rel_error(y, ref) <= TOL_DECODE
+    check_decode(y, ref)
 
 
 @pytest.fixture(scope="module")
@@ -182,7 +204,7 @@ def test_matmul_head_sampled(head_case, M):
     rng = np.random.default_rng(123)
     rows = np.unique(np.concatenate([[0, 1, c.workload.n - 1], rng.integers(0, c.workload.n, 3000)]))
     ref = oracle_matmul_rows("PQ2_0_G128", sub, rows)
-    assert oracle.max_rel_error(y[:, rows], ref) <= TOL_DECODE
+    check_decode(y[:, rows], ref)
     assert np.all(np.isfinite(y))
 
 
@@ -195,7 +217,7 @@ def test_embed_head_rows(head_case):
     torch.cuda.synchronize()
     sub = oracle.pack_planes("PQ2_0_G128", c.values[c.ids], c.scales[c.ids])
     ref = oracle.embed_rows("PQ2_0_G128", sub, c.ids.size, k, np.arange(c.ids.size), signs_values(c))
-    assert oracle.max_rel_error(out.cpu().numpy(), ref) <= TOL_DECODE
+    check_decode(out.cpu().numpy(), ref)
 
 
 @pytest.mark.parametrize("fmt", ["PQ2_0_G128", "PTQ1_0_G128"])
@@ -208,7 +230,7 @@ def test_matmul_prefill_small(fmt, preset, n, k, M):
     c = synth.make_case(preset, n=n, k=k, M=M, seed=n + k + M)
     y = run_matmul(fmt, c)
     ref = oracle_matmul_rows(fmt, c, np.arange(n))
-    assert oracle.max_rel_error(y, ref) <= TOL_PREFILL
+    check_prefill(y, ref)
 
 
 @pytest.mark.parametrize("fmt", ["PQ2_0_G128", "PTQ1_0_G128"])
@@ -219,7 +241,7 @@ def test_matmul_prefill_multi_tile(fmt):
     c = synth.make_case("prefill", n=7601, k=1024, M=1500, seed=7)
     y = run_matmul(fmt, c)
     ref = oracle_matmul_rows(fmt, c, np.arange(7601))
-    assert oracle.max_rel_error(y, ref) <= TOL_PREFILL
+    check_prefill(y, ref)
 
 
 def test_matmul_prefill_ptq1_invalid_trits():
@@ -237,14 +259,14 @@ def test_matmul_prefill_ptq1_invalid_trits():
     high[rng.integers(0, high.size, 20)] = rng.integers(81, 256, 20).astype(np.uint8)
     y = run_matmul("PTQ1_0_G128", c, payload_dev=dev_u8(pay))
     ref = oracle.ternary_matmul("PTQ1_0_G128", pay, 40, 1024, c.x, signs_values(c))
-    assert oracle.max_rel_error(y, ref) <= TOL_PREFILL
+    check_prefill(y, ref)
 
 
 def test_matmul_prefill_unrotated_bf16_out():
     c = synth.make_case("prefill", n=256, k=2048, M=64, seed=11)
     y = run_matmul("PQ2_0_G128", c, rotate=False, y_dtype=torch.bfloat16)
     ref = oracle_matmul_rows("PQ2_0_G128", c, np.arange(256), rotate=False)
-    assert oracle.max_rel_error(y, ref) <= TOL_PREFILL
+    check_prefill(y, ref)
 
 
 @pytest.mark.slow
@@ -254,7 +276,7 @@ def test_matmul_prefill_down_sampled():
     rng = np.random.default_rng(8)
     rows = np.unique(np.concatenate([[0, c.workload.n - 1], rng.integers(0, c.workload.n, 128)]))
     ref = oracle_matmul_rows("PTQ1_0_G128", c, rows)
-    assert oracle.max_rel_error(y[:, rows], ref) <= TOL_PREFILL
+    check_prefill(y[:, rows], ref)
 
 
 @pytest.mark.slow
@@ -264,7 +286,7 @@ def test_matmul_prefill_sampled():
     rng = np.random.default_rng(7)
     rows = np.unique(np.concatenate([[0, c.workload.n - 1], rng.integers(0, c.workload.n, 256)]))
     ref = oracle_matmul_rows("PQ2_0_G128", c, rows)
-    assert oracle.max_rel_error(y[:, rows], ref) <= TOL_PREFILL
+    check_prefill(y[:, rows], ref)
 
 
 # --------------------------------------------------------------- embedding ---
@@ -276,7 +298,7 @@ def test_embed_small(fmt):
     out = nt.ninfer_ternary_embed(fmt, payload, 500, 3072, torch.from_numpy(ids_np).to(DEV), dev_signs(c.signs))
     torch.cuda.synchronize()
     ref = oracle.embed_rows(fmt, oracle.pack_planes(fmt, c.values, c.scales), 500, 3072, ids_np, signs_values(c))
-    assert oracle.max_rel_error(out.cpu().numpy(), ref) <= TOL_DECODE
+    check_decode(out.cpu().numpy(), ref)
 
 
 def test_embed_out_of_range_ids_flagged():
@@ -291,7 +313,7 @@ def test_embed_out_of_range_ids_flagged():
     assert np.all(o[1] == 0) and np.all(o[2] == 0)
     ref = oracle.embed_rows("PQ2_0_G128", oracle.pack_planes("PQ2_0_G128", c.values, c.scales), 64, 1024, [3, 5],
                             signs_values(c))
-    assert oracle.max_rel_error(o[[0, 3]], ref) <= TOL_DECODE
+    check_decode(o[[0, 3]], ref)
     status.zero_()
     nt.ninfer_ternary_embed("PQ2_0_G128", payload, 64, 1024, ids[[0, 3]].contiguous(), dev_signs(c.signs), status=status)
     torch.cuda.synchronize()

@@ -222,6 +222,69 @@ def m_ptq1_fifth_digit_dropped(mp):
     _patch(mp, "_decode_ptq1", dec)
 
 
+def m_error_abs_dropped(mp):
+    def f(got, ref):
+        got, ref = np.asarray(got, np.float64), np.asarray(ref, np.float64)
+        den = np.max(np.abs(ref)) if ref.size else 0.0
+        num = np.max(got - ref) if ref.size else 0.0
+        return float(num / den) if den > 0 else float(num)
+    _patch(mp, "max_rel_error", f)
+
+
+def m_error_normalised_by_got(mp):
+    def f(got, ref):
+        got, ref = np.asarray(got, np.float64), np.asarray(ref, np.float64)
+        den = np.max(np.abs(got)) if got.size else 0.0
+        num = np.max(np.abs(got - ref)) if ref.size else 0.0
+        return float(num / den) if den > 0 else float(num)
+    _patch(mp, "max_rel_error", f)
+
+
+def m_error_mean_not_max(mp):
+    def f(got, ref):
+        got, ref = np.asarray(got, np.float64), np.asarray(ref, np.float64)
+        den = np.mean(np.abs(ref)) if ref.size else 0.0
+        num = np.mean(np.abs(got - ref)) if ref.size else 0.0
+        return float(num / den) if den > 0 else float(num)
+    _patch(mp, "max_rel_error", f)
+
+
+def m_error_zero_reference_scores_zero(mp):
+    orig = _orig("max_rel_error")
+    def f(got, ref):
+        ref_a = np.asarray(ref, np.float64)
+        return 0.0 if not np.any(ref_a) else orig(got, ref)
+    _patch(mp, "max_rel_error", f)
+
+
+def m_significant_threshold_on_max(mp):
+    def f(got, ref, floor=0.1):
+        got, ref = np.asarray(got, np.float64).reshape(-1), np.asarray(ref, np.float64).reshape(-1)
+        if ref.size == 0 or not np.any(ref):
+            return 0.0
+        sel = np.abs(ref) >= floor * np.max(np.abs(ref))
+        return float(np.max(np.abs(got[sel] - ref[sel]) / np.abs(ref[sel])))
+    _patch(mp, "significant_rel_error", f)
+
+
+def m_significant_normalised_by_max(mp):
+    def f(got, ref, floor=0.1):
+        got, ref = np.asarray(got, np.float64).reshape(-1), np.asarray(ref, np.float64).reshape(-1)
+        if ref.size == 0 or not np.any(ref):
+            return 0.0
+        sel = np.abs(ref) >= floor * np.sqrt(np.mean(ref * ref))
+        return float(np.max(np.abs(got[sel] - ref[sel])) / np.max(np.abs(ref)))
+    _patch(mp, "significant_rel_error", f)
+
+
+def m_significant_no_threshold(mp):
+    def f(got, ref, floor=0.1):
+        got, ref = np.asarray(got, np.float64).reshape(-1), np.asarray(ref, np.float64).reshape(-1)
+        sel = ref != 0
+        return float(np.max(np.abs(got[sel] - ref[sel]) / np.abs(ref[sel]))) if np.any(sel) else 0.0
+    _patch(mp, "significant_rel_error", f)
+
+
 MUTATIONS = [v for k, v in sorted(globals().items()) if k.startswith("m_")]
 
 

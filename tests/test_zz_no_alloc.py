@@ -21,7 +21,7 @@ from gpu_util import DEV, dev_signs, dev_u8, dev_x
 
 pytestmark = pytest.mark.gpu
 
-TOL = 1e-3      # same infinity-norm relative tolerance as the decode parity tests
+TOL = {True: 1e-3, False: 2e-2}     # decode (M <= 8) / prefill: the parity tests' infinity-norm bounds
 
 
 def _rel(a, b):
@@ -44,11 +44,17 @@ def _noalloc(fmt_id, payload, n, k, x, signs, y):
               signs.data_ptr() if signs is not None else None, y.data_ptr(), 0, x.shape[0], stream)
 
 
-@pytest.mark.parametrize("fmt,n,k,M", [("PTQ1_0_G128", 300, 2048, 3), ("PQ2_0_G128", 517, 5120, 1)])
+# Every case is one whose path takes a workspace, so the built-in array is
+# written and read: per-block partial sums (PTQ1_0, 2 <= M <= 8), binary16
+# activation fragments (PQ2_0, 2 <= M <= 8), and on the prefill path the
+# rotated binary16 activations (PQ2_0) plus the PTQ1_0 planes rewritten as
+# PQ2_0 planes.
+@pytest.mark.parametrize("fmt,n,k,M", [("PTQ1_0_G128", 300, 2048, 3), ("PQ2_0_G128", 517, 5120, 4),
+                                       ("PQ2_0_G128", 200, 2048, 24), ("PTQ1_0_G128", 64, 1024, 16)])
 def test_noalloc_matches_workspace_entry_two_calls(fmt, n, k, M):
     fmt_id = nt.FORMATS[fmt]
     need = nt.ninfer_ternary_matmul_workspace(fmt, n, k, M, True)
-    assert need <= nt.NOALLOC_SCRATCH_BYTES
+    assert 0 < need <= nt.NOALLOC_SCRATCH_BYTES
     for call, seed in enumerate((31, 32)):          # two calls in a row share the scratch array
         c = synth.make_case("gateup", n=n, k=k, M=M, seed=seed)
         payload = dev_u8(nt.ninfer_ternary_pack(fmt, c.values, c.scales))
@@ -59,7 +65,7 @@ def test_noalloc_matches_workspace_entry_two_calls(fmt, n, k, M):
         torch.cuda.synchronize()
         got, want = y.cpu().numpy(), ref.cpu().numpy()
         assert np.all(np.isfinite(got)), f"call {call}: non-finite output"
-        assert _rel(got, want) <= TOL, f"call {call}: rel {_rel(got, want)}"
+        assert _rel(got, want) <= TOL[M <= 8], f"call {call}: rel {_rel(got, want)}"
 
 
 def test_noalloc_rejects_problem_larger_than_scratch():
