@@ -8,10 +8,14 @@ pool of weight-payload copies whose total size is more than 3x the L2 cache.
 Steps are captured in CUDA graphs and timed with CUDA events on the launching
 stream.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload gateup|ffn_gate_up|down|down_m8|head|head_m8|
-                                                                  prefill|prefill_down|tiny]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--no-extra]
+  python bench.py --workload gateup|ffn_gate_up|down|down_m8|head|head_m8|head_ptq1|head_ptq1_m8|
+                             prefill|prefill_down|embed|embed_ptq1|tiny   (one workload alone)
   python bench.py --impl reference ...   (the fp64 CPU oracle on the host cores)
 
+Without --workload, gate/up is the headline and the FFN down (PTQ1_0, M = 1
+and M = 8) and the output head (both formats) are timed in the same run, each
+in its own graphs over its own payload pool, under "workloads".
 Prints one JSON line (rank 0).
 """
 from __future__ import annotations
@@ -179,123 +183,227 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------- our arm ---
+# Workloads timed in the same run as the default headline (gate/up), each with
+# its own graph of back-to-back calls: the other 17408 x 5120 decode shape (FFN
+# down, PTQ1_0, M = 1 and M = 8) and the output head in both formats.
+EXTRA_WORKLOADS = ("down", "down_m8", "head", "head_ptq1")
+EXTRA_STEPS = {"down": 20000, "down_m8": 20000, "head": 3000, "head_ptq1": 3000}
+
+_CASES = {}
+
+
+def _case(w):
+    """Inputs of workload w; workloads drawn from the same preset shape and seed
+    (the head in both formats) share one draw."""
+    key = (w.n, w.k, w.M if w.kind != "embed" else 1, w.seed, w.mats, w.kind == "embed", w.x_dtype)
+    if key not in _CASES:
+        _CASES.clear()
+        _CASES[key] = synth.make_case(w, with_ids=w.kind == "embed")
+    return _CASES[key]
+
+
+class _Setup:
+    """Device buffers and the per-call step of one workload: a pool of payload
+    copies larger than 3x L2 (cycled call by call), the activation, the signs,
+    the output and the workspace, all resident in HBM."""
+
+    def __init__(self, name, dev):
+        import torch
+
+        import bit_gemv_gb300 as nt
+
+        self.nt = nt
+        self.w = w = synth.WORKLOADS[name]
+        c = _case(w)
+        self.embed = w.kind == "embed"
+        payload_host = nt.ninfer_ternary_pack(w.fmt, c.values, c.scales)
+        up_host = nt.ninfer_ternary_pack(w.fmt, c.up[0], c.up[1]) if w.mats == 2 else None
+        self.l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        self.pool = max(2, -(-3 * self.l2 // (w.mats * payload_host.size)))
+        self.pool_bytes = self.pool * w.mats * payload_host.size
+        self.payloads = [torch.from_numpy(payload_host).to(dev) for _ in range(self.pool)]
+        del payload_host
+        self.signs = torch.from_numpy(c.signs.view(np.int16)).to(dev)
+        if w.mats == 2:
+            self.payloads_up = [torch.from_numpy(up_host).to(dev) for _ in range(self.pool)]
+            self.signs_up = torch.from_numpy(c.up[2].view(np.int16)).to(dev)
+        M = w.M
+        if w.x_dtype == "bf16":
+            self.x_host = torch.from_numpy(c.x_raw[:M].view(np.int16)).view(torch.bfloat16)
+        else:
+            self.x_host = torch.from_numpy(c.x[:M])
+        self.x = self.x_host.to(dev)
+        self.y = torch.empty((synth.EMBED_COUNT, w.k) if self.embed else (M, w.n), dtype=torch.float32, device=dev)
+        self.ids_host = torch.from_numpy(c.ids) if self.embed else None
+        self.ids = self.ids_host.to(dev) if self.embed else None
+        if w.mats == 2:
+            ws_bytes = nt.ninfer_ternary_gate_up_workspace(w.fmt, w.n, w.k, M, True, True)
+        else:
+            ws_bytes = nt.ninfer_ternary_matmul_workspace(w.fmt, w.n, w.k, M, True)
+        self.ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+
+    def step(self, i):
+        w, nt = self.w, self.nt
+        if self.embed:
+            nt.ninfer_ternary_embed(w.fmt, self.payloads[i % self.pool], w.n, w.k, self.ids, self.signs, out=self.y)
+        elif w.mats == 2:
+            nt.ninfer_ternary_gate_up(w.fmt, self.payloads[i % self.pool], self.payloads_up[i % self.pool], w.n, w.k,
+                                      self.x, self.signs, self.signs_up, y=self.y, workspace=self.ws)
+        else:
+            nt.ninfer_ternary_matmul(w.fmt, self.payloads[i % self.pool], w.n, w.k, self.x, self.signs, y=self.y,
+                                     workspace=self.ws)
+
+
+def _capture(stream, fn, count, offset=0):
+    import torch
+
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(count):
+                fn(offset + i)
+    return g
+
+
+def _timed_graphs(stream, graphs, warm_replays, world, dev):
+    """Replay graphs (each a list replayed in order) after warm-up replays of the
+    first; CUDA events on the launching stream, barrier + synchronize on both
+    sides; the slowest rank's milliseconds."""
+    import torch
+
+    with torch.cuda.stream(stream):
+        for _ in range(warm_replays):
+            graphs[0].replay()
+    stream.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for gr in graphs:
+            gr.replay()
+        e1.record(stream)
+    e1.synchronize()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        ms = max_over_ranks(ms, dev)
+    return ms
+
+
+def _graph_set(stream, fn, steps, per_graph):
+    full, rem = divmod(steps, per_graph)
+    g_main = _capture(stream, fn, per_graph) if full else None
+    g_rem = _capture(stream, fn, rem, per_graph * full) if rem else None
+    return ([g_main] * full) + ([g_rem] if g_rem is not None else [])
+
+
+def _roofline(w, M, s_step, traffic):
+    nbytes = algorithmic_bytes(w, M)
+    if M > 8:
+        return tensor_roofline(M, w.n, w.k, s_step, traffic)
+    achieved = nbytes["total"] / s_step / 1e9
+    peak, peak_kind = measured_peaks()
+    return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": f"{peak_kind} hbm_gbs (copy)",
+            "frac_of_8000_nominal": round(achieved / 8000, 4)}
+
+
+def _measure_extra(name, stream, dev, world, steps, warmup):
+    """One more workload timed in the same run: its own graphs of back-to-back
+    calls over its own payload pool."""
+    su = _Setup(name, dev)
+    w = su.w
+    with torch_stream(stream):
+        for i in range(max(warmup, 3)):
+            su.step(i)
+    stream.synchronize()
+    graphs = _graph_set(stream, su.step, steps, min(steps, 1000))
+    ms = _timed_graphs(stream, graphs, max(1, -(-warmup // min(steps, 1000))), world, dev)
+    s_step = ms / steps / 1e3
+    tag, srcs = dominant_kernel(w)
+    res = {"format": w.fmt, "n": w.n, "k": w.k, "M": w.M, "steps": steps, "ms_per_step": round(ms / steps, 6),
+           "value": round(job_value(algorithmic_bytes(w, w.M)["weights"], world, s_step), 2), "unit": "GB/s",
+           "projection_tokens_per_s": round(world * w.M / s_step, 1),
+           "roofline": _roofline(w, w.M, s_step, profile_traffic(tag, name, srcs)),
+           "gpu_launches": steps * kernels_per_step(w),
+           "l2": f"rotating pool of {su.pool} payload copies ({su.pool_bytes / 1e6:.0f} MB > 3x L2)"}
+    del su, graphs
+    import torch
+
+    torch.cuda.empty_cache()
+    return res
+
+
+def torch_stream(stream):
+    import torch
+
+    return torch.cuda.stream(stream)
+
+
 def run_ours(args, rank: int, world: int, local_rank: int):
     import torch
 
-    import bit_gemv_gb300 as nt
-
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    w = synth.WORKLOADS[args.workload]
-    embed = w.kind == "embed"
-    c = synth.make_case(w, with_ids=embed)
+    name = args.workload or "gateup"
+    su = _Setup(name, dev)
+    w = su.w
     n, k, M = w.n, w.k, w.M
     nbytes = algorithmic_bytes(w, M)
-    payload_host = nt.ninfer_ternary_pack(w.fmt, c.values, c.scales)
-    del c.values
-    up_host = nt.ninfer_ternary_pack(w.fmt, c.up[0], c.up[1]) if w.mats == 2 else None
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    pool = max(2, -(-3 * l2 // (w.mats * payload_host.size)))
-    payloads = [torch.from_numpy(payload_host).to(dev) for _ in range(pool)]
-    signs = torch.from_numpy(c.signs.view(np.int16)).to(dev)
-    if w.mats == 2:
-        payloads_up = [torch.from_numpy(up_host).to(dev) for _ in range(pool)]
-        signs_up = torch.from_numpy(c.up[2].view(np.int16)).to(dev)
-    if w.x_dtype == "bf16":
-        x_host = torch.from_numpy(c.x_raw.view(np.int16)).view(torch.bfloat16)
-    else:
-        x_host = torch.from_numpy(c.x)
-    x = x_host.to(dev)
-    y = torch.empty((synth.EMBED_COUNT, k) if embed else (M, n), dtype=torch.float32, device=dev)
-    ids = torch.from_numpy(c.ids).to(dev) if embed else None
-    if w.mats == 2:
-        ws_bytes = nt.ninfer_ternary_gate_up_workspace(w.fmt, n, k, M, True, True)
-    else:
-        ws_bytes = nt.ninfer_ternary_matmul_workspace(w.fmt, n, k, M, True)
-    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(dev)
 
-    def step(i):
-        if embed:
-            nt.ninfer_ternary_embed(w.fmt, payloads[i % pool], n, k, ids, signs, out=y)
-        elif w.mats == 2:
-            nt.ninfer_ternary_gate_up(w.fmt, payloads[i % pool], payloads_up[i % pool], n, k, x, signs, signs_up, y=y,
-                                      workspace=ws)
-        else:
-            nt.ninfer_ternary_matmul(w.fmt, payloads[i % pool], n, k, x, signs, y=y, workspace=ws)
-
     # e2e buffers: pinned host inputs (activations, or token ids) in, pinned host result out
-    in_dev = ids if embed else x
-    in_host = torch.from_numpy(c.ids) if embed else x_host
-    x_pin = [in_host.clone().pin_memory() for _ in range(pool)]
-    y_pin = [torch.empty(tuple(y.shape), dtype=torch.float32).pin_memory() for _ in range(pool)]
+    in_dev = su.ids if su.embed else su.x
+    in_host = su.ids_host if su.embed else su.x_host
+    x_pin = [in_host.clone().pin_memory() for _ in range(su.pool)]
+    y_pin = [torch.empty(tuple(su.y.shape), dtype=torch.float32).pin_memory() for _ in range(su.pool)]
 
     def step_e2e(i):
-        in_dev.copy_(x_pin[i % pool], non_blocking=True)
-        step(i)
-        y_pin[i % pool].copy_(y, non_blocking=True)
+        in_dev.copy_(x_pin[i % su.pool], non_blocking=True)
+        su.step(i)
+        y_pin[i % su.pool].copy_(su.y, non_blocking=True)
 
     per_graph = min(args.steps, 1000)
-
-    def capture(fn, count, offset=0):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(stream):
-            with torch.cuda.graph(g, stream=stream):
-                for i in range(count):
-                    fn(offset + i)
-        return g
-
     with torch.cuda.stream(stream):
         for i in range(max(args.warmup, 1)):     # eager warm-up (module load, first launches)
-            step(i)
+            su.step(i)
     stream.synchronize()
-    full, rem = divmod(args.steps, per_graph)
-    g_main = capture(step, per_graph)
-    g_rem = capture(step, rem, per_graph * full) if rem else None
-    g_e2e = capture(step_e2e, per_graph)
-    g_e2e_rem = capture(step_e2e, rem, per_graph * full) if rem else None
-
-    def timed(graph, graph_rem, warm_graph_replays):
-        with torch.cuda.stream(stream):
-            for _ in range(warm_graph_replays):
-                graph.replay()
-        stream.synchronize()
-        if world > 1:
-            torch.distributed.barrier()
-        torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            e0.record(stream)
-            for _ in range(full):
-                graph.replay()
-            if graph_rem is not None:
-                graph_rem.replay()
-            e1.record(stream)
-        e1.synchronize()
-        torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1)
-        if world > 1:
-            ms = max_over_ranks(ms, dev)
-        return ms
-
+    g_main = _graph_set(stream, su.step, args.steps, per_graph)
+    g_e2e = _graph_set(stream, step_e2e, args.steps, per_graph)
     warm_replays = max(1, -(-args.warmup // per_graph))
+
     clocks = ClockSampler(local_rank, args.clocks_dir)
     clocks.start()
-    ms_total = timed(g_main, g_rem, warm_replays)
+    ms_total = _timed_graphs(stream, g_main, warm_replays, world, dev)
     clock_info = clocks.stop()
-    ms_e2e = timed(g_e2e, g_e2e_rem, warm_replays)
+    ms_e2e = _timed_graphs(stream, g_e2e, warm_replays, world, dev)
 
-    # final output check against the first warm-up result (same inputs -> same bits)
+    # eager calls (no graph): what a caller that launches each projection
+    # itself sees, host-side argument checks and launch set-up included
+    eager_calls = min(args.steps, 2000)
+    with torch.cuda.stream(stream):
+        for i in range(20):
+            su.step(i)
+    stream.synchronize()
+    ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        ea.record(stream)
+        for i in range(eager_calls):
+            su.step(i)
+        eb.record(stream)
+    eb.synchronize()
+    eager_us = ea.elapsed_time(eb) / eager_calls * 1e3
+
     torch.cuda.synchronize()
     ms_step = ms_total / args.steps
     s_step = ms_step / 1e3
     value = job_value(nbytes["weights"], world, s_step)
-    achieved = nbytes["total"] / s_step / 1e9
-    peak, peak_kind = measured_peaks()
     e2e_s = ms_e2e / args.steps / 1e3
     tag, srcs = dominant_kernel(w)
-    traffic = profile_traffic(tag, args.workload, srcs)
+    traffic = profile_traffic(tag, name, srcs)
     res = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -309,23 +417,32 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         "vs_baseline": None,
         "dtype": path_dtype(w),
         "data": "synthetic",
-        "config": {"workload": args.workload, "format": w.fmt, "n": n, "k": k, "M": M, "x_dtype": w.x_dtype,
+        "config": {"workload": name, "format": w.fmt, "n": n, "k": k, "M": M, "x_dtype": w.x_dtype,
                    "seed": w.seed, "rotate": True, "projections": w.mats,
-                   **({"rows_gathered": synth.EMBED_COUNT} if embed else {}),
-                   "l2": f"rotating pool of {pool} payload copies ({pool * w.mats * payload_host.size / 1e6:.0f} MB > 3x L2 "
-                         f"{l2 / 1e6:.0f} MB)",
+                   **({"rows_gathered": synth.EMBED_COUNT} if su.embed else {}),
+                   "l2": f"rotating pool of {su.pool} payload copies ({su.pool_bytes / 1e6:.0f} MB > 3x L2 "
+                         f"{su.l2 / 1e6:.0f} MB)",
                    "parallelism": f"replicas x{world}"},
-        "tokens_per_s": round(world * (synth.EMBED_COUNT if embed else M) / s_step, 1),
-        "roofline": ({"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                      "peak_source": f"{peak_kind} hbm_gbs (copy)", "frac_of_8000_nominal": round(achieved / 8000, 4)}
-                     if M <= 8 else tensor_roofline(M, n, k, s_step, traffic)),
+        "projection_tokens_per_s": round(world * (synth.EMBED_COUNT if su.embed else M) / s_step, 1),
+        "roofline": _roofline(w, M, s_step, traffic),
         "e2e": {"value": round(job_value(nbytes["weights"], world, e2e_s), 2), "unit": "GB/s",
                 "h2d_bytes_per_step": int(in_host.numel() * in_host.element_size()),
-                "d2h_bytes_per_step": int(y.numel() * 4), "ms_per_step": round(ms_e2e / args.steps, 6)},
+                "d2h_bytes_per_step": int(su.y.numel() * 4), "ms_per_step": round(ms_e2e / args.steps, 6)},
+        "eager_us_per_call": round(eager_us, 3),
         "clocks": clock_info,
         "gpu_launches": args.steps * kernels_per_step(w),
     }
+    del g_main, g_e2e, su
+    torch.cuda.empty_cache()
+    extras = EXTRA_WORKLOADS if args.workload is None and not args.no_extra else ()
+    if extras:
+        clocks2 = ClockSampler(local_rank, args.clocks_dir)
+        clocks2.start()
+        res["workloads"] = {}
+        for nm in extras:
+            res["workloads"][nm] = _measure_extra(nm, stream, dev, world, min(EXTRA_STEPS[nm], args.steps), args.warmup)
+            res["gpu_launches"] += res["workloads"][nm]["gpu_launches"]
+        res["workloads_clocks"] = clocks2.stop()
     return res
 
 
@@ -491,7 +608,10 @@ def main():
     ap.add_argument("--steps", type=int, default=50000)
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="gateup", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--workload", default=None, choices=sorted(synth.WORKLOADS),
+                    help="time one workload alone (default: gate/up as the headline, plus the down and head "
+                         "workloads in the same run)")
+    ap.add_argument("--no-extra", action="store_true", help="time the headline workload only")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--clocks-dir", default=None, help="where to keep the raw nvidia-smi samples (default: temp dir)")
     args = ap.parse_args()
@@ -501,6 +621,7 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
+        args.workload = args.workload or "gateup"
         res = run_reference(args, rank, world)
         if res is not None:
             print(json.dumps(res))
@@ -513,7 +634,7 @@ def main():
     res = run_ours(args, rank, world, local_rank)
     if rank == 0:
         if not args.no_cpu_baseline:
-            res["cpu_baseline"] = cpu_baseline(args.workload)
+            res["cpu_baseline"] = cpu_baseline(args.workload or "gateup")
         print(json.dumps(res))
     if world > 1:
         import torch.distributed as dist

@@ -66,6 +66,7 @@ _sig = {
     "ninfer_ternary_embed": (_int, [_int, _vp, _u64, _u64, _u64, _vp, _u64, _vp, _vp, _int, _vp, _vp]),
     "ninfer_device_errors": (_int, [C.POINTER(C.c_uint32), _int]),
     "ninfer_set_prefetch_before_dependency": (_int, [_int]),
+    "ninfer_set_wait_limit": (_int, [C.c_longlong]),
     "ninfer_ternary_matmul_noalloc": (_int, [_int, _vp, _u64, _u64, _u64, _vp, _int, _vp, _vp, _int, _u64, _vp]),
     "ninfer_ternary_gate_up_workspace": (_int, [_int, _u64, _u64, _u64, _int, _int, C.POINTER(_u64)]),
     "ninfer_ternary_gate_up": (_int, [_int, _vp, _vp, _u64, _u64, _u64, _vp, _int, _vp, _vp, _vp, _int, _u64, _vp,
@@ -173,6 +174,13 @@ def ninfer_device_errors(clear: bool = True) -> int:
 
 def ninfer_set_prefetch_before_dependency(enable: bool) -> None:
     _check(_lib.ninfer_set_prefetch_before_dependency(int(bool(enable))))
+
+
+WAIT_LIMIT_DEFAULT = 4_000_000_000
+
+
+def ninfer_set_wait_limit(cycles: int) -> None:
+    _check(_lib.ninfer_set_wait_limit(int(cycles)))
 
 
 # ---------------------------------------------------------------- device ---

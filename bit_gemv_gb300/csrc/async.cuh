@@ -76,8 +76,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 
 // Waits for the phase with the given parity to complete; gives up after about
 // `cycles` SM clocks (~2 s), sets kErrBarrierTimeout in *err and returns false.
+// cycles <= 0 gives up at once, without looking at the barrier (the failure
+// path's test hook).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t *err,
                                           long long cycles = 4000000000ll) {
+    if (cycles <= 0) {
+        atomicOr(err, kErrBarrierTimeout);
+        return false;
+    }
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (!mbar_try_wait(bar, parity)) {
@@ -94,6 +100,11 @@ __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepc
 
 __device__ __forceinline__ void named_barrier(uint32_t id, uint32_t threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// Arrives at a named barrier without waiting for it (whole warps).
+__device__ __forceinline__ void named_barrier_arrive(uint32_t id, uint32_t threads) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
 __device__ __forceinline__ uint2 lds64(uint32_t addr) {

@@ -31,13 +31,16 @@ __device__ __forceinline__ void wht1024_warp(float (&v)[32], int lane) {
             v[j | (1 << b)] = a - c;
         }
     }
-#pragma unroll
+    // lane bits: the lane whose bit s is set keeps partner - own, the other own +
+    // partner; fmaf(+-1, own, partner) rounds once, exactly as that add does.
+    // One rolled loop keeps the code (fetched once per launch) short.
+#pragma unroll 1
     for (int s = 0; s < 5; ++s) {
-        const bool upper = (lane >> s) & 1;
+        const float sg = ((lane >> s) & 1) ? -1.f : 1.f;
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
             const float p = __shfl_xor_sync(0xffffffffu, v[j], 1 << s);
-            v[j] = upper ? (p - v[j]) : (v[j] + p);
+            v[j] = fmaf(sg, v[j], p);
         }
     }
 }

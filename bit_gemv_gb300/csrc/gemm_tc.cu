@@ -436,8 +436,8 @@ int gemm_tc_launch(const TcPlan &plan, const uint8_t *payload, const ninfer_row_
     if (!st) st = encode_rows(&p.cmap, payload + g.base_offset, g.base_row_bytes, g.n, 16, kBN, false);
     if (!st) st = encode_rows(&p.smap, payload + g.scale_offset, g.scale_row_bytes, g.n, 16, kBN, false);
     if (st) return st;
-    e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.smem);
-    if (e != cudaSuccess) return fail(NINFER_ERR_CUDA, "prefill: smem attribute: %s", cudaGetErrorString(e));
+    int st_attr = set_smem_attribute((const void *)gemm_tc_kernel, (int)plan.smem);
+    if (st_attr) return st_attr;
     gemm_tc_kernel<<<plan.grid, kThreads, plan.smem, stream>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return fail(NINFER_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));

@@ -21,6 +21,11 @@ int device_error_word(uint32_t **out);
 // Whether decode kernels may request weights before the dependency wait
 // (ninfer_set_prefetch_before_dependency).
 bool prefetch_before_dependency();
+// Bound, in SM clock cycles, of the weight-ring waits of the kernels that take
+// it as a parameter (ninfer_set_wait_limit; default about two seconds).
+long long wait_limit_cycles();
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per kernel, device and size.
+int set_smem_attribute(const void *kernel, int bytes);
 
 // Rows of a plane as a 2-D byte tensor {row_bytes, rows}, for 2-D box loads:
 // boxes of box_bytes x box_rows, optionally 128-byte swizzled.
@@ -44,8 +49,8 @@ struct IntPlan {
     bool ok;
     int mats;
     uint32_t act_one;
-    uint32_t grid, rows_per_cta, nitem, nslots, pre_issue;
-    uint32_t off_ring, off_act, off_part, off_bar, off_cnt, smem;
+    uint32_t grid, rows_per_cta, nitem, nslots, pre_issue, nrot;
+    uint32_t off_ring, off_act, off_rot, off_part, off_bar, off_cnt, smem;
     uint64_t workspace;
 };
 bool gemv_pq2_int_plan(const ninfer_row_split_geometry &g, uint64_t M, bool rotate, int sms, int smem_limit,

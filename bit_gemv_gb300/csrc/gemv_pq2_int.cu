@@ -9,32 +9,36 @@
 // ("GGUF 完整讲解" §4.3), and one binary16 scale per 128-weight group at
 // scale_offset ("bonsai三元GGUF模型转ninfer模型01" §3).
 //
-// Arithmetic: every CTA rotates x itself (one warp per 1024-block: sign
-// multiply, the 1024-point butterfly, block maximum) and keeps it in shared
-// memory as 16-bit fixed point, x16 = rint(xr * 2^E) with E per block so that
-// max |x16| < 2^14, laid out as dp2a operands. In a 32-bit word of codes (16
-// weights, four per byte) the mask 0x03 << 2p per byte leaves the four codes of
-// position p as bytes (times 4^p); dp2a multiplies two of them by two int16
-// activations and accumulates exactly in int32. Per group:
-//   sum_j c_j x16_j = acc0 + acc1/4 + acc2/16 + acc3/64        (exact shifts)
-//   y += scale * 2^-E * (that - sum_j x16_j)                     (value = code - 1)
-// dp2a issues on the FMA-heavy pipe and the masks on the ALU pipe, so the two
-// overlap; legacy mma.sync with changing operands is slower on GB300.
+// Activation: one warp per 1024-block rotates it in registers (the warp-held
+// butterfly of device.cuh: five stages within the lane, five across lanes),
+// takes the block maximum with shuffles and rounds to 16-bit fixed point,
+// x16 = rint(v * 2^E) with max |x16| < 2^14, no shared-memory transpose and no
+// barrier. A lane then holds 8 consecutive elements, which are exactly one
+// 16-byte dp2a operand entry of the shared-memory activation table:
+//   entry(word w, h) = {(x16[16w + 8h + p], x16[16w + 8h + 4 + p]), p = 0..3}.
 //
-// Data movement: one CTA per SM owns a contiguous row range, in tiles of 128
-// rows. Weights stream through a ring of item slots; an item is 128 rows x 8
+// Arithmetic: in a 32-bit word of codes (16 weights, four per byte) the mask
+// 0x03 << 2p per byte leaves the four codes of position p as bytes (times
+// 4^p); dp2a multiplies two of them by two int16 activations and accumulates
+// exactly in int32, one chain per position. Per group:
+//   64 sum_j (code_j - 1) x16_j = ((acc0 * 4 + acc1) * 4 + acc2) * 4 + acc3
+// where acc3 starts at -64 sum_j x16_j (exact in int32: |64 acc0| < 2^29),
+// then y += scale * 2^-E / 64 * that, in fp32.
+//
+// Work: one CTA per SM owns a contiguous row range, in tiles of 128 rows.
+// Weights stream through a ring of chunk slots; a chunk is 128 rows x 8
 // groups: two 128-byte-swizzled tensor boxes of 128 rows x 128 bytes (a 3-D
 // map view keeps them inside the CTA's rows) and one box of the rows' 8 scales
-// (128 rows x 16 bytes), completing on the slot's mbarrier. Warps w and w + 8
-// take words 0-3 and 4-7 of group w of every item, lane l rows l, l+32, l+64,
-// l+96 of the tile, so each activation word read from shared memory serves
-// four rows. A few items are
-// requested before the programmatic-dependent-launch wait (weights and signs
-// are read-only parameters, so the stream overlaps the previous kernel's
-// tail); x is requested right after the wait and the rest of the ring behind
-// it, so the latency-critical read does not queue behind the whole slice. The
-// last of the sixteen warps reading an item re-arms its slot with the item
-// nslots further on.
+// (128 rows x 16 bytes), completing on the slot's mbarrier. The chunks of a
+// tile are taken two at a time: warps 0-7 take chunk 2r and warps 8-15 chunk
+// 2r + 1, warp w the whole group w % 8, lane l rows l, l+32, l+64, l+96, so
+// each activation entry read from shared memory serves four rows. With an
+// odd number of chunks per tile the last one is shared by all sixteen warps,
+// half a group each. One chunk is requested before the programmatic-
+// dependent-launch wait (weights and signs are read-only), the rest of the
+// ring after the rotating warps have requested x, by a warp that does not
+// rotate; the last reader of a chunk refills its slot with the chunk nslots
+// further on.
 #include <cstring>
 
 #include <cuda.h>
@@ -49,13 +53,15 @@
 namespace ninfer {
 namespace {
 
-constexpr int kThreads = 512;     // 16 warps, two per group of an item; one CTA per SM
+constexpr int kThreads = 512;     // 16 warps; one CTA per SM
 constexpr int kWarps = 16;
 constexpr int kRows = 128;        // rows per tile, four per lane
-constexpr uint32_t kBoxBytes = 128 * kRows;              // one 128-byte column of the tile
-constexpr uint32_t kItemBytes = 2 * kBoxBytes + 16 * kRows;
+constexpr uint32_t kBoxBytes = 128 * kRows;               // one 128-byte column of the tile
+constexpr uint32_t kChunkBytes = 2 * kBoxBytes + 16 * kRows;
 constexpr uint32_t kMaxSlots = 8;
-constexpr uint32_t kRotPairs = 8;     // warp pairs that rotate x (one 1024-block at a time each)
+constexpr uint32_t kActGroupBytes = 256;                  // 16 operand entries per group
+constexpr uint32_t kBarX = 1;                             // named barrier: x has arrived
+constexpr uint32_t kRotScratchBytes = 4352;               // per rotating warp: 1048 floats / 1072 int16
 
 struct IntParams {
     CUtensorMap wmap_main, wmap_last;   // base rows: {row bytes, R rows, CTA} / last CTA {row bytes, rows}
@@ -64,27 +70,28 @@ struct IntParams {
     const void *x;
     const uint16_t *signs;              // bf16 +-1 per element, or null (no rotation)
     const uint16_t *signs2;             // second matrix's signs (may equal signs)
-    uint32_t act_bytes;                 // operand words + group entries of one rotation
+    uint32_t act_bytes;                 // operand entries + group entries of one rotation
     void *y;
     uint64_t n;
-    uint32_t k, groups, nblk, nitem, rows_per_cta;     // nitem: items per tile, ceil(groups / 8)
+    uint32_t k, groups, nblk, nchunk, rows_per_cta;     // nchunk: chunks per tile and matrix, groups / 8
     int x_dtype, y_dtype;
-    uint32_t nslots, pre_issue;
-    uint32_t off_ring, off_act, off_part, off_bar, off_cnt;
+    uint32_t nslots, pre_issue, nrot;    // nrot: warps rotating at once (one scratch each)
+    uint32_t off_ring, off_act, off_rot, off_part, off_bar, off_cnt;
     uint32_t *err;
+    long long wait_cycles;              // bound of each ring wait
 };
 
-// Item i = tile * (kMats * nitem) + mat * nitem + j (groups 8j .. 8j + 7 of
+// Chunk i = tile * (kMats * nchunk) + mat * nchunk + j (groups 8j .. 8j + 7 of
 // the tile's rows of matrix mat): its two weight boxes and its scale box into
 // ring slot i % nslots (one thread).
 template <int kMats>
-__device__ __forceinline__ void issue_item(const IntParams &p, uint8_t *smem, uint32_t item, bool last_cta) {
-    const uint32_t per_tile = kMats * p.nitem;
-    const uint32_t tile = item / per_tile, jj = item % per_tile, mat = kMats == 1 ? 0 : jj / p.nitem;
-    const uint32_t j = jj - mat * p.nitem, slot = item % p.nslots;
-    const uint32_t dst = smem_u32(smem + p.off_ring) + slot * kItemBytes;
+__device__ __forceinline__ void issue_chunk(const IntParams &p, uint8_t *smem, uint32_t item, bool last_cta) {
+    const uint32_t per_tile = kMats * p.nchunk;
+    const uint32_t tile = item / per_tile, jj = item % per_tile, mat = kMats == 1 ? 0 : jj / p.nchunk;
+    const uint32_t j = jj - mat * p.nchunk, slot = item % p.nslots;
+    const uint32_t dst = smem_u32(smem + p.off_ring) + slot * kChunkBytes;
     const uint32_t bar = smem_u32(smem + p.off_bar) + 8 * slot;
-    mbar_arrive_expect_tx(bar, kItemBytes);
+    mbar_arrive_expect_tx(bar, kChunkBytes);
     const int y0 = (int)(tile * kRows), xs = (int)(j * 16);
     if (last_cta) {
         const CUtensorMap *wm = mat ? &p.wmap2_last : &p.wmap_last, *sm = mat ? &p.smap2_last : &p.smap_last;
@@ -99,56 +106,172 @@ __device__ __forceinline__ void issue_item(const IntParams &p, uint8_t *smem, ui
     }
 }
 
-// Writes block b's dp2a operand words and group entries (x16 from
-// rotate_quantize16, act16.cuh):
-//   act[word][4h + p] = (x16[16 word + 8h + p], x16[16 word + 8h + 4 + p]),
-//   gs[group] = {2^-E, sum of the group's x16 (as int bits)}.
-// Thread t of the pair takes runs t and t + 64 of eight consecutive elements.
-__device__ __forceinline__ void pack_pq2(const int16_t *qs, uint8_t *act_s, uint32_t groups, uint32_t b, int t, int E,
-                                         uint32_t bar) {
-    const int lane = t & 31;
-    uint4 *act = reinterpret_cast<uint4 *>(act_s);
-    float2 *gs = reinterpret_cast<float2 *>(act_s + (uint64_t)groups * 256);
+// Block b of x (and its signs) in the warp-held layout: v[8i + e] = element
+// 1024 b + 256 i + 8 lane + e; zero past k.
+template <int kXType>
+__device__ __forceinline__ void load_block(const void *x, uint32_t k, uint32_t b, int lane, float (&v)[32]) {
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const int run = t + 64 * i;
-        const uint4 raw = reinterpret_cast<const uint4 *>(qs)[run];
-        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};     // x16 pairs (2e, 2e+1)
-        // entry p = (x16[p], x16[4 + p]) of the run
-        uint4 pk;
-        pk.x = __byte_perm(w[0], w[2], 0x5410);
-        pk.y = __byte_perm(w[0], w[2], 0x7632);
-        pk.z = __byte_perm(w[1], w[3], 0x5410);
-        pk.w = __byte_perm(w[1], w[3], 0x7632);
-        const uint32_t word = b * 64 + (run >> 1);
-        if (word < groups * 8) act[word * 2 + (run & 1)] = pk;
-        int sum = 0;
+    for (int i = 0; i < 4; ++i) {
+        float u[8];
+        const uint64_t idx = (uint64_t)b * 1024 + 256 * i + 8 * lane;
+        if (idx + 8 <= k) {
+            load8(x, idx, kXType, u);
+        } else {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) sum += (int)(int16_t)(w[q] & 0xffff) + (int)(int16_t)(w[q] >> 16);
+            for (int e = 0; e < 8; ++e) u[e] = idx + e < k ? load1(x, idx + e, kXType) : 0.f;
+        }
 #pragma unroll
-        for (int sh = 8; sh > 0; sh >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, sh);
-        const uint32_t G = b * 8 + (run >> 4);     // 16 runs per group of 128
-        if ((lane & 15) == 0 && G < groups) gs[G] = make_float2(ldexpf(1.f, -E), __int_as_float(sum));
+        for (int e = 0; e < 8; ++e) v[8 * i + e] = u[e];
     }
-    named_barrier(bar, 64);      // qs is read before the next block reuses the tile
+}
+
+__device__ __forceinline__ void load_block_signs(const uint16_t *s, uint32_t b, int lane, float (&d)[32]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float u[8];
+        load_signs8(s, (uint64_t)b * 1024 + 256 * i + 8 * lane, u);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) d[8 * i + e] = u[e];
+    }
+}
+
+// Butterflies over register index bits 0-4 of the warp's 32 values (element
+// bits held in the registers).
+__device__ __forceinline__ void butterfly32(float (&v)[32]) {
+#pragma unroll
+    for (int bit = 0; bit < 5; ++bit)
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            if (j & (1 << bit)) continue;
+            const float a = v[j], c = v[j | (1 << bit)];
+            v[j] = a + c;
+            v[j | (1 << bit)] = a - c;
+        }
+}
+
+// Rotates block b (x in v, as load_block leaves it; signs in d unless rotate is
+// false) with one warp, rounds it to 16-bit fixed point and writes its operand
+// entries and group entries {2^-E / 64 (with the transform's 1/32), -64 * sum
+// of x16}. The element bits held in registers are first {0,1,2,8,9} (lane =
+// bits 3-7), then, after a transpose through the warp's scratch (fp32, element
+// e at e + 8 (e >> 8)), bits 3-7 (lane = {0,1,2,8,9}): every butterfly stage
+// runs in registers. The rounded values go back through the scratch (int16,
+// element e at e + 16 (e >> 8)) so that each lane again holds runs of eight
+// consecutive elements, which are exactly operand entries. scr: kRotScratchBytes.
+__device__ __forceinline__ void rotate_pack(bool rotate, float (&v)[32], const float (&d)[32], uint32_t b,
+                                            uint32_t groups, uint8_t *act, float *scr, int lane) {
+    if (rotate) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] *= d[j];
+        butterfly32(v);      // element bits 0, 1, 2, 8, 9
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+            *reinterpret_cast<float4 *>(scr + 264 * i + 8 * lane + 4 * c) =
+                make_float4(v[8 * i + 4 * c], v[8 * i + 4 * c + 1], v[8 * i + 4 * c + 2], v[8 * i + 4 * c + 3]);
+    __syncwarp();
+    // lane = element bits (0, 1, 2, 8, 9), register j = bits 3-7: e = (lane & 7) + 8 j + 256 (lane >> 3)
+    const int base = (lane & 7) + 264 * (lane >> 3);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = scr[base + 8 * j];
+    if (rotate) butterfly32(v);      // element bits 3-7: v = H (D x) = 32 xr
+    // block maximum (a tree, then across the lanes)
+    float m[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) m[j] = fmaxf(fabsf(v[j]), fabsf(v[j + 16]));
+#pragma unroll
+    for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+        for (int j = 0; j < w; ++j) m[j] = fmaxf(m[j], m[j + w]);
+    float mx = m[0];
+#pragma unroll
+    for (int s = 16; s > 0; s >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, s));
+    int E = 0;
+    if (mx > 0.f) E = 13 - ilogbf(mx);     // max |x16| < 2^14
+    E = max(-100, min(100, E));
+    const float up = ldexpf(1.f, E);
+    const float f = ldexpf(1.f, -E - 6 - (rotate ? 5 : 0));
+    __syncwarp();        // every lane has read its transposed values
+    // quantise: x16 = rint(v * 2^E) (adding 1.5 * 2^23 rounds to nearest, ties to even);
+    // group (element bits 7-9) sums, bit 7 = j >> 4, bits 8-9 = lane >> 3
+    int16_t *qs = reinterpret_cast<int16_t *>(scr);
+    const int qbase = (lane & 7) + 272 * (lane >> 3);
+    int gsum[2][2] = {{0, 0}, {0, 0}};
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        const int q = __float_as_int(fmaf(v[j], up, 12582912.0f)) - 0x4B400000;
+        gsum[j >> 4][j & 1] += q;
+        qs[qbase + 8 * j] = (int16_t)q;
+    }
+    int gs2[2] = {gsum[0][0] + gsum[0][1], gsum[1][0] + gsum[1][1]};
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int s = 1; s < 8; s <<= 1) gs2[h] += __shfl_xor_sync(0xffffffffu, gs2[h], s);
+    float2 *gs = reinterpret_cast<float2 *>(act + (uint64_t)groups * kActGroupBytes);
+    if ((lane & 7) == 0) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint32_t G = b * 8 + 2 * (lane >> 3) + h;
+            if (G < groups) gs[G] = make_float2(f, __int_as_float(-64 * gs2[h]));
+        }
+    }
+    __syncwarp();
+    // element 1024 b + 256 i + 8 lane + r (r < 8): entry (lane % 2) of word (lane / 2) of
+    // the 16 words starting at block word 16 i
+    uint4 *ent = reinterpret_cast<uint4 *>(act);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint4 raw = *reinterpret_cast<const uint4 *>(qs + 272 * i + 8 * lane);
+        const uint32_t G = b * 8 + 2 * i + (lane >> 4);
+        uint4 en;     // (x16[p], x16[4 + p]), p = 0..3
+        en.x = __byte_perm(raw.x, raw.z, 0x5410);
+        en.y = __byte_perm(raw.x, raw.z, 0x7632);
+        en.z = __byte_perm(raw.y, raw.w, 0x5410);
+        en.w = __byte_perm(raw.y, raw.w, 0x7632);
+        if (G < groups) ent[(uint64_t)b * 128 + 32 * i + lane] = en;
+    }
+    __syncwarp();        // the scratch may be reused
 }
 
 // kMats = 1: y = W x. kMats = 2 (fused FFN gate/up): y = silu(Wg x_g) * (Wu x_u)
-// for the same rows of both matrices, x_g and x_u rotated with each matrix's signs.
-template <int kMats>
+// for the same rows of both matrices, x_g and x_u rotated with each matrix's
+// signs. kXType: the dtype of x (one instance per dtype keeps the code short).
+template <int kMats, int kXType>
 __global__ void __launch_bounds__(kThreads, 1) gemv_pq2_int_kernel(const __grid_constant__ IntParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint64_t r_begin = (uint64_t)blockIdx.x * p.rows_per_cta;
     const uint64_t r_end = r_begin + p.rows_per_cta < p.n ? r_begin + p.rows_per_cta : p.n;
     const bool last_cta = blockIdx.x == gridDim.x - 1;
+    const uint32_t per_tile = kMats * p.nchunk;
     const uint32_t ntile = (uint32_t)((r_end - r_begin + kRows - 1) / kRows);
-    const uint32_t nitems = ntile * kMats * p.nitem;
+    const uint32_t nitems = ntile * per_tile;
     const uint32_t bar0 = smem_u32(smem + p.off_bar);
     uint32_t *cnt = reinterpret_cast<uint32_t *>(smem + p.off_cnt);
     uint32_t *issued = cnt + kMaxSlots, *failed = cnt + kMaxSlots + 1;
+    // rotation tasks (matrix, block): one rotation per block, or two when the
+    // fused matrices have different signs; rotating warp w takes tasks w, w + nrot, ...
+    const uint32_t nrmat = (kMats == 2 && p.signs2 != p.signs) ? 2 : 1;
+    const uint32_t ntask = nrmat * p.nblk;
+    // the ring is issued by the last warp, which never rotates
+    const int producer = kWarps - 1;
+    const uint32_t ring_to = p.nslots < nitems ? p.nslots : nitems;
+    const uint32_t pre = p.pre_issue < ring_to ? p.pre_issue : ring_to;
+    const uint32_t nrot = ntask < p.nrot ? ntask : p.nrot;     // at most 15: the producer never rotates
+    const bool rotating = (uint32_t)warp < nrot;
+    // Up to four idle warps (one per SM sub-partition) run the rotation of the
+    // first block once, before the dependency wait, with the same instructions
+    // as the rotating warps (x read early, results into scratch and discarded):
+    // every line of that code, executed once per launch, is then already in the
+    // instruction caches when x arrives.
+    const uint32_t nwarm = (uint32_t)producer - nrot < 4 ? (uint32_t)producer - nrot : 4;
+    const bool warm = !rotating && (uint32_t)warp < nrot + nwarm;
+    const uint32_t nwait = 32 * (nrot + nwarm + 1);
 
-    if (tid == 0) {
+    if (tid == producer * 32) {
         prefetch_tmap(last_cta ? &p.wmap_last : &p.wmap_main);
         prefetch_tmap(last_cta ? &p.smap_last : &p.smap_main);
         if (kMats == 2) {
@@ -161,139 +284,167 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_pq2_int_kernel(const __grid_
         }
         *failed = 0;
         fence_mbar_init();
-    }
-    __syncthreads();
-    const uint32_t ring_to = p.nslots < nitems ? p.nslots : nitems;
-    const uint32_t pre = p.pre_issue < ring_to ? p.pre_issue : ring_to;
-    if (tid == 0) {
-        // weights are read-only parameters: a few items before the dependency wait
-        for (uint32_t i = 0; i < pre; ++i) issue_item<kMats>(p, smem, i, last_cta);
-    }
-    // rotation tasks (matrix, block): one rotation per block, or two when the
-    // fused matrices have different signs; warp pair pr takes tasks pr, pr + nrot, ...
-    const uint32_t nrmat = (kMats == 2 && p.signs2 != p.signs) ? 2 : 1;
-    const uint32_t ntask = nrmat * p.nblk;
-    const uint32_t nrot = ntask < kRotPairs ? ntask : kRotPairs;
-    const uint32_t pr = warp >> 1;
-    const int t = tid & 63;
-    auto task_src = [&](uint32_t task) {
-        return XSource{p.x, task >= p.nblk ? p.signs2 : p.signs, p.k, p.x_dtype};
-    };
-    float d[16];
-    if (pr < nrot) {
-        const XSource xs0 = task_src(pr);
-        if (xs0.signs) load_signs16(xs0, pr % p.nblk, t, d);     // also read-only
-    }
-    pdl_launch_dependents();
-    pdl_wait();          // x may come from the preceding kernel
-
-    float v[16];
-    if (pr < nrot) load_run16(task_src(pr), pr % p.nblk, t, v);
-    __syncthreads();     // every warp's x request is out: the rest of the ring queues behind them
-    if (tid == 0) {
-        for (uint32_t i = pre; i < ring_to; ++i) issue_item<kMats>(p, smem, i, last_cta);
-        *issued = ring_to;
+        // weights are read-only parameters: the first chunks before the dependency wait
+        for (uint32_t i = 0; i < pre; ++i) issue_chunk<kMats>(p, smem, i, last_cta);
+        *issued = pre;
     }
     uint8_t *act_s = smem + p.off_act;
-    if (pr < nrot) {
-        float *tile = reinterpret_cast<float *>(smem + p.off_part + pr * kRotScratch);
-        for (uint32_t task = pr; task < ntask; task += nrot) {
-            const XSource xs = task_src(task);
-            const uint32_t b = task % p.nblk;
-            if (task != pr) {
-                if (xs.signs) load_signs16(xs, b, t, d);
-                load_run16(xs, b, t, v);
+    float v[32], d[32];
+    if (rotating || warm) {
+        // the first rotation of a rotating warp, or the warm-up pass: one code path
+        const uint32_t task = rotating ? (uint32_t)warp : 0;
+        const uint32_t b = task % p.nblk;
+        float *scr = reinterpret_cast<float *>(smem + (rotating ? p.off_rot + warp * kRotScratchBytes : p.off_part));
+        if (p.signs) load_block_signs(task >= p.nblk ? p.signs2 : p.signs, b, lane, d);     // read-only
+        pdl_launch_dependents();
+        if (rotating) pdl_wait();        // x may come from the preceding kernel
+        load_block<kXType>(p.x, p.k, b, lane, v);
+        // x has arrived once its first and last values can be stored; then the
+        // producer may queue the rest of the ring behind it
+        *reinterpret_cast<volatile float *>(scr) = v[0] + v[31];
+        named_barrier_arrive(kBarX, nwait);
+        rotate_pack(p.signs != nullptr, v, d, b, rotating ? p.groups : 8,
+                    rotating ? act_s + (task / p.nblk) * p.act_bytes : smem + p.off_part, scr, lane);
+        if (warm) pdl_wait();
+    } else {
+        pdl_launch_dependents();
+        pdl_wait();
+        if (warp == producer) {
+            // the rest of the ring is requested once x has arrived in every rotating
+            // warp, so that x does not queue behind it
+            named_barrier(kBarX, nwait);
+            if (lane == 0) {
+                for (uint32_t i = pre; i < ring_to; ++i) issue_chunk<kMats>(p, smem, i, last_cta);
+                *issued = ring_to;
             }
-            int E;
-            const int16_t *qs = rotate_quantize16(xs.signs != nullptr, t, v, d, tile, 1 + pr, &E);
-            pack_pq2(qs, act_s + (task / p.nblk) * p.act_bytes, p.groups, b, t, E, 1 + pr);
+            __syncwarp();
         }
     }
-    __syncthreads();
+    // more rotations than rotating warps: further rounds
+#pragma unroll 1
+    for (uint32_t task = warp + nrot; rotating && task < ntask; task += nrot) {
+        const uint32_t b = task % p.nblk;
+        if (p.signs) load_block_signs(task >= p.nblk ? p.signs2 : p.signs, b, lane, d);
+        load_block<kXType>(p.x, p.k, b, lane, v);
+        rotate_pack(p.signs != nullptr, v, d, b, p.groups, act_s + (task / p.nblk) * p.act_bytes,
+                    reinterpret_cast<float *>(smem + p.off_rot + warp * kRotScratchBytes), lane);
+    }
+    // (the ring's barriers and counters, set up by the producer, are first used
+    // after the barrier that completes the activation table)
+    __syncthreads();     // the activation table is complete
 
     bool ok = true;
-    // group gw of the item = 16-byte chunks 2gi, 2gi+1 of column h's 128-byte
-    // line; this warp reads chunk 2gi + half (words 4 half .. 4 half + 3), swizzled by row % 8
-    const uint32_t gw = warp & 7, half = warp >> 3, h = gw >> 2, gi = gw & 3;
-    const uint32_t ch = ((2 * gi + half) ^ (lane & 7)) << 4;
     float *part = reinterpret_cast<float *>(smem + p.off_part);
-    const bool refill = nitems > p.nslots;    // otherwise the whole slice sits in the ring
-    uint32_t slot = 0, phase = 0, item = 0;
+    const uint32_t gw = warp & 7, upper = warp >> 3;
+    const uint32_t h = gw >> 2, gi = gw & 3;
+    // swizzled 16-byte chunks (row % 8 pattern) of the group in column h's 128-byte line
+    const uint32_t ch0 = ((2 * gi) ^ (lane & 7)) << 4, ch1 = ((2 * gi + 1) ^ (lane & 7)) << 4;
+    const uint32_t rounds = (per_tile + 1) / 2;
+#pragma unroll 1
     for (uint32_t tile = 0; tile < ntile; ++tile) {
         float y[kMats][4];      // rows lane + 32q of the tile, per matrix
 #pragma unroll
         for (int mt = 0; mt < kMats; ++mt)
 #pragma unroll
             for (int q = 0; q < 4; ++q) y[mt][q] = 0.f;
-        for (uint32_t jj = 0; jj < kMats * p.nitem; ++jj, ++item) {
-            const uint32_t mat = kMats == 1 ? 0 : (jj >= p.nitem), j = jj - mat * p.nitem;
+#pragma unroll 1
+        for (uint32_t r = 0; r < rounds; ++r) {
+            // a full round: chunks 2r (warps 0-7) and 2r + 1 (warps 8-15), a whole group per warp;
+            // the last round of an odd count: chunk 2r for all warps, half a group each
+            const bool full = 2 * r + 1 < per_tile;
+            const uint32_t jj = full ? 2 * r + upper : 2 * r;
+            const uint32_t item = tile * per_tile + jj;
+            const uint32_t slot = item % p.nslots, phase = (item / p.nslots) & 1;
+            const uint32_t mat = kMats == 1 ? 0 : (jj >= p.nchunk), j = jj - mat * p.nchunk;
             const uint8_t *act_m = act_s + (mat < nrmat ? mat : 0) * p.act_bytes;
-            const float2 *gs = reinterpret_cast<const float2 *>(act_m + p.groups * 256);
-            ok = ok && mbar_wait(bar0 + 8 * slot, phase, p.err);
+            const float2 *gs = reinterpret_cast<const float2 *>(act_m + (uint64_t)p.groups * kActGroupBytes);
+            ok = ok && mbar_wait(bar0 + 8 * slot, phase, p.err, p.wait_cycles);
             const uint32_t G = j * 8 + gw;
             if (ok && G < p.groups) {
-                const uint8_t *sa = smem + p.off_ring + slot * kItemBytes;
-                const uint8_t *wr = sa + h * kBoxBytes + lane * 128 + ch;
-                uint32_t w[4][4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const uint4 a = *reinterpret_cast<const uint4 *>(wr + q * 4096);
-                    w[q][0] = a.x; w[q][1] = a.y; w[q][2] = a.z; w[q][3] = a.w;
-                }
-                const uint4 *aw = reinterpret_cast<const uint4 *>(act_m + (uint64_t)G * 256 + half * 128);
+                const uint8_t *sa = smem + p.off_ring + slot * kChunkBytes;
+                const uint8_t *wr = sa + h * kBoxBytes + lane * 128;
+                const uint4 *aw = reinterpret_cast<const uint4 *>(act_m + (uint64_t)G * kActGroupBytes);
+                const float2 f = gs[G];
                 int acc[4][4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-#pragma unroll
-                    for (int t = 0; t < 4; ++t) acc[q][t] = 0;
-#pragma unroll
-                for (int wi = 0; wi < 4; ++wi) {
-                    const uint4 lo = aw[2 * wi], hi = aw[2 * wi + 1];
+                if (full) {
+                    uint32_t w[4][8];
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        const uint32_t c = w[q][wi];
-                        acc[q][0] = dp2a_hi(hi.x, c & 0x03030303u, dp2a_lo(lo.x, c & 0x03030303u, acc[q][0]));
-                        acc[q][1] = dp2a_hi(hi.y, c & 0x0C0C0C0Cu, dp2a_lo(lo.y, c & 0x0C0C0C0Cu, acc[q][1]));
-                        acc[q][2] = dp2a_hi(hi.z, c & 0x30303030u, dp2a_lo(lo.z, c & 0x30303030u, acc[q][2]));
-                        acc[q][3] = dp2a_hi(hi.w, c & 0xC0C0C0C0u, dp2a_lo(lo.w, c & 0xC0C0C0C0u, acc[q][3]));
+                        const uint4 a = *reinterpret_cast<const uint4 *>(wr + q * 4096 + ch0);
+                        const uint4 c = *reinterpret_cast<const uint4 *>(wr + q * 4096 + ch1);
+                        w[q][0] = a.x; w[q][1] = a.y; w[q][2] = a.z; w[q][3] = a.w;
+                        w[q][4] = c.x; w[q][5] = c.y; w[q][6] = c.z; w[q][7] = c.w;
                     }
-                }
-                const float2 f = gs[G];
-                const int off = half ? 0 : __float_as_int(f.y);     // the group's sum of x16, once
-                // scale box: row r at r * 16 bytes holds the item's 8 scales
-                const uint8_t *sc = sa + 2 * kBoxBytes + lane * 16 + 2 * gw;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int t = acc[q][0] + (acc[q][1] >> 2) + (acc[q][2] >> 4) + (acc[q][3] >> 6) - off;
-                    const float s = __half2float(*reinterpret_cast<const __half *>(sc + q * 512));
-                    if (kMats == 1 || mat == 0) y[0][q] = fmaf(s * f.x, (float)t, y[0][q]);
-                    else y[kMats - 1][q] = fmaf(s * f.x, (float)t, y[kMats - 1][q]);
-                }
-            }
-            if (refill) {
-                // release the slot; the last of the sixteen readers re-arms it with item + nslots
-                __syncwarp();
-                if (lane == 0) {
-                    if (!ok) *failed = 1;
-                    __threadfence_block();
-                    const uint32_t seen = atomicAdd(&cnt[slot], 1u);
-                    if (seen == kWarps - 1) {
-                        cnt[slot] = 0;
-                        if (ok && !*(volatile uint32_t *)failed && item + p.nslots < nitems) {
-                            fence_proxy_async();
-                            issue_item<kMats>(p, smem, item + p.nslots, last_cta);
-                            atomicAdd(issued, 1u);
+                    for (int q = 0; q < 4; ++q) {
+                        acc[q][0] = 0; acc[q][1] = 0; acc[q][2] = 0; acc[q][3] = __float_as_int(f.y);
+                    }
+#pragma unroll
+                    for (int wi = 0; wi < 8; ++wi) {
+                        const uint4 lo = aw[2 * wi], hi = aw[2 * wi + 1];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const uint32_t c = w[q][wi];
+                            acc[q][0] = dp2a_hi(hi.x, c & 0x03030303u, dp2a_lo(lo.x, c & 0x03030303u, acc[q][0]));
+                            acc[q][1] = dp2a_hi(hi.y, c & 0x0C0C0C0Cu, dp2a_lo(lo.y, c & 0x0C0C0C0Cu, acc[q][1]));
+                            acc[q][2] = dp2a_hi(hi.z, c & 0x30303030u, dp2a_lo(lo.z, c & 0x30303030u, acc[q][2]));
+                            acc[q][3] = dp2a_hi(hi.w, c & 0xC0C0C0C0u, dp2a_lo(lo.w, c & 0xC0C0C0C0u, acc[q][3]));
+                        }
+                    }
+                } else {
+                    // half a group: words 4 upper .. 4 upper + 3 (chunk 2 gi + upper of the line)
+                    const uint32_t chh = upper ? ch1 : ch0;
+                    uint32_t w[4][4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint4 a = *reinterpret_cast<const uint4 *>(wr + q * 4096 + chh);
+                        w[q][0] = a.x; w[q][1] = a.y; w[q][2] = a.z; w[q][3] = a.w;
+                    }
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        acc[q][0] = 0; acc[q][1] = 0; acc[q][2] = 0; acc[q][3] = upper ? 0 : __float_as_int(f.y);
+                    }
+                    const uint4 *awh = aw + 8 * upper;
+#pragma unroll
+                    for (int wi = 0; wi < 4; ++wi) {
+                        const uint4 lo = awh[2 * wi], hi = awh[2 * wi + 1];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const uint32_t c = w[q][wi];
+                            acc[q][0] = dp2a_hi(hi.x, c & 0x03030303u, dp2a_lo(lo.x, c & 0x03030303u, acc[q][0]));
+                            acc[q][1] = dp2a_hi(hi.y, c & 0x0C0C0C0Cu, dp2a_lo(lo.y, c & 0x0C0C0C0Cu, acc[q][1]));
+                            acc[q][2] = dp2a_hi(hi.z, c & 0x30303030u, dp2a_lo(lo.z, c & 0x30303030u, acc[q][2]));
+                            acc[q][3] = dp2a_hi(hi.w, c & 0xC0C0C0C0u, dp2a_lo(lo.w, c & 0xC0C0C0C0u, acc[q][3]));
                         }
                     }
                 }
-                __syncwarp();
-            } else if (!ok && lane == 0) {
-                *failed = 1;
+                // scale box: row r at r * 16 bytes holds the chunk's 8 scales
+                const uint8_t *sc = sa + 2 * kBoxBytes + lane * 16 + 2 * gw;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int t64 = ((acc[q][0] * 4 + acc[q][1]) * 4 + acc[q][2]) * 4 + acc[q][3];
+                    const float s = __half2float(*reinterpret_cast<const __half *>(sc + q * 512));
+                    if (kMats == 1 || mat == 0) y[0][q] = fmaf(s * f.x, (float)t64, y[0][q]);
+                    else y[kMats - 1][q] = fmaf(s * f.x, (float)t64, y[kMats - 1][q]);
+                }
             }
-            if (++slot == p.nslots) {
-                slot = 0;
-                phase ^= 1u;
+            // release the slot; its last reader (8 warps in a full round, 16 in the last
+            // round of an odd count) refills it with the chunk nslots further on
+            __syncwarp();
+            if (lane == 0) {
+                if (!ok) *failed = 1;
+                __threadfence_block();
+                const uint32_t seen = atomicAdd(&cnt[slot], 1u);
+                if (seen == (full ? 7u : 15u)) {
+                    cnt[slot] = 0;
+                    if (ok && !*(volatile uint32_t *)failed && item + p.nslots < nitems) {
+                        fence_proxy_async();
+                        issue_chunk<kMats>(p, smem, item + p.nslots, last_cta);
+                        atomicAdd(issued, 1u);
+                    }
+                }
             }
+            __syncwarp();
         }
 #pragma unroll
         for (int mt = 0; mt < kMats; ++mt)
@@ -336,17 +487,21 @@ bool gemv_pq2_int_plan(const ninfer_row_split_geometry &g, uint64_t M, bool rota
     if (g.scale_row_bytes % 16 || g.base_row_bytes % 16 || g.payload_bytes % 16) return false;
     if (g.k > (1u << 24) || g.n > (1ull << 31)) return false;
     const uint32_t groups = (uint32_t)g.groups_per_row;
-    const uint32_t act_one = ((groups * 264 + 15) / 16) * 16;
+    const uint32_t act_one = ((groups * (kActGroupBytes + 8) + 15) / 16) * 16;
     const uint32_t nrmat = (mats == 2 && two_rotations) ? 2 : 1;
     const uint32_t act_bytes = nrmat * act_one;
-    // tile partial sums, and before them the rotation's scratch (one padded tile per rotating warp pair)
-    const uint32_t nrot = std::min<uint32_t>(nrmat * (uint32_t)((g.k + 1023) / 1024), kRotPairs);
-    const uint32_t part_bytes = std::max<uint32_t>(mats * kWarps * kRows * 4, nrot * kRotScratch);
+    const uint32_t part_bytes = mats * kWarps * kRows * 4;     // per-warp row sums of a tile (>= one scratch)
     const uint32_t bar_bytes = kMaxSlots * 8;
     const uint32_t cnt_bytes = (kMaxSlots + 4) * 4;
-    const uint32_t fixed = act_bytes + part_bytes + bar_bytes + cnt_bytes;
-    if ((int)fixed + 2 * (int)kItemBytes > smem_limit) return false;
-    const uint32_t nslots = std::min<uint32_t>(kMaxSlots, (uint32_t)((smem_limit - (int)fixed) / (int)kItemBytes));
+    // warps rotating at once, each with its own scratch: as many as there are
+    // rotations (at most 16) while the ring keeps at least four slots
+    const uint32_t ntask = nrmat * (uint32_t)((g.k + 1023) / 1024);
+    uint32_t nrot = std::min<uint32_t>(ntask, (uint32_t)kWarps - 1);     // the producer warp never rotates
+    auto fixed_of = [&](uint32_t nr) { return act_bytes + nr * kRotScratchBytes + part_bytes + bar_bytes + cnt_bytes; };
+    while (nrot > 1 && (int)fixed_of(nrot) + 4 * (int)kChunkBytes > smem_limit) nrot = (nrot + 1) / 2;
+    const uint32_t fixed = fixed_of(nrot);
+    if ((int)fixed + 2 * (int)kChunkBytes > smem_limit) return false;
+    const uint32_t nslots = std::min<uint32_t>(kMaxSlots, (uint32_t)((smem_limit - (int)fixed) / (int)kChunkBytes));
     // one CTA per SM with ~n / SMs rows each
     const uint64_t grid0 = std::max<uint64_t>(1, std::min<uint64_t>((uint64_t)sms, g.n / 64));
     const uint64_t R = (g.n + grid0 - 1) / grid0;
@@ -356,12 +511,14 @@ bool gemv_pq2_int_plan(const ninfer_row_split_geometry &g, uint64_t M, bool rota
     plan->act_one = act_one;
     plan->grid = (uint32_t)grid;
     plan->rows_per_cta = (uint32_t)R;
-    plan->nitem = (groups + 7) / 8;
+    plan->nitem = groups / 8;
     plan->nslots = nslots;
     plan->pre_issue = std::min<uint32_t>(1, nslots);
     plan->off_ring = 0;
-    plan->off_act = nslots * kItemBytes;
-    plan->off_part = plan->off_act + act_bytes;
+    plan->off_act = nslots * kChunkBytes;
+    plan->nrot = nrot;
+    plan->off_rot = plan->off_act + act_bytes;
+    plan->off_part = plan->off_rot + nrot * kRotScratchBytes;
     plan->off_bar = plan->off_part + part_bytes;
     plan->off_cnt = plan->off_bar + bar_bytes;
     plan->smem = plan->off_cnt + cnt_bytes;
@@ -384,7 +541,7 @@ int gemv_pq2_int_launch(const IntPlan &plan, const uint8_t *payload, const ninfe
     p.k = (uint32_t)g.k;
     p.groups = (uint32_t)g.groups_per_row;
     p.nblk = (uint32_t)((g.k + 1023) / 1024);
-    p.nitem = plan.nitem;
+    p.nchunk = plan.nitem;
     p.rows_per_cta = plan.rows_per_cta;
     p.x_dtype = x_dtype;
     p.y_dtype = y_dtype;
@@ -392,9 +549,12 @@ int gemv_pq2_int_launch(const IntPlan &plan, const uint8_t *payload, const ninfe
     p.pre_issue = plan.pre_issue;
     p.off_ring = plan.off_ring;
     p.off_act = plan.off_act;
+    p.nrot = plan.nrot;
+    p.off_rot = plan.off_rot;
     p.off_part = plan.off_part;
     p.off_bar = plan.off_bar;
     p.off_cnt = plan.off_cnt;
+    p.wait_cycles = wait_limit_cycles();
     int st = device_error_word(&p.err);
     if (st) return st;
     const uint64_t R = plan.rows_per_cta, G = plan.grid, last_rows = g.n - (G - 1) * R;
@@ -424,9 +584,13 @@ int gemv_pq2_int_launch(const IntPlan &plan, const uint8_t *payload, const ninfe
                              16, kRows, false);
         if (st) return st;
     }
-    auto kernel = plan.mats == 2 ? gemv_pq2_int_kernel<2> : gemv_pq2_int_kernel<1>;
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.smem);
-    if (e != cudaSuccess) return fail(NINFER_ERR_CUDA, "gemv: smem attribute: %s", cudaGetErrorString(e));
+    void (*kernel)(IntParams) = nullptr;
+    if (x_dtype == NINFER_F32) kernel = plan.mats == 2 ? gemv_pq2_int_kernel<2, NINFER_F32> : gemv_pq2_int_kernel<1, NINFER_F32>;
+    else if (x_dtype == NINFER_BF16)
+        kernel = plan.mats == 2 ? gemv_pq2_int_kernel<2, NINFER_BF16> : gemv_pq2_int_kernel<1, NINFER_BF16>;
+    else kernel = plan.mats == 2 ? gemv_pq2_int_kernel<2, NINFER_F16> : gemv_pq2_int_kernel<1, NINFER_F16>;
+    st = set_smem_attribute((const void *)kernel, (int)plan.smem);
+    if (st) return st;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(plan.grid);
     cfg.blockDim = dim3(kThreads);
@@ -437,7 +601,7 @@ int gemv_pq2_int_launch(const IntPlan &plan, const uint8_t *payload, const ninfe
     attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, kernel, p);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, p);
     if (e != cudaSuccess) return fail(NINFER_ERR_CUDA, "gemv launch: %s", cudaGetErrorString(e));
     return NINFER_OK;
 }

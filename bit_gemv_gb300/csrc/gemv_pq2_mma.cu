@@ -458,8 +458,9 @@ int gemv_pq2_mma_launch(const MmaPlan &plan, const uint8_t *payload, const ninfe
         st = encode_rows(&p.smap_last, scale + (G - 1) * R * g.scale_row_bytes, g.scale_row_bytes, last_rows, 16,
                          kRows, false);
     if (st) return st;
-    cudaError_t e = cudaFuncSetAttribute(gemv_pq2_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.smem);
-    if (e != cudaSuccess) return fail(NINFER_ERR_CUDA, "decode gemv: smem attribute: %s", cudaGetErrorString(e));
+    int st_attr = set_smem_attribute((const void *)gemv_pq2_mma_kernel, (int)plan.smem);
+    if (st_attr) return st_attr;
+    cudaError_t e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(plan.grid);
     cfg.blockDim = dim3(kThreads);

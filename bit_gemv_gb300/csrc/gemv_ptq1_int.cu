@@ -562,8 +562,9 @@ int gemv_ptq1_int_launch(const Ptq1Plan &plan, const uint8_t *payload, const nin
         cudaError_t pe = cudaLaunchKernelEx(&pc, ptq1_prep_kernel, xsrc, p.groups, static_cast<uint8_t *>(workspace));
         if (pe != cudaSuccess) return fail(NINFER_ERR_CUDA, "ptq1 prep launch: %s", cudaGetErrorString(pe));
     }
-    cudaError_t e = cudaFuncSetAttribute(gemv_ptq1_int_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.smem);
-    if (e != cudaSuccess) return fail(NINFER_ERR_CUDA, "ptq1 gemv: smem attribute: %s", cudaGetErrorString(e));
+    int st_attr = set_smem_attribute((const void *)gemv_ptq1_int_kernel, (int)plan.smem);
+    if (st_attr) return st_attr;
+    cudaError_t e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(plan.grid);
     cfg.blockDim = dim3(kThreads);

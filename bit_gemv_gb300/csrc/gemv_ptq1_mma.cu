@@ -509,8 +509,9 @@ int gemv_ptq1_mma_launch(const Ptq1MmaPlan &plan, const uint8_t *payload, const 
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
-    cudaError_t e = cudaFuncSetAttribute(gemv_ptq1_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan.smem);
-    if (e != cudaSuccess) return fail(NINFER_ERR_CUDA, "ptq1 mma gemv: smem attribute: %s", cudaGetErrorString(e));
+    int st_attr = set_smem_attribute((const void *)gemv_ptq1_mma_kernel, (int)plan.smem);
+    if (st_attr) return st_attr;
+    cudaError_t e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(plan.nblk, plan.tiles);
     cfg.blockDim = dim3(kThreads);

@@ -317,6 +317,21 @@ int ninfer_ternary_embed(int fmt, const uint8_t *payload, uint64_t payload_bytes
 int ninfer_device_errors(uint32_t *out, int clear);
 
 /*
+ * ninfer_set_wait_limit -- bound, in SM clock cycles, of each wait of the
+ * PQ2_0_G128 M = 1 decode kernel (ninfer_ternary_matmul and the one-kernel
+ * ninfer_ternary_gate_up) for its weight copies, for calls launched after
+ * this one; the default is 4e9 (about two seconds). No counterpart on the
+ * source pages: a diagnostic hook that lets a test drive the failure path
+ * described under ninfer_device_errors without breaking anything. cycles == 0
+ * makes every such wait give up at its first check even when the copy has
+ * landed: the call then returns NINFER_OK, sets bit 0 of the error word,
+ * leaves its output incomplete, and its CTAs let the copies already issued
+ * land before they exit. Other kernels keep their fixed bound. Process-wide,
+ * host only. Errors: INVALID_ARGUMENT (cycles < 0).
+ */
+int ninfer_set_wait_limit(long long cycles);
+
+/*
  * ninfer_set_prefetch_before_dependency -- process-wide switch, default 1.
  * With 1, decode projections (ninfer_ternary_matmul with M <= 8) are launched
  * with programmatic dependent launch: they begin streaming the weight payload

@@ -136,6 +136,14 @@ WORKLOADS = {
                      description="output head, PQ2_0_G128 n=248320 k=5120, M=1"),
     "head_m8": Workload("head_m8", "PQ2_0_G128", 248320, 5120, 8, "bf16", 4,
                         description="output head, PQ2_0_G128 n=248320 k=5120, M=8"),
+    "head_ptq1": Workload("head_ptq1", "PTQ1_0_G128", 248320, 5120, 1, "bf16", 4,
+                          description="output head, PTQ1_0_G128 n=248320 k=5120 (278,118,400-byte payload), M=1"),
+    "head_ptq1_m8": Workload("head_ptq1_m8", "PTQ1_0_G128", 248320, 5120, 8, "bf16", 4,
+                             description="output head, PTQ1_0_G128 n=248320 k=5120, M=8"),
+    "embed_ptq1": Workload("embed_ptq1", "PTQ1_0_G128", 248320, 5120, 1, "bf16", 4,
+                           description="embedding: 64 token ids uniform in [0, 248320) gathered from the PTQ1_0_G128 "
+                                       "head matrix 248320x5120, dequantised, inverse transform D*(H*e)/32",
+                           kind="embed"),
 }
 
 EMBED_COUNT = 64     # gathered embedding rows for the embedding workload (seed 4, head matrix)

@@ -107,6 +107,15 @@ def test_host_errors():
     assert st == 4
 
 
+def test_wait_limit_setting():
+    """The wait-bound hook rejects a negative bound and accepts 0 and the default."""
+    with pytest.raises(nt.NinferError) as e:
+        nt.ninfer_set_wait_limit(-1)
+    assert e.value.status == 1
+    nt.ninfer_set_wait_limit(0)
+    nt.ninfer_set_wait_limit(nt.WAIT_LIMIT_DEFAULT)
+
+
 def test_device_entry_points_validate_before_launch():
     """Invalid arguments return a status without touching the device (so this
     runs without a GPU). Fake, aligned addresses stand in for device buffers."""

@@ -190,33 +190,52 @@ def test_matmul_down_full(M):
 
 @pytest.fixture(scope="module")
 def head_case():
+    """The output-head matrix (248320 x 5120, seed 4) with 8 activation rows and
+    64 token ids; its payload is packed per format on first use (PQ2_0:
+    337,715,200 bytes; PTQ1_0: 278,118,400 bytes), one format on the device at
+    a time."""
     c = synth.make_case("head", M=8, with_ids=True)
-    payload = dev_u8(nt.ninfer_ternary_pack("PQ2_0_G128", c.values, c.scales))
+    cache = {}
+
+    def payload(fmt):
+        if fmt not in cache:
+            cache.clear()
+            torch.cuda.empty_cache()
+            cache[fmt] = dev_u8(nt.ninfer_ternary_pack(fmt, c.values, c.scales))
+        return cache[fmt]
     return c, payload
 
 
+HEAD_FORMATS = ["PQ2_0_G128", "PTQ1_0_G128"]
+
+
 @pytest.mark.slow
+@pytest.mark.parametrize("fmt", HEAD_FORMATS)
 @pytest.mark.parametrize("M", [1, 8])
-def test_matmul_head_sampled(head_case, M):
+def test_matmul_head_sampled(head_case, fmt, M):
+    """The head shape in both formats: over 1,600 rows per CTA at M = 1 (PQ2_0 and
+    PTQ1_0 rings refilled many times per CTA), sampled rows (the first, the
+    last, 3,000 random) against the oracle, which packs exactly those rows."""
     c, payload = head_case
     sub = synth.Case(c.workload, c.values, c.scales, c.signs, c.x[:M], c.x_raw[:M])
-    y = run_matmul("PQ2_0_G128", sub, payload_dev=payload)
+    y = run_matmul(fmt, sub, payload_dev=payload(fmt))
     rng = np.random.default_rng(123)
     rows = np.unique(np.concatenate([[0, 1, c.workload.n - 1], rng.integers(0, c.workload.n, 3000)]))
-    ref = oracle_matmul_rows("PQ2_0_G128", sub, rows)
+    ref = oracle_matmul_rows(fmt, sub, rows)
     check_decode(y[:, rows], ref)
     assert np.all(np.isfinite(y))
 
 
 @pytest.mark.slow
-def test_embed_head_rows(head_case):
+@pytest.mark.parametrize("fmt", HEAD_FORMATS)
+def test_embed_head_rows(head_case, fmt):
     c, payload = head_case
     n, k = c.values.shape
     ids = torch.from_numpy(c.ids).to(DEV)
-    out = nt.ninfer_ternary_embed("PQ2_0_G128", payload, n, k, ids, dev_signs(c.signs))
+    out = nt.ninfer_ternary_embed(fmt, payload(fmt), n, k, ids, dev_signs(c.signs))
     torch.cuda.synchronize()
-    sub = oracle.pack_planes("PQ2_0_G128", c.values[c.ids], c.scales[c.ids])
-    ref = oracle.embed_rows("PQ2_0_G128", sub, c.ids.size, k, np.arange(c.ids.size), signs_values(c))
+    sub = oracle.pack_planes(fmt, c.values[c.ids], c.scales[c.ids])
+    ref = oracle.embed_rows(fmt, sub, c.ids.size, k, np.arange(c.ids.size), signs_values(c))
     check_decode(out.cpu().numpy(), ref)
 
 
@@ -332,6 +351,31 @@ def test_embed_unrotated():
 
 def test_no_device_errors_after_suite():
     torch.cuda.synchronize()
+    assert nt.ninfer_device_errors(clear=True) == 0
+
+
+@pytest.mark.parametrize("n,k", [(600, 5120), (3000, 16384)])
+def test_bounded_wait_failure_path(n, k):
+    """A weight-ring wait that gives up: with the bound set to 0 every wait of
+    the PQ2_0 M = 1 kernel gives up at its first check, although the copies
+    land normally. The call still returns OK and sets bit 0 of the device error
+    word (the call's output is not meaningful); the CTAs let their issued
+    copies land before exiting, so the context stays usable: the next call
+    with the default bound matches the oracle and leaves the word clear. The
+    second shape refills the ring (more chunks per CTA than slots)."""
+    c = synth.make_case("gateup", n=n, k=k, M=1, seed=n + k)
+    payload = dev_u8(nt.ninfer_ternary_pack("PQ2_0_G128", c.values, c.scales))
+    torch.cuda.synchronize()
+    assert nt.ninfer_device_errors(clear=True) == 0
+    try:
+        nt.ninfer_set_wait_limit(0)
+        nt.ninfer_ternary_matmul("PQ2_0_G128", payload, n, k, dev_x(c), dev_signs(c.signs))
+        torch.cuda.synchronize()
+    finally:
+        nt.ninfer_set_wait_limit(nt.WAIT_LIMIT_DEFAULT)
+    assert nt.ninfer_device_errors(clear=True) & 1
+    y = run_matmul("PQ2_0_G128", c, payload_dev=payload)
+    check_decode(y, oracle_matmul_rows("PQ2_0_G128", c, np.arange(n)))
     assert nt.ninfer_device_errors(clear=True) == 0
 
 
