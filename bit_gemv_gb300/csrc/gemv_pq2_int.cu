@@ -61,7 +61,9 @@ constexpr uint32_t kChunkBytes = 2 * kBoxBytes + 16 * kRows;
 constexpr uint32_t kMaxSlots = 8;
 constexpr uint32_t kActGroupBytes = 256;                  // 16 operand entries per group
 constexpr uint32_t kBarX = 1;                             // named barrier: x has arrived
-constexpr uint32_t kRotScratchBytes = 4352;               // per rotating warp: 1048 floats / 1072 int16
+constexpr uint32_t kRotScratchBytes = 4352;               // per rotating pair: 1080 + 2 floats
+constexpr uint32_t kBarPair0 = 2;                         // named barriers 2.. : one per rotating pair
+constexpr uint32_t kMaxPairs = 7;                         // warps 0-13 (the producer, warp 15, never rotates)
 
 struct IntParams {
     CUtensorMap wmap_main, wmap_last;   // base rows: {row bytes, R rows, CTA} / last CTA {row bytes, rows}
@@ -75,7 +77,8 @@ struct IntParams {
     uint64_t n;
     uint32_t k, groups, nblk, nchunk, rows_per_cta;     // nchunk: chunks per tile and matrix, groups / 8
     int x_dtype, y_dtype;
-    uint32_t nslots, pre_issue, nrot;    // nrot: warps rotating at once (one scratch each)
+    uint32_t nslots, pre_issue, nrot;    // nrot: warp pairs rotating at once (one scratch each)
+    uint32_t nslots_inv;                 // floor(2^32 / nslots) + 1: item / nslots = umulhi(item, nslots_inv)
     uint32_t off_ring, off_act, off_rot, off_part, off_bar, off_cnt;
     uint32_t *err;
     long long wait_cycles;              // bound of each ring wait
@@ -106,14 +109,15 @@ __device__ __forceinline__ void issue_chunk(const IntParams &p, uint8_t *smem, u
     }
 }
 
-// Block b of x (and its signs) in the warp-held layout: v[8i + e] = element
-// 1024 b + 256 i + 8 lane + e; zero past k.
+// The two warps of a pair rotate one 1024-element block together; thread
+// t = lane + 32 wh of the pair. Layout A (the load layout): v[8i + r] = element
+// 512 i + 8 t + r (i < 2, r < 8). Zero past k.
 template <int kXType>
-__device__ __forceinline__ void load_block(const void *x, uint32_t k, uint32_t b, int lane, float (&v)[32]) {
+__device__ __forceinline__ void load_block2(const void *x, uint32_t k, uint32_t b, int t, float (&v)[16]) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < 2; ++i) {
         float u[8];
-        const uint64_t idx = (uint64_t)b * 1024 + 256 * i + 8 * lane;
+        const uint64_t idx = (uint64_t)b * 1024 + 512 * i + 8 * t;
         if (idx + 8 <= k) {
             load8(x, idx, kXType, u);
         } else {
@@ -125,115 +129,165 @@ __device__ __forceinline__ void load_block(const void *x, uint32_t k, uint32_t b
     }
 }
 
-__device__ __forceinline__ void load_block_signs(const uint16_t *s, uint32_t b, int lane, float (&d)[32]) {
+__device__ __forceinline__ void load_signs2(const uint16_t *s, uint32_t b, int t, float (&d)[16]) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < 2; ++i) {
         float u[8];
-        load_signs8(s, (uint64_t)b * 1024 + 256 * i + 8 * lane, u);
+        load_signs8(s, (uint64_t)b * 1024 + 512 * i + 8 * t, u);
 #pragma unroll
         for (int e = 0; e < 8; ++e) d[8 * i + e] = u[e];
     }
 }
 
-// Butterflies over register index bits 0-4 of the warp's 32 values (element
-// bits held in the registers).
-__device__ __forceinline__ void butterfly32(float (&v)[32]) {
-#pragma unroll
-    for (int bit = 0; bit < 5; ++bit)
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            if (j & (1 << bit)) continue;
-            const float a = v[j], c = v[j | (1 << bit)];
-            v[j] = a + c;
-            v[j | (1 << bit)] = a - c;
-        }
+__device__ __forceinline__ uint64_t f2pack(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
 }
 
-// Rotates block b (x in v, as load_block leaves it; signs in d unless rotate is
-// false) with one warp, rounds it to 16-bit fixed point and writes its operand
-// entries and group entries {2^-E / 64 (with the transform's 1/32), -64 * sum
-// of x16}. The element bits held in registers are first {0,1,2,8,9} (lane =
-// bits 3-7), then, after a transpose through the warp's scratch (fp32, element
-// e at e + 8 (e >> 8)), bits 3-7 (lane = {0,1,2,8,9}): every butterfly stage
-// runs in registers. The rounded values go back through the scratch (int16,
-// element e at e + 16 (e >> 8)) so that each lane again holds runs of eight
-// consecutive elements, which are exactly operand entries. scr: kRotScratchBytes.
-__device__ __forceinline__ void rotate_pack(bool rotate, float (&v)[32], const float (&d)[32], uint32_t b,
-                                            uint32_t groups, uint8_t *act, float *scr, int lane) {
+__device__ __forceinline__ void f2unpack(uint64_t r, float &a, float &b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+
+// Butterflies over the four register index bits of 16 values: bits 1-3 as
+// paired fp32 adds and subtracts (each element rounded exactly as by a scalar
+// add), bit 0 within the pairs.
+__device__ __forceinline__ void butterfly16(float (&v)[16]) {
+    uint64_t w[8];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) w[m] = f2pack(v[2 * m], v[2 * m + 1]);
+#pragma unroll
+    for (int bit = 0; bit < 3; ++bit)
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            if (m & (1 << bit)) continue;
+            uint64_t sum, dif;
+            asm("add.rn.f32x2 %0, %1, %2;" : "=l"(sum) : "l"(w[m]), "l"(w[m | (1 << bit)]));
+            asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(dif) : "l"(w[m]), "l"(w[m | (1 << bit)]));
+            w[m] = sum;
+            w[m | (1 << bit)] = dif;
+        }
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+        float a, c;
+        f2unpack(w[m], a, c);
+        v[2 * m] = a + c;
+        v[2 * m + 1] = a - c;
+    }
+}
+
+// Rotates block b with the pair (x in v as load_block2 leaves it; signs in d
+// unless rotate is false), rounds it to 16-bit fixed point and writes its
+// operand entries and group entries {2^-E / 64 (with the transform's 1/32),
+// -64 * sum of x16}. Stages: register butterflies on element bits {0,1,2,9}
+// (layout A); a transpose through the pair's scratch to layout B (lane =
+// element bits {0,1,2,7,8}, wh = bit 9, register j = bits 3-6:
+// e = (lane & 7) + 8 j + 128 (lane >> 3) + 512 wh) for register butterflies on
+// bits 3-6 and two shuffle stages on bits 7-8; a transpose back to layout A,
+// where each thread holds two runs of eight consecutive elements, i.e. two
+// operand entries. Scratch slot of element e: e + 8 (e >> 7); the pair's
+// maximum goes through floats 1080-1081. bar: the pair's named barrier.
+__device__ __forceinline__ void rotate_pack2(bool rotate, float (&v)[16], const float (&d)[16], uint32_t b,
+                                             uint32_t groups, uint8_t *act, float *scr, int t, uint32_t bar) {
+    const int lane = t & 31, wh = t >> 5;
     if (rotate) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] *= d[j];
-        butterfly32(v);      // element bits 0, 1, 2, 8, 9
+        for (int m = 0; m < 8; ++m) {
+            uint64_t r;
+            asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2pack(v[2 * m], v[2 * m + 1])),
+                "l"(f2pack(d[2 * m], d[2 * m + 1])));
+            f2unpack(r, v[2 * m], v[2 * m + 1]);
+        }
+        butterfly16(v);      // element bits 0, 1, 2, 9
     }
+    const int aA = 8 * t + 8 * (t >> 4);
+    const int aB = (lane & 7) + 136 * (lane >> 3) + 544 * wh;
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < 2; ++i)
 #pragma unroll
         for (int c = 0; c < 2; ++c)
-            *reinterpret_cast<float4 *>(scr + 264 * i + 8 * lane + 4 * c) =
+            *reinterpret_cast<float4 *>(scr + 544 * i + aA + 4 * c) =
                 make_float4(v[8 * i + 4 * c], v[8 * i + 4 * c + 1], v[8 * i + 4 * c + 2], v[8 * i + 4 * c + 3]);
-    __syncwarp();
-    // lane = element bits (0, 1, 2, 8, 9), register j = bits 3-7: e = (lane & 7) + 8 j + 256 (lane >> 3)
-    const int base = (lane & 7) + 264 * (lane >> 3);
+    named_barrier(bar, 64);
 #pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] = scr[base + 8 * j];
-    if (rotate) butterfly32(v);      // element bits 3-7: v = H (D x) = 32 xr
-    // block maximum (a tree, then across the lanes)
-    float m[16];
+    for (int j = 0; j < 16; ++j) v[j] = scr[aB + 8 * j];
+    if (rotate) {
+        butterfly16(v);      // element bits 3-6
+        // element bits 7 and 8 (lane bits 3 and 4): the lane whose bit is set keeps
+        // partner - own, the other own + partner (fmaf(+-1, own, partner): one rounding)
 #pragma unroll
-    for (int j = 0; j < 16; ++j) m[j] = fmaxf(fabsf(v[j]), fabsf(v[j + 16]));
+        for (int s = 8; s <= 16; s <<= 1) {
+            const float sg = (lane & s) ? -1.f : 1.f;
 #pragma unroll
-    for (int w = 8; w > 0; w >>= 1)
+            for (int j = 0; j < 16; ++j) v[j] = fmaf(sg, v[j], __shfl_xor_sync(0xffffffffu, v[j], s));
+        }
+    }
+    // each thread rewrites exactly the slots it read, so only the reads below wait
+#pragma unroll
+    for (int j = 0; j < 16; ++j) scr[aB + 8 * j] = v[j];
+    named_barrier(bar, 64);
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            const float4 q = *reinterpret_cast<const float4 *>(scr + 544 * i + aA + 4 * c);
+            v[8 * i + 4 * c] = q.x;
+            v[8 * i + 4 * c + 1] = q.y;
+            v[8 * i + 4 * c + 2] = q.z;
+            v[8 * i + 4 * c + 3] = q.w;
+        }
+    // block maximum: a tree in registers, the warp, then the pair
+    float m[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) m[j] = fmaxf(fabsf(v[j]), fabsf(v[j + 8]));
+#pragma unroll
+    for (int w = 4; w > 0; w >>= 1)
 #pragma unroll
         for (int j = 0; j < w; ++j) m[j] = fmaxf(m[j], m[j + w]);
-    float mx = m[0];
-#pragma unroll
-    for (int s = 16; s > 0; s >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, s));
+    // (a non-negative float's bits order as its value: one warp-wide integer max)
+    float mx = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(m[0])));
+    if (lane == 0) scr[1080 + wh] = mx;
+    named_barrier(bar, 64);
+    mx = fmaxf(scr[1080], scr[1081]);
     int E = 0;
     if (mx > 0.f) E = 13 - ilogbf(mx);     // max |x16| < 2^14
     E = max(-100, min(100, E));
     const float up = ldexpf(1.f, E);
     const float f = ldexpf(1.f, -E - 6 - (rotate ? 5 : 0));
-    __syncwarp();        // every lane has read its transposed values
-    // quantise: x16 = rint(v * 2^E) (adding 1.5 * 2^23 rounds to nearest, ties to even);
-    // group (element bits 7-9) sums, bit 7 = j >> 4, bits 8-9 = lane >> 3
-    int16_t *qs = reinterpret_cast<int16_t *>(scr);
-    const int qbase = (lane & 7) + 272 * (lane >> 3);
-    int gsum[2][2] = {{0, 0}, {0, 0}};
+    // x16 = rint(v * 2^E): fma(v, 2^E, 1.5 * 2^23) rounds to nearest (ties to even)
+    // and leaves x16 in the low 16 bits; the bits minus 0x4B400000 are x16
+    uint32_t qb[16];
+    const uint64_t up2 = f2pack(up, up), mg = f2pack(12582912.0f, 12582912.0f);
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-        const int q = __float_as_int(fmaf(v[j], up, 12582912.0f)) - 0x4B400000;
-        gsum[j >> 4][j & 1] += q;
-        qs[qbase + 8 * j] = (int16_t)q;
+    for (int m2 = 0; m2 < 8; ++m2) {
+        uint64_t r;
+        asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(f2pack(v[2 * m2], v[2 * m2 + 1])), "l"(up2), "l"(mg));
+        float a, c;
+        f2unpack(r, a, c);
+        qb[2 * m2] = __float_as_uint(a);
+        qb[2 * m2 + 1] = __float_as_uint(c);
     }
-    int gs2[2] = {gsum[0][0] + gsum[0][1], gsum[1][0] + gsum[1][1]};
-#pragma unroll
-    for (int h = 0; h < 2; ++h)
-#pragma unroll
-        for (int s = 1; s < 8; s <<= 1) gs2[h] += __shfl_xor_sync(0xffffffffu, gs2[h], s);
-    float2 *gs = reinterpret_cast<float2 *>(act + (uint64_t)groups * kActGroupBytes);
-    if ((lane & 7) == 0) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const uint32_t G = b * 8 + 2 * (lane >> 3) + h;
-            if (G < groups) gs[G] = make_float2(f, __int_as_float(-64 * gs2[h]));
-        }
-    }
-    __syncwarp();
-    // element 1024 b + 256 i + 8 lane + r (r < 8): entry (lane % 2) of word (lane / 2) of
-    // the 16 words starting at block word 16 i
     uint4 *ent = reinterpret_cast<uint4 *>(act);
+    float2 *gs = reinterpret_cast<float2 *>(act + (uint64_t)groups * kActGroupBytes);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const uint4 raw = *reinterpret_cast<const uint4 *>(qs + 272 * i + 8 * lane);
-        const uint32_t G = b * 8 + 2 * i + (lane >> 4);
-        uint4 en;     // (x16[p], x16[4 + p]), p = 0..3
-        en.x = __byte_perm(raw.x, raw.z, 0x5410);
-        en.y = __byte_perm(raw.x, raw.z, 0x7632);
-        en.z = __byte_perm(raw.y, raw.w, 0x5410);
-        en.w = __byte_perm(raw.y, raw.w, 0x7632);
-        if (G < groups) ent[(uint64_t)b * 128 + 32 * i + lane] = en;
+    for (int i = 0; i < 2; ++i) {
+        // the run of elements 512 i + 8 t .. + 7: entry (t % 2) of word 32 i + t / 2 of the block,
+        // group 4 i + t / 16 of the block; entry = {(x16[p], x16[4 + p]), p = 0..3}
+        const uint32_t *q = qb + 8 * i;
+        const uint32_t G = b * 8 + 4 * i + (t >> 4);
+        uint4 en;
+        en.x = __byte_perm(q[0], q[4], 0x5410);
+        en.y = __byte_perm(q[1], q[5], 0x5410);
+        en.z = __byte_perm(q[2], q[6], 0x5410);
+        en.w = __byte_perm(q[3], q[7], 0x5410);
+        if (G < groups) ent[(uint64_t)b * 128 + 64 * i + t] = en;
+        // the group's sum of x16: the 16 lanes of each half-warp, one warp-wide add per half
+        const int sum = (int)(q[0] + q[1] + q[2] + q[3] + q[4] + q[5] + q[6] + q[7] - 8u * 0x4B400000u);
+        const int s_lo = __reduce_add_sync(0xffffffffu, lane < 16 ? sum : 0);
+        const int s_hi = __reduce_add_sync(0xffffffffu, lane < 16 ? 0 : sum);
+        if ((lane & 15) == 0 && G < groups) gs[G] = make_float2(f, __int_as_float(-64 * (lane < 16 ? s_lo : s_hi)));
     }
-    __syncwarp();        // the scratch may be reused
+    named_barrier(bar, 64);      // the scratch may be reused
 }
 
 // kMats = 1: y = W x. kMats = 2 (fused FFN gate/up): y = silu(Wg x_g) * (Wu x_u)
@@ -253,23 +307,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_pq2_int_kernel(const __grid_
     uint32_t *cnt = reinterpret_cast<uint32_t *>(smem + p.off_cnt);
     uint32_t *issued = cnt + kMaxSlots, *failed = cnt + kMaxSlots + 1;
     // rotation tasks (matrix, block): one rotation per block, or two when the
-    // fused matrices have different signs; rotating warp w takes tasks w, w + nrot, ...
+    // fused matrices have different signs
     const uint32_t nrmat = (kMats == 2 && p.signs2 != p.signs) ? 2 : 1;
     const uint32_t ntask = nrmat * p.nblk;
     // the ring is issued by the last warp, which never rotates
     const int producer = kWarps - 1;
     const uint32_t ring_to = p.nslots < nitems ? p.nslots : nitems;
     const uint32_t pre = p.pre_issue < ring_to ? p.pre_issue : ring_to;
-    const uint32_t nrot = ntask < p.nrot ? ntask : p.nrot;     // at most 15: the producer never rotates
-    const bool rotating = (uint32_t)warp < nrot;
-    // Up to four idle warps (one per SM sub-partition) run the rotation of the
-    // first block once, before the dependency wait, with the same instructions
-    // as the rotating warps (x read early, results into scratch and discarded):
-    // every line of that code, executed once per launch, is then already in the
-    // instruction caches when x arrives.
-    const uint32_t nwarm = (uint32_t)producer - nrot < 4 ? (uint32_t)producer - nrot : 4;
-    const bool warm = !rotating && (uint32_t)warp < nrot + nwarm;
-    const uint32_t nwait = 32 * (nrot + nwarm + 1);
+    // warp pairs rotate blocks: rotating pair pr takes tasks pr, pr + npr, ...
+    const uint32_t npr = ntask < p.nrot ? ntask : p.nrot;       // rotating pairs, at most kMaxPairs
+    const uint32_t pr = (uint32_t)warp >> 1;
+    const int t = tid & 63;
+    const bool rotating = pr < npr;
+    const uint32_t nwait = 32 * (2 * npr + 1);
 
     if (tid == producer * 32) {
         prefetch_tmap(last_cta ? &p.wmap_last : &p.wmap_main);
@@ -289,23 +339,23 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_pq2_int_kernel(const __grid_
         *issued = pre;
     }
     uint8_t *act_s = smem + p.off_act;
-    float v[32], d[32];
-    if (rotating || warm) {
-        // the first rotation of a rotating warp, or the warm-up pass: one code path
-        const uint32_t task = rotating ? (uint32_t)warp : 0;
+    float v[16], d[16];
+    if (rotating) {
+        // the first rotation of a rotating pair
+        const uint32_t task = pr;
         const uint32_t b = task % p.nblk;
-        float *scr = reinterpret_cast<float *>(smem + (rotating ? p.off_rot + warp * kRotScratchBytes : p.off_part));
-        if (p.signs) load_block_signs(task >= p.nblk ? p.signs2 : p.signs, b, lane, d);     // read-only
+        float *scr = reinterpret_cast<float *>(smem + p.off_rot + pr * kRotScratchBytes);
+        if (p.signs) load_signs2(task >= p.nblk ? p.signs2 : p.signs, b, t, d);     // read-only
         pdl_launch_dependents();
-        if (rotating) pdl_wait();        // x may come from the preceding kernel
-        load_block<kXType>(p.x, p.k, b, lane, v);
-        // x has arrived once its first and last values can be stored; then the
-        // producer may queue the rest of the ring behind it
-        *reinterpret_cast<volatile float *>(scr) = v[0] + v[31];
+        pdl_wait();          // x may come from the preceding kernel
+        load_block2<kXType>(p.x, p.k, b, t, v);
+        // x has arrived once its first and last values can be stored (in the
+        // pair's maximum slot, written again later); then the producer may
+        // queue the rest of the ring behind it
+        *reinterpret_cast<volatile float *>(scr + 1080 + (t >> 5)) = v[0] + v[15];
         named_barrier_arrive(kBarX, nwait);
-        rotate_pack(p.signs != nullptr, v, d, b, rotating ? p.groups : 8,
-                    rotating ? act_s + (task / p.nblk) * p.act_bytes : smem + p.off_part, scr, lane);
-        if (warm) pdl_wait();
+        rotate_pack2(p.signs != nullptr, v, d, b, p.groups, act_s + (task / p.nblk) * p.act_bytes, scr, t,
+                     kBarPair0 + pr);
     } else {
         pdl_launch_dependents();
         pdl_wait();
@@ -320,14 +370,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_pq2_int_kernel(const __grid_
             __syncwarp();
         }
     }
-    // more rotations than rotating warps: further rounds
+    // more rotations than rotating pairs: further rounds
 #pragma unroll 1
-    for (uint32_t task = warp + nrot; rotating && task < ntask; task += nrot) {
+    for (uint32_t task = pr + npr; rotating && task < ntask; task += npr) {
         const uint32_t b = task % p.nblk;
-        if (p.signs) load_block_signs(task >= p.nblk ? p.signs2 : p.signs, b, lane, d);
-        load_block<kXType>(p.x, p.k, b, lane, v);
-        rotate_pack(p.signs != nullptr, v, d, b, p.groups, act_s + (task / p.nblk) * p.act_bytes,
-                    reinterpret_cast<float *>(smem + p.off_rot + warp * kRotScratchBytes), lane);
+        if (p.signs) load_signs2(task >= p.nblk ? p.signs2 : p.signs, b, t, d);
+        load_block2<kXType>(p.x, p.k, b, t, v);
+        rotate_pack2(p.signs != nullptr, v, d, b, p.groups, act_s + (task / p.nblk) * p.act_bytes,
+                     reinterpret_cast<float *>(smem + p.off_rot + pr * kRotScratchBytes), t, kBarPair0 + pr);
     }
     // (the ring's barriers and counters, set up by the producer, are first used
     // after the barrier that completes the activation table)
@@ -354,7 +404,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_pq2_int_kernel(const __grid_
             const bool full = 2 * r + 1 < per_tile;
             const uint32_t jj = full ? 2 * r + upper : 2 * r;
             const uint32_t item = tile * per_tile + jj;
-            const uint32_t slot = item % p.nslots, phase = (item / p.nslots) & 1;
+            const uint32_t cycle = __umulhi(item, p.nslots_inv);      // item / nslots (item < 2^29)
+            const uint32_t slot = item - cycle * p.nslots, phase = cycle & 1;
             const uint32_t mat = kMats == 1 ? 0 : (jj >= p.nchunk), j = jj - mat * p.nchunk;
             const uint8_t *act_m = act_s + (mat < nrmat ? mat : 0) * p.act_bytes;
             const float2 *gs = reinterpret_cast<const float2 *>(act_m + (uint64_t)p.groups * kActGroupBytes);
@@ -487,16 +538,18 @@ bool gemv_pq2_int_plan(const ninfer_row_split_geometry &g, uint64_t M, bool rota
     if (g.scale_row_bytes % 16 || g.base_row_bytes % 16 || g.payload_bytes % 16) return false;
     if (g.k > (1u << 24) || g.n > (1ull << 31)) return false;
     const uint32_t groups = (uint32_t)g.groups_per_row;
+    // chunk indices per CTA stay below 2^29 (the ring's slot arithmetic)
+    if ((uint64_t)mats * (groups / 8) * ((g.n + 127) / 128) >= (1ull << 29)) return false;
     const uint32_t act_one = ((groups * (kActGroupBytes + 8) + 15) / 16) * 16;
     const uint32_t nrmat = (mats == 2 && two_rotations) ? 2 : 1;
     const uint32_t act_bytes = nrmat * act_one;
     const uint32_t part_bytes = mats * kWarps * kRows * 4;     // per-warp row sums of a tile (>= one scratch)
     const uint32_t bar_bytes = kMaxSlots * 8;
     const uint32_t cnt_bytes = (kMaxSlots + 4) * 4;
-    // warps rotating at once, each with its own scratch: as many as there are
-    // rotations (at most 16) while the ring keeps at least four slots
+    // warp pairs rotating at once, each with its own scratch: as many as there
+    // are rotations (at most kMaxPairs) while the ring keeps at least four slots
     const uint32_t ntask = nrmat * (uint32_t)((g.k + 1023) / 1024);
-    uint32_t nrot = std::min<uint32_t>(ntask, (uint32_t)kWarps - 1);     // the producer warp never rotates
+    uint32_t nrot = std::min<uint32_t>(ntask, kMaxPairs);     // rotating warp pairs
     auto fixed_of = [&](uint32_t nr) { return act_bytes + nr * kRotScratchBytes + part_bytes + bar_bytes + cnt_bytes; };
     while (nrot > 1 && (int)fixed_of(nrot) + 4 * (int)kChunkBytes > smem_limit) nrot = (nrot + 1) / 2;
     const uint32_t fixed = fixed_of(nrot);
@@ -546,6 +599,7 @@ int gemv_pq2_int_launch(const IntPlan &plan, const uint8_t *payload, const ninfe
     p.x_dtype = x_dtype;
     p.y_dtype = y_dtype;
     p.nslots = plan.nslots;
+    p.nslots_inv = (uint32_t)((1ull << 32) / plan.nslots + 1);
     p.pre_issue = plan.pre_issue;
     p.off_ring = plan.off_ring;
     p.off_act = plan.off_act;
