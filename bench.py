@@ -483,11 +483,11 @@ def tensor_roofline(M, n, k, s_step, traffic):
 
 def kernels_per_step(w) -> int:
     """Kernels one projection launches: the M = 1 decode kernels rotate x
-    themselves (PTQ1_0 with k > 8192 also runs its prep kernel); the PTQ1_0
-    M <= 8 kernel rotates x itself and, with more than one 1024-block, is
-    followed by the block reduction; the PQ2_0 M <= 8, prefill and general
-    paths run a prep or transform kernel and then the main one. The fused
-    gate/up pair at PQ2_0, M = 1 is one kernel, and so is the embedding."""
+    themselves (one kernel, whatever k); the PTQ1_0 M <= 8 kernel rotates x
+    itself and, with more than one 1024-block, is followed by the block
+    reduction; the PQ2_0 M <= 8, prefill and general paths run a prep or
+    transform kernel and then the main one. The fused gate/up pair at PQ2_0,
+    M = 1 is one kernel, and so is the embedding."""
     if w.kind == "embed":
         return 1
     if w.mats == 2 and w.fmt == "PQ2_0_G128" and w.M == 1:
@@ -496,7 +496,7 @@ def kernels_per_step(w) -> int:
         import dataclasses
         return 2 * kernels_per_step(dataclasses.replace(w, mats=1)) + 1
     if w.M == 1:
-        return 2 if (w.fmt == "PTQ1_0_G128" and w.k > 8192) else 1
+        return 1
     if w.fmt == "PTQ1_0_G128" and w.M <= 8:
         return 2 if w.k > 1024 else 1
     if w.fmt == "PTQ1_0_G128":

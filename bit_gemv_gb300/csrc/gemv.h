@@ -49,7 +49,8 @@ struct IntPlan {
     bool ok;
     int mats;
     uint32_t act_one;
-    uint32_t grid, rows_per_cta, nitem, nslots, pre_issue, nrot;
+    uint32_t grid, grid_rows, rows_per_cta, nitem, nslots, pre_issue, nrot;
+    bool cluster;                // CTA pairs share the rotations (grid even)
     uint32_t off_ring, off_act, off_rot, off_part, off_bar, off_cnt, smem;
     uint64_t workspace;
 };
@@ -63,9 +64,10 @@ int gemv_pq2_int_launch(const IntPlan &plan, const uint8_t *payload, const ninfe
 // M = 1 integer kernel (PTQ1_0_G128), rotation fused in.
 struct Ptq1Plan {
     bool ok;
-    uint32_t grid, rows_per_cta, nch, nslots, pre_issue;
-    uint32_t off_ring, off_lut, off_act, off_rot, off_rem, off_part, off_bar, off_cnt, smem;
-    bool split;              // operand words from a separate prep kernel (wide x)
+    int rl;                  // rows per lane: 4 for large row ranges, else 1
+    bool cluster;            // CTA pairs share the rotations (grid even)
+    uint32_t grid, grid_rows, rows_per_cta, nch, nslots, pre_issue, nrot;
+    uint32_t off_ring, off_act, off_rem, off_part, off_bar, off_cnt, smem;
     uint32_t act_bytes;
     uint64_t workspace;
 };

@@ -49,6 +49,7 @@
 #include "common.h"
 #include "device.cuh"
 #include "gemv.h"
+#include "rot2.cuh"
 
 namespace ninfer {
 namespace {
@@ -61,7 +62,6 @@ constexpr uint32_t kChunkBytes = 2 * kBoxBytes + 16 * kRows;
 constexpr uint32_t kMaxSlots = 8;
 constexpr uint32_t kActGroupBytes = 256;                  // 16 operand entries per group
 constexpr uint32_t kBarX = 1;                             // named barrier: x has arrived
-constexpr uint32_t kRotScratchBytes = 4352;               // per rotating pair: 1080 + 2 floats
 constexpr uint32_t kBarPair0 = 2;                         // named barriers 2.. : one per rotating pair
 constexpr uint32_t kMaxPairs = 7;                         // warps 0-13 (the producer, warp 15, never rotates)
 
@@ -79,6 +79,7 @@ struct IntParams {
     int x_dtype, y_dtype;
     uint32_t nslots, pre_issue, nrot;    // nrot: warp pairs rotating at once (one scratch each)
     uint32_t nslots_inv;                 // floor(2^32 / nslots) + 1: item / nslots = umulhi(item, nslots_inv)
+    uint32_t grid_rows;                  // CTAs with rows (the grid may have one more, for pairs)
     uint32_t off_ring, off_act, off_rot, off_part, off_bar, off_cnt;
     uint32_t *err;
     long long wait_cycles;              // bound of each ring wait
@@ -109,164 +110,17 @@ __device__ __forceinline__ void issue_chunk(const IntParams &p, uint8_t *smem, u
     }
 }
 
-// The two warps of a pair rotate one 1024-element block together; thread
-// t = lane + 32 wh of the pair. Layout A (the load layout): v[8i + r] = element
-// 512 i + 8 t + r (i < 2, r < 8). Zero past k.
-template <int kXType>
-__device__ __forceinline__ void load_block2(const void *x, uint32_t k, uint32_t b, int t, float (&v)[16]) {
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        float u[8];
-        const uint64_t idx = (uint64_t)b * 1024 + 512 * i + 8 * t;
-        if (idx + 8 <= k) {
-            load8(x, idx, kXType, u);
-        } else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) u[e] = idx + e < k ? load1(x, idx + e, kXType) : 0.f;
-        }
-#pragma unroll
-        for (int e = 0; e < 8; ++e) v[8 * i + e] = u[e];
-    }
-}
-
-__device__ __forceinline__ void load_signs2(const uint16_t *s, uint32_t b, int t, float (&d)[16]) {
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        float u[8];
-        load_signs8(s, (uint64_t)b * 1024 + 512 * i + 8 * t, u);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) d[8 * i + e] = u[e];
-    }
-}
-
-__device__ __forceinline__ uint64_t f2pack(float a, float b) {
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
-    return r;
-}
-
-__device__ __forceinline__ void f2unpack(uint64_t r, float &a, float &b) {
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
-}
-
-// Butterflies over the four register index bits of 16 values: bits 1-3 as
-// paired fp32 adds and subtracts (each element rounded exactly as by a scalar
-// add), bit 0 within the pairs.
-__device__ __forceinline__ void butterfly16(float (&v)[16]) {
-    uint64_t w[8];
-#pragma unroll
-    for (int m = 0; m < 8; ++m) w[m] = f2pack(v[2 * m], v[2 * m + 1]);
-#pragma unroll
-    for (int bit = 0; bit < 3; ++bit)
-#pragma unroll
-        for (int m = 0; m < 8; ++m) {
-            if (m & (1 << bit)) continue;
-            uint64_t sum, dif;
-            asm("add.rn.f32x2 %0, %1, %2;" : "=l"(sum) : "l"(w[m]), "l"(w[m | (1 << bit)]));
-            asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(dif) : "l"(w[m]), "l"(w[m | (1 << bit)]));
-            w[m] = sum;
-            w[m | (1 << bit)] = dif;
-        }
-#pragma unroll
-    for (int m = 0; m < 8; ++m) {
-        float a, c;
-        f2unpack(w[m], a, c);
-        v[2 * m] = a + c;
-        v[2 * m + 1] = a - c;
-    }
-}
-
-// Rotates block b with the pair (x in v as load_block2 leaves it; signs in d
-// unless rotate is false), rounds it to 16-bit fixed point and writes its
-// operand entries and group entries {2^-E / 64 (with the transform's 1/32),
-// -64 * sum of x16}. Stages: register butterflies on element bits {0,1,2,9}
-// (layout A); a transpose through the pair's scratch to layout B (lane =
-// element bits {0,1,2,7,8}, wh = bit 9, register j = bits 3-6:
-// e = (lane & 7) + 8 j + 128 (lane >> 3) + 512 wh) for register butterflies on
-// bits 3-6 and two shuffle stages on bits 7-8; a transpose back to layout A,
-// where each thread holds two runs of eight consecutive elements, i.e. two
-// operand entries. Scratch slot of element e: e + 8 (e >> 7); the pair's
-// maximum goes through floats 1080-1081. bar: the pair's named barrier.
+// Rotates block b with the pair (rotate_quant2) and writes its operand entries
+// and group entries {2^-E / 64 (with the transform's 1/32), -64 * sum of x16}
+// into act and, when act_remote is non-zero (the cluster address of the same
+// table in the other CTA of the cluster), into that table too.
 __device__ __forceinline__ void rotate_pack2(bool rotate, float (&v)[16], const float (&d)[16], uint32_t b,
-                                             uint32_t groups, uint8_t *act, float *scr, int t, uint32_t bar) {
-    const int lane = t & 31, wh = t >> 5;
-    if (rotate) {
-#pragma unroll
-        for (int m = 0; m < 8; ++m) {
-            uint64_t r;
-            asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2pack(v[2 * m], v[2 * m + 1])),
-                "l"(f2pack(d[2 * m], d[2 * m + 1])));
-            f2unpack(r, v[2 * m], v[2 * m + 1]);
-        }
-        butterfly16(v);      // element bits 0, 1, 2, 9
-    }
-    const int aA = 8 * t + 8 * (t >> 4);
-    const int aB = (lane & 7) + 136 * (lane >> 3) + 544 * wh;
-#pragma unroll
-    for (int i = 0; i < 2; ++i)
-#pragma unroll
-        for (int c = 0; c < 2; ++c)
-            *reinterpret_cast<float4 *>(scr + 544 * i + aA + 4 * c) =
-                make_float4(v[8 * i + 4 * c], v[8 * i + 4 * c + 1], v[8 * i + 4 * c + 2], v[8 * i + 4 * c + 3]);
-    named_barrier(bar, 64);
-#pragma unroll
-    for (int j = 0; j < 16; ++j) v[j] = scr[aB + 8 * j];
-    if (rotate) {
-        butterfly16(v);      // element bits 3-6
-        // element bits 7 and 8 (lane bits 3 and 4): the lane whose bit is set keeps
-        // partner - own, the other own + partner (fmaf(+-1, own, partner): one rounding)
-#pragma unroll
-        for (int s = 8; s <= 16; s <<= 1) {
-            const float sg = (lane & s) ? -1.f : 1.f;
-#pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] = fmaf(sg, v[j], __shfl_xor_sync(0xffffffffu, v[j], s));
-        }
-    }
-    // each thread rewrites exactly the slots it read, so only the reads below wait
-#pragma unroll
-    for (int j = 0; j < 16; ++j) scr[aB + 8 * j] = v[j];
-    named_barrier(bar, 64);
-#pragma unroll
-    for (int i = 0; i < 2; ++i)
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-            const float4 q = *reinterpret_cast<const float4 *>(scr + 544 * i + aA + 4 * c);
-            v[8 * i + 4 * c] = q.x;
-            v[8 * i + 4 * c + 1] = q.y;
-            v[8 * i + 4 * c + 2] = q.z;
-            v[8 * i + 4 * c + 3] = q.w;
-        }
-    // block maximum: a tree in registers, the warp, then the pair
-    float m[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) m[j] = fmaxf(fabsf(v[j]), fabsf(v[j + 8]));
-#pragma unroll
-    for (int w = 4; w > 0; w >>= 1)
-#pragma unroll
-        for (int j = 0; j < w; ++j) m[j] = fmaxf(m[j], m[j + w]);
-    // (a non-negative float's bits order as its value: one warp-wide integer max)
-    float mx = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(m[0])));
-    if (lane == 0) scr[1080 + wh] = mx;
-    named_barrier(bar, 64);
-    mx = fmaxf(scr[1080], scr[1081]);
-    int E = 0;
-    if (mx > 0.f) E = 13 - ilogbf(mx);     // max |x16| < 2^14
-    E = max(-100, min(100, E));
-    const float up = ldexpf(1.f, E);
-    const float f = ldexpf(1.f, -E - 6 - (rotate ? 5 : 0));
-    // x16 = rint(v * 2^E): fma(v, 2^E, 1.5 * 2^23) rounds to nearest (ties to even)
-    // and leaves x16 in the low 16 bits; the bits minus 0x4B400000 are x16
+                                             uint32_t groups, uint8_t *act, uint32_t act_remote, float *scr, int t,
+                                             uint32_t bar) {
+    const int lane = t & 31;
     uint32_t qb[16];
-    const uint64_t up2 = f2pack(up, up), mg = f2pack(12582912.0f, 12582912.0f);
-#pragma unroll
-    for (int m2 = 0; m2 < 8; ++m2) {
-        uint64_t r;
-        asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(f2pack(v[2 * m2], v[2 * m2 + 1])), "l"(up2), "l"(mg));
-        float a, c;
-        f2unpack(r, a, c);
-        qb[2 * m2] = __float_as_uint(a);
-        qb[2 * m2 + 1] = __float_as_uint(c);
-    }
+    const int E = rotate_quant2(rotate, v, d, scr, t, bar, qb);
+    const float f = ldexpf(1.f, -E - 6 - (rotate ? 5 : 0));
     uint4 *ent = reinterpret_cast<uint4 *>(act);
     float2 *gs = reinterpret_cast<float2 *>(act + (uint64_t)groups * kActGroupBytes);
 #pragma unroll
@@ -280,14 +134,20 @@ __device__ __forceinline__ void rotate_pack2(bool rotate, float (&v)[16], const 
         en.y = __byte_perm(q[1], q[5], 0x5410);
         en.z = __byte_perm(q[2], q[6], 0x5410);
         en.w = __byte_perm(q[3], q[7], 0x5410);
-        if (G < groups) ent[(uint64_t)b * 128 + 64 * i + t] = en;
+        if (G < groups) {
+            ent[(uint64_t)b * 128 + 64 * i + t] = en;
+            if (act_remote) st_cluster_v4(act_remote + (b * 128 + 64 * i + t) * 16, en);
+        }
         // the group's sum of x16: the 16 lanes of each half-warp, one warp-wide add per half
         const int sum = (int)(q[0] + q[1] + q[2] + q[3] + q[4] + q[5] + q[6] + q[7] - 8u * 0x4B400000u);
         const int s_lo = __reduce_add_sync(0xffffffffu, lane < 16 ? sum : 0);
         const int s_hi = __reduce_add_sync(0xffffffffu, lane < 16 ? 0 : sum);
-        if ((lane & 15) == 0 && G < groups) gs[G] = make_float2(f, __int_as_float(-64 * (lane < 16 ? s_lo : s_hi)));
+        if ((lane & 15) == 0 && G < groups) {
+            const int off = -64 * (lane < 16 ? s_lo : s_hi);
+            gs[G] = make_float2(f, __int_as_float(off));
+            if (act_remote) st_cluster_v2(act_remote + groups * kActGroupBytes + 8 * G, __float_as_uint(f), (uint32_t)off);
+        }
     }
-    named_barrier(bar, 64);      // the scratch may be reused
 }
 
 // kMats = 1: y = W x. kMats = 2 (fused FFN gate/up): y = silu(Wg x_g) * (Wu x_u)
@@ -299,17 +159,22 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_pq2_int_kernel(const __grid_
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint64_t r_begin = (uint64_t)blockIdx.x * p.rows_per_cta;
     const uint64_t r_end = r_begin + p.rows_per_cta < p.n ? r_begin + p.rows_per_cta : p.n;
-    const bool last_cta = blockIdx.x == gridDim.x - 1;
+    const bool last_cta = blockIdx.x == p.grid_rows - 1;     // the last CTA with rows (an even grid may add one)
     const uint32_t per_tile = kMats * p.nchunk;
-    const uint32_t ntile = (uint32_t)((r_end - r_begin + kRows - 1) / kRows);
+    const uint32_t ntile = r_end > r_begin ? (uint32_t)((r_end - r_begin + kRows - 1) / kRows) : 0;
     const uint32_t nitems = ntile * per_tile;
     const uint32_t bar0 = smem_u32(smem + p.off_bar);
     uint32_t *cnt = reinterpret_cast<uint32_t *>(smem + p.off_cnt);
     uint32_t *issued = cnt + kMaxSlots, *failed = cnt + kMaxSlots + 1;
     // rotation tasks (matrix, block): one rotation per block, or two when the
-    // fused matrices have different signs
+    // fused matrices have different signs. In a cluster of two CTAs each takes
+    // every other task (local task i is task 2 i + rank) and writes the result
+    // into both CTAs' tables.
     const uint32_t nrmat = (kMats == 2 && p.signs2 != p.signs) ? 2 : 1;
-    const uint32_t ntask = nrmat * p.nblk;
+    const uint32_t ntask_all = nrmat * p.nblk;
+    const uint32_t csize = cluster_nctarank(), crank = cluster_ctarank();
+    const uint32_t ntask = csize == 2 ? (ntask_all + 1 - crank) / 2 : ntask_all;
+    auto task_of = [&](uint32_t i) { return csize == 2 ? 2 * i + crank : i; };
     // the ring is issued by the last warp, which never rotates
     const int producer = kWarps - 1;
     const uint32_t ring_to = p.nslots < nitems ? p.nslots : nitems;
@@ -339,10 +204,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_pq2_int_kernel(const __grid_
         *issued = pre;
     }
     uint8_t *act_s = smem + p.off_act;
+    const uint32_t act_remote0 = csize == 2 ? mapa_shared(smem_u32(act_s), crank ^ 1u) : 0u;
     float v[16], d[16];
     if (rotating) {
         // the first rotation of a rotating pair
-        const uint32_t task = pr;
+        const uint32_t task = task_of(pr);
         const uint32_t b = task % p.nblk;
         float *scr = reinterpret_cast<float *>(smem + p.off_rot + pr * kRotScratchBytes);
         if (p.signs) load_signs2(task >= p.nblk ? p.signs2 : p.signs, b, t, d);     // read-only
@@ -354,8 +220,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_pq2_int_kernel(const __grid_
         // queue the rest of the ring behind it
         *reinterpret_cast<volatile float *>(scr + 1080 + (t >> 5)) = v[0] + v[15];
         named_barrier_arrive(kBarX, nwait);
-        rotate_pack2(p.signs != nullptr, v, d, b, p.groups, act_s + (task / p.nblk) * p.act_bytes, scr, t,
-                     kBarPair0 + pr);
+        rotate_pack2(p.signs != nullptr, v, d, b, p.groups, act_s + (task / p.nblk) * p.act_bytes,
+                     act_remote0 ? act_remote0 + (task / p.nblk) * p.act_bytes : 0u, scr, t, kBarPair0 + pr);
     } else {
         pdl_launch_dependents();
         pdl_wait();
@@ -372,16 +238,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_pq2_int_kernel(const __grid_
     }
     // more rotations than rotating pairs: further rounds
 #pragma unroll 1
-    for (uint32_t task = pr + npr; rotating && task < ntask; task += npr) {
-        const uint32_t b = task % p.nblk;
+    for (uint32_t i = pr + npr; rotating && i < ntask; i += npr) {
+        const uint32_t task = task_of(i), b = task % p.nblk;
         if (p.signs) load_signs2(task >= p.nblk ? p.signs2 : p.signs, b, t, d);
         load_block2<kXType>(p.x, p.k, b, t, v);
         rotate_pack2(p.signs != nullptr, v, d, b, p.groups, act_s + (task / p.nblk) * p.act_bytes,
+                     act_remote0 ? act_remote0 + (task / p.nblk) * p.act_bytes : 0u,
                      reinterpret_cast<float *>(smem + p.off_rot + pr * kRotScratchBytes), t, kBarPair0 + pr);
     }
     // (the ring's barriers and counters, set up by the producer, are first used
     // after the barrier that completes the activation table)
-    __syncthreads();     // the activation table is complete
+    // the activation table is complete, in both CTAs of a cluster (this also
+    // publishes the ring's barriers and counters to every warp)
+    if (csize == 2) cluster_sync();
+    else __syncthreads();
 
     bool ok = true;
     float *part = reinterpret_cast<float *>(smem + p.off_part);
@@ -548,18 +418,26 @@ bool gemv_pq2_int_plan(const ninfer_row_split_geometry &g, uint64_t M, bool rota
     const uint32_t cnt_bytes = (kMaxSlots + 4) * 4;
     // warp pairs rotating at once, each with its own scratch: as many as there
     // are rotations (at most kMaxPairs) while the ring keeps at least four slots
-    const uint32_t ntask = nrmat * (uint32_t)((g.k + 1023) / 1024);
+    // one CTA per SM with ~n / SMs rows each. When a CTA alone would need more
+    // than one round of rotations, CTA pairs form clusters that share them (an
+    // odd count gets one CTA without rows); otherwise the cluster's barrier
+    // and paired scheduling would only add to the call.
+    const uint64_t grid0 = std::max<uint64_t>(1, std::min<uint64_t>((uint64_t)sms, g.n / 64));
+    const uint64_t R = (g.n + grid0 - 1) / grid0;
+    const uint64_t grid_rows = (g.n + R - 1) / R;
+    const uint32_t ntask_all = nrmat * (uint32_t)((g.k + 1023) / 1024);
+    const bool cluster = grid_rows >= 2 && ntask_all > kMaxPairs;
+    const uint64_t grid = cluster ? (grid_rows + 1) / 2 * 2 : grid_rows;
+    const uint32_t ntask = cluster ? (ntask_all + 1) / 2 : ntask_all;      // per CTA
     uint32_t nrot = std::min<uint32_t>(ntask, kMaxPairs);     // rotating warp pairs
     auto fixed_of = [&](uint32_t nr) { return act_bytes + nr * kRotScratchBytes + part_bytes + bar_bytes + cnt_bytes; };
     while (nrot > 1 && (int)fixed_of(nrot) + 4 * (int)kChunkBytes > smem_limit) nrot = (nrot + 1) / 2;
     const uint32_t fixed = fixed_of(nrot);
     if ((int)fixed + 2 * (int)kChunkBytes > smem_limit) return false;
     const uint32_t nslots = std::min<uint32_t>(kMaxSlots, (uint32_t)((smem_limit - (int)fixed) / (int)kChunkBytes));
-    // one CTA per SM with ~n / SMs rows each
-    const uint64_t grid0 = std::max<uint64_t>(1, std::min<uint64_t>((uint64_t)sms, g.n / 64));
-    const uint64_t R = (g.n + grid0 - 1) / grid0;
-    const uint64_t grid = (g.n + R - 1) / R;
     plan->ok = true;
+    plan->grid_rows = (uint32_t)grid_rows;
+    plan->cluster = cluster;
     plan->mats = mats;
     plan->act_one = act_one;
     plan->grid = (uint32_t)grid;
@@ -600,6 +478,7 @@ int gemv_pq2_int_launch(const IntPlan &plan, const uint8_t *payload, const ninfe
     p.y_dtype = y_dtype;
     p.nslots = plan.nslots;
     p.nslots_inv = (uint32_t)((1ull << 32) / plan.nslots + 1);
+    p.grid_rows = plan.grid_rows;
     p.pre_issue = plan.pre_issue;
     p.off_ring = plan.off_ring;
     p.off_act = plan.off_act;
@@ -611,7 +490,7 @@ int gemv_pq2_int_launch(const IntPlan &plan, const uint8_t *payload, const ninfe
     p.wait_cycles = wait_limit_cycles();
     int st = device_error_word(&p.err);
     if (st) return st;
-    const uint64_t R = plan.rows_per_cta, G = plan.grid, last_rows = g.n - (G - 1) * R;
+    const uint64_t R = plan.rows_per_cta, G = plan.grid_rows, last_rows = g.n - (G - 1) * R;
     if (G > 1) {
         st = encode_row_tiles(&p.wmap_main, base, g.base_row_bytes, R, G - 1, 128, kRows, true);
         if (!st) st = encode_row_tiles(&p.smap_main, scale, g.scale_row_bytes, R, G - 1, 16, kRows, false);
@@ -650,11 +529,15 @@ int gemv_pq2_int_launch(const IntPlan &plan, const uint8_t *payload, const ninfe
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = plan.smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = plan.cluster ? 2 : 1;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = plan.cluster ? 2 : 1;     // no cluster attribute at all unless CTA pairs are wanted
     cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, p);
     if (e != cudaSuccess) return fail(NINFER_ERR_CUDA, "gemv launch: %s", cudaGetErrorString(e));
     return NINFER_OK;

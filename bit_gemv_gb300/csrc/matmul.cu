@@ -69,7 +69,7 @@ int plan_matmul(int fmt, const ninfer_row_split_geometry &g, uint64_t M, bool ro
     }
     if (fmt == NINFER_PTQ1_0_G128 && gemv_ptq1_int_plan(g, M, rotate, d.sms, d.smem_optin, &mp->gptq)) {
         mp->path = Path::kIntPtq1;
-        mp->workspace = mp->gptq.workspace;     // operand words when x is rotated by the prep kernel
+        mp->workspace = mp->gptq.workspace;     // none: the CTAs rotate x themselves
         return NINFER_OK;
     }
     if (fmt == NINFER_PQ2_0_G128 && gemv_pq2_mma_plan(g, M, rotate, d.sms, d.smem_optin, &mp->gmma)) {

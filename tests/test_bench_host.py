@@ -47,9 +47,9 @@ def test_launch_counts():
     w = synth.WORKLOADS
     assert bench.kernels_per_step(w["gateup"]) == 1
     assert bench.kernels_per_step(w["ffn_gate_up"]) == 1
-    assert bench.kernels_per_step(w["down"]) == 2           # rotation kernel + decode
+    assert bench.kernels_per_step(w["down"]) == 1           # rotation fused into the decode kernel
     assert bench.kernels_per_step(w["prefill"]) == 2
     assert bench.kernels_per_step(w["prefill_down"]) == 3
     # the general gate/up path: two projections and the SwiGLU kernel
-    assert bench.kernels_per_step(dataclasses.replace(w["down"], mats=2)) == 5
+    assert bench.kernels_per_step(dataclasses.replace(w["down"], mats=2)) == 3
     assert bench.kernels_per_step(dataclasses.replace(w["gateup"], mats=2, M=4)) == 5

@@ -118,10 +118,13 @@ def test_matmul_ptq1_m1_wide_k(n, k, rotate):
     check_decode(y, ref)
 
 
-@pytest.mark.parametrize("n,k,rotate", [(300, 16384, True), (130, 20480, True), (90, 20400, False)])
+@pytest.mark.parametrize("n,k,rotate", [(300, 16384, True), (130, 20480, True), (90, 20400, False),
+                                        (200, 8192, True), (4800, 9216, True)])
 def test_matmul_pq2_m1_wide_k(n, k, rotate):
-    """PQ2_0 at M = 1 with more than eight 1024-blocks: one warp rotates each
-    block (one round up to sixteen blocks, then a second)."""
+    """PQ2_0 at M = 1 with more than seven 1024-blocks: CTA pairs (clusters)
+    share the rotations, a warp pair rotating one block per round; an odd
+    number of CTAs with rows (n = 200: three, n = 4800: seventy-five) adds a
+    CTA without rows that only rotates for its partner."""
     c = synth.make_case("gateup", n=n, k=k, M=1, seed=n + k)
     y = run_matmul("PQ2_0_G128", c, rotate=rotate)
     ref = oracle_matmul_rows("PQ2_0_G128", c, np.arange(n), rotate=rotate)
@@ -402,7 +405,7 @@ _up_inputs = synth.up_projection     # the up projection's values, scales and si
 @pytest.mark.parametrize("fmt,n,k,M,same_signs", [
     ("PQ2_0_G128", 300, 2048, 1, False), ("PQ2_0_G128", 300, 2048, 1, True), ("PQ2_0_G128", 150, 5120, 1, False),
     ("PQ2_0_G128", 1, 1024, 1, False), ("PTQ1_0_G128", 300, 2048, 1, False), ("PQ2_0_G128", 77, 3072, 4, False),
-    ("PTQ1_0_G128", 129, 2048, 40, True)])
+    ("PTQ1_0_G128", 129, 2048, 40, True), ("PQ2_0_G128", 200, 5120, 1, False), ("PQ2_0_G128", 4800, 4096, 1, False)])
 def test_gate_up_swiglu(fmt, n, k, M, same_signs):
     """silu(gate x) * (up x), each projection with its own signs (or one shared
     vector): PQ2_0 at M = 1 runs the fused two-matrix kernel, the other cases
