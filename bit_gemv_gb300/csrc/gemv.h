@@ -37,6 +37,11 @@ int encode_rows(CUtensorMap *map, const uint8_t *addr, uint64_t row_bytes, uint6
 int encode_row_tiles(CUtensorMap *map, const uint8_t *addr, uint64_t row_bytes, uint64_t rows, uint64_t tiles,
                      uint32_t box_bytes, uint32_t box_rows, bool swizzle128);
 
+// A 3-D tensor of 8-byte elements (dims[0] contiguous; strides in bytes of
+// dims 1-2), unswizzled boxes of box[0] x box[1] x box[2] elements.
+int encode_3d_u64(CUtensorMap *map, const uint8_t *addr, const uint64_t (&dims)[3], const uint64_t (&strides)[2],
+                  const uint32_t (&box)[3]);
+
 // A 2-D tensor map over a row-major array: `inner` elements per row, `outer`
 // rows, rows `row_stride_bytes` apart; boxes of box_inner x box_outer.
 int encode_2d(CUtensorMap *map, CUtensorMapDataType dtype, uint32_t elem_bytes, const void *addr, uint64_t inner,
@@ -64,11 +69,10 @@ int gemv_pq2_int_launch(const IntPlan &plan, const uint8_t *payload, const ninfe
 // M = 1 integer kernel (PTQ1_0_G128), rotation fused in.
 struct Ptq1Plan {
     bool ok;
-    int rl;                  // rows per lane: 4 for large row ranges, else 1
-    bool cluster;            // CTA pairs share the rotations (grid even)
-    uint32_t grid, grid_rows, rows_per_cta, nch, nslots, pre_issue, nrot;
-    uint32_t off_ring, off_act, off_rem, off_part, off_bar, off_cnt, smem;
-    uint32_t act_bytes;
+    bool cluster;            // CTA pairs split the groups of one row range (grid even)
+    uint32_t grid, units, rows_per_cta, split, ng, hbytes, wg, nbx, bstride, nsets, u, nslots, pre_issue;
+    uint32_t slot_bytes, slot_high, slot_scale, part_stride, part_slot_bytes;
+    uint32_t off_ring, off_part, off_rs, off_bar, smem;
     uint64_t workspace;
 };
 bool gemv_ptq1_int_plan(const ninfer_row_split_geometry &g, uint64_t M, bool rotate, int sms, int smem_limit,

@@ -156,6 +156,27 @@ int encode_row_tiles(CUtensorMap *map, const uint8_t *addr, uint64_t row_bytes, 
     return encode_bytes(map, addr, 3, dims, strides, box_bytes, box_rows, swizzle128);
 }
 
+int encode_3d_u64(CUtensorMap *map, const uint8_t *addr, const uint64_t (&dims)[3], const uint64_t (&strides)[2],
+                  const uint32_t (&box)[3]) {
+    const MapKey key{{3, reinterpret_cast<uint64_t>(addr), dims[0], dims[1], dims[2], strides[0], strides[1], box[0],
+                      box[1], box[2], 0, 0, 0, 0}};
+    if (map_lookup(key, map)) return NINFER_OK;
+    EncodeTiledFn fn;
+    int st = encode_fn(&fn);
+    if (st) return st;
+    std::memset(map, 0, sizeof *map);
+    const cuuint64_t d[3] = {dims[0], dims[1], dims[2]};
+    const cuuint64_t str[2] = {strides[0], strides[1]};
+    const cuuint32_t bx[3] = {box[0], box[1], box[2]};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT64, 3, const_cast<uint8_t *>(addr), d, str, bx, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(NINFER_ERR_CUDA, "tensor map encode failed (CUresult %d)", (int)r);
+    map_store(key, *map);
+    return NINFER_OK;
+}
+
 int encode_2d(CUtensorMap *map, CUtensorMapDataType dtype, uint32_t elem_bytes, const void *addr, uint64_t inner,
               uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer, bool swizzle128) {
     const MapKey key{{2, reinterpret_cast<uint64_t>(addr), (uint64_t)dtype, elem_bytes, inner, outer, row_stride_bytes,

@@ -9,34 +9,48 @@
 // byte j of a group holds weights 5j .. 5j+4 as (byte / 3^i) % 3, high byte h
 // holds weights 120 + 4h .. 123 + 4h; one binary16 scale per group.
 //
-// Activation: warp pairs rotate and round it (rot2.cuh), write its 16-bit
-// values in natural order to their scratch and pack, per group, 64 operand
-// words: for base byte j (< 24), (x16[5j], x16[5j+1]) and (x16[5j+2],
-// x16[5j+3]); for the four bytes 4q .. 4q+3, the pairs of their fifth weights
-// (x16[5(4q+2c)+4], x16[5(4q+2c+1)+4]); for high byte h, its two pairs. With
-// more than seven 1024-blocks, two CTAs of a cluster share the rotations and
-// each writes its groups into both tables.
+// Work split: a CTA owns a contiguous range of rows. When its sixteen warps
+// could not rotate all 1024-blocks of k in one round, two CTAs of a cluster
+// share a row range and split the groups in halves: each rotates and reads only
+// its half, and the two partial row sums meet through distributed shared memory
+// at the end (rank 0 finishes the first half of the rows, rank 1 the second).
+//
+// Activation: each warp rotates one of the CTA's blocks in registers (element
+// bits {0,1,2,8,9} in the registers, then, after a transpose through the
+// warp's scratch, bits 3-7), rounds it to 16-bit fixed point (x16 =
+// rint(xr * 2^E'), max |x16| < 2^14) and packs, per group, 64 operand words: for base byte
+// j (< 24), (x16[5j], x16[5j+1]) and (x16[5j+2], x16[5j+3]); for the four bytes
+// 4q .. 4q+3, the pairs of their fifth weights (x16[5(4q+2c)+4],
+// x16[5(4q+2c+1)+4]); for high byte h, its two pairs; and one group entry
+// {2^-E (with the transform's 1/32), sum of the group's x16}.
+//
+// Thread mapping: thread t owns group t % nG of the CTA's nG
+// groups for the whole launch, holding its 64 operand words in registers, and
+// row set t / nG. Weights arrive in batches of nsets * u rows as tensor boxes
+// of 8-byte elements, each plane seen as {row, rows, row ranges}: the CTA's
+// base bytes of the batch's rows in one box per wg groups (wg <= 84, so that a
+// box row stays within 256 elements), then their high bytes and their scales
+// (one box each, rounded out to whole 16-byte units). The boxes land row-major
+// in a slot of a shared-memory ring, so that the lanes of a warp read
+// consecutive groups of one row, without bank conflicts. Per row a
+// thread writes one partial sum to the slot's partial buffer (group-major, an
+// odd number of floats per group). Once every math warp has finished a batch,
+// its partials are added per row, y (or the CTA's share of it) stored and the
+// slot refilled: by warp 15 when it has no group of its own (it shares a
+// scheduler with fewer math warps), else by the warps in turn, each after its
+// own next batch. Only the first batch is requested before the
+// programmatic-dependent-launch wait: that wait returns only once memory
+// requests already in flight have landed.
 //
 // Arithmetic: a 256-entry table maps a code byte to its digits as bytes
-// (t0 | t1 << 8 | t2 << 16 | t3 << 24, with t4 in bits 2-3 of byte 0), held 32
-// times so that lane l always reads bank l (entry B of lane l at B * 128 + 4 l,
-// from the start of shared memory). Per base byte dp2a multiplies (t0, t1) and
-// (t2, t3) by their activation pairs; the t4 fields of four consecutive bytes
-// are gathered into one word by byte permutes and multiplied by their pairs
-// (times 4, removed at the end); all exact in int32. Per group:
+// (t0 | t1 << 8 | t2 << 16 | t3 << 24, with t4 in bits 2-3 of byte 0), entry B
+// at B * 256 and held once per lane (lane l's copy at + 4 l, bank l), so that a
+// byte permute of the code word and 4 l forms a lane's address in one
+// instruction. Per base byte dp2a multiplies (t0, t1) and (t2, t3) by their
+// activation pairs; the t4 fields of four consecutive bytes are gathered into
+// one word by byte permutes and multiplied by their pairs (times 4, removed at
+// the end); all exact in int32. Per group:
 //   y += scale * 2^-E * (sum t x16 - sum x16)                    (value = t - 1)
-//
-// Work: one CTA per SM owns a contiguous range of rows, in tiles of 32 kRL
-// rows (lane l: rows l, l + 32, .. of the tile, so that the 64 operand words of
-// a group, read once into registers, serve kRL rows). A chunk of the ring is a
-// tile's 16 groups: three 128-byte-swizzled boxes of base bytes (384 bytes per
-// row), one box of high bytes and one of scales, on one mbarrier; warp w takes
-// group w of the chunk, or half of group w % 8 when the chunk has only eight
-// groups. With kRL = 1 a CTA whose rows exceed a multiple of 32 by one or two
-// copies those rows whole into shared memory and computes them with lanes =
-// (row, group). One chunk is requested before the programmatic-dependent-
-// launch wait; the rest of the ring, by a warp that does not rotate, once x
-// has arrived.
 #include <cstring>
 
 #include <cuda.h>
@@ -53,187 +67,269 @@
 namespace ninfer {
 namespace {
 
-constexpr int kThreads = 512;
-constexpr int kWarps = 16;
-constexpr int kProducer = kWarps - 1;       // issues the ring; never rotates
-constexpr uint32_t kChunkGroups = 16;
-constexpr uint32_t kMaxSlots = 8;
-constexpr uint32_t kMaxRem = 2;             // extra rows beyond whole 32-row tiles handled per (row, group)
+constexpr int kThreads = 512;              // four warps per scheduler: up to 128 registers a thread
+constexpr int kWarps = kThreads / 32;
+constexpr uint32_t kMaxSlots = 12;
 constexpr uint32_t kActWords = 64;
-// Groups sit kActStride words apart: the 4-word pad moves consecutive groups 16
-// bytes along the banks, so the remainder-row path (lanes = 16 groups) reads
-// its operand words with at most two-way conflicts; the tile path reads one
-// group per warp (a broadcast) either way.
+// Groups sit kActStride words apart: 17 16-byte units, an odd number, so that
+// lanes loading consecutive groups' words meet no bank conflicts.
 constexpr uint32_t kActStride = 68;
-static_assert(kActStride >= kActWords && kActStride % 4 == 0, "operand words: 16-byte aligned groups");
+static_assert(kActStride >= kActWords && kActStride % 8 == 4, "operand words: an odd number of 16-byte units");
 constexpr uint32_t kActGroupBytes = kActStride * 4;
-constexpr uint32_t kLutBytes = 256 * 128;   // entry B at B * 128: 32 lane copies
-constexpr uint32_t kBarX = 1;               // named barrier: x has arrived
-constexpr uint32_t kBarPair0 = 2;           // named barriers 2.. : one per rotating pair
-constexpr uint32_t kMaxPairs = 7;           // warps 0-13
-static_assert(kMaxPairs * kRotScratchBytes <= kLutBytes, "rotation scratch lives where the table is built later");
-
-template <int kRL>
-struct Tile {
-    static constexpr uint32_t rows = 32 * kRL;
-    static constexpr uint32_t base_box = 128 * rows;                   // one 128-byte column of base bytes
-    static constexpr uint32_t chunk_bytes = 3 * base_box + 2 * 32 * rows;
-};
+constexpr uint32_t kLutStride = 256;        // entry B at B * 256: 32 lane copies, then unused
+constexpr uint32_t kLutBytes = 256 * kLutStride;
+// a warp's rotation scratch: 1024 fp32 values, element e at e + 8 (e >> 8)
+constexpr uint32_t kRotScratch = 4 * 264 * 4;
+// the table, and before it the warps' rotation scratch, start the shared memory
+constexpr uint32_t kRegion0 = (kWarps * kRotScratch > kLutBytes ? kWarps * kRotScratch : kLutBytes);
+static_assert(kRegion0 % 128 == 0, "ring slots 128-byte aligned");
+constexpr uint32_t kMaxClusterRows = 4096;  // rows of a split range (their partial sums stay in shared memory)
+// after the full and empty barriers of the slots: the failure flag, then per slot
+// the last batch issued into it
+constexpr uint32_t kFlagWords = 1 + kMaxSlots;
+constexpr uint32_t kBarBytes = (2 * kMaxSlots * 8 + 4 * kFlagWords + 15) / 16 * 16;
 
 struct Ptq1Params {
-    CUtensorMap bmap_main, bmap_last;   // base rows {row bytes, R rows, CTA} / last CTA with rows, 128-byte boxes
-    CUtensorMap hmap_main, hmap_last;   // high rows, 32-byte boxes
-    CUtensorMap smap_main, smap_last;   // scale rows, 32-byte boxes
-    const uint8_t *base, *high, *scale; // plane starts (remainder rows)
-    uint64_t base_row, high_row, scale_row;
+    // planes as 8-byte elements {row, rows, row ranges}: every row range but the
+    // last, and the last
+    CUtensorMap bmap_main, bmap_last, hmap_main, hmap_last, smap_main, smap_last;
     const void *x;
     const uint16_t *signs;
-    uint32_t act_bytes;
     void *y;
     uint64_t n;
-    uint32_t k, groups, nblk, nch, rows_per_cta, grid_rows;     // nch: chunks per tile
+    uint32_t units;                 // row ranges (CTAs, or CTA pairs when clustered)
+    uint32_t k, groups, split;      // split: groups of cluster rank 0 (all groups without a cluster)
+    uint32_t rows_per_cta;          // rows of a CTA (of a CTA pair when clustered)
+    uint32_t nsets, u;              // row sets and rows per set of a batch
+    uint32_t wg, nbx, bstride;      // groups per base box, base boxes per batch, their distance in a slot
+    uint32_t nslots, nslots_inv, pre_issue;
+    uint32_t slot_bytes, slot_high, slot_scale;         // slot size and the offsets of its high / scale regions
+    uint32_t part_stride, part_slot_bytes;
+    uint32_t off_ring, off_part, off_rs, off_bar;       // table / rotation scratch at 0; operand words at off_part
     int x_dtype, y_dtype;
-    uint32_t nslots, nslots_inv, pre_issue, nrot;               // nrot: rotating pairs at most
-    uint32_t off_ring, off_act, off_rem, off_part, off_bar, off_cnt;     // table / rotation scratch at 0
     uint32_t *err;
     long long wait_cycles;
 };
 
-struct CtaRows {
-    uint64_t begin;
-    uint32_t ntile, rem;    // tiles (the last may be partial when rem == 0), remainder rows
-    uint32_t rows;
+// This CTA's share: row range unit (rows [r0, r0 + rows)), groups [g0, g0 + ng),
+// high bytes and scales of groups [h0, h0 + hbytes / 2).
+struct Cta {
+    uint64_t r0;
+    uint32_t unit, rows, g0, ng, h0, hbytes, nbatch;
 };
 
-template <int kRL>
-__device__ __forceinline__ CtaRows cta_rows(const Ptq1Params &p) {
-    CtaRows c;
-    c.begin = (uint64_t)blockIdx.x * p.rows_per_cta;
-    const uint64_t end = c.begin + p.rows_per_cta < p.n ? c.begin + p.rows_per_cta : p.n;
-    c.rows = end > c.begin ? (uint32_t)(end - c.begin) : 0u;
-    const uint32_t T = Tile<kRL>::rows, full = c.rows / T, extra = c.rows % T;
-    if (kRL == 1 && full >= 1 && extra <= kMaxRem) {
-        c.ntile = full;
-        c.rem = extra;
-    } else {
-        c.ntile = full + (extra ? 1 : 0);
-        c.rem = 0;
-    }
+__device__ __forceinline__ Cta cta_share(const Ptq1Params &p, uint32_t csize, uint32_t crank) {
+    Cta c;
+    c.unit = blockIdx.x / csize;
+    c.r0 = (uint64_t)c.unit * p.rows_per_cta;
+    const uint64_t left = c.r0 < p.n ? p.n - c.r0 : 0;
+    c.rows = left < p.rows_per_cta ? (uint32_t)left : p.rows_per_cta;
+    c.g0 = crank ? p.split : 0u;
+    c.ng = csize == 2 ? (crank ? p.groups - p.split : p.split) : p.groups;
+    c.h0 = c.g0 & ~7u;
+    c.hbytes = 2 * (((c.g0 + c.ng + 7) & ~7u) - c.h0);
+    const uint32_t br = p.nsets * p.u;
+    c.nbatch = (c.rows + br - 1) / br;
     return c;
 }
 
-// Chunk i = tile * nch + ch: its three base boxes, high box and scale box into ring slot i % nslots.
-template <int kRL>
-__device__ __forceinline__ void issue_chunk(const Ptq1Params &p, uint8_t *smem, uint32_t item, bool last_cta) {
-    using T = Tile<kRL>;
-    const uint32_t tile = item / p.nch, ch = item % p.nch, slot = item % p.nslots;
-    const uint32_t dst = smem_u32(smem + p.off_ring) + slot * T::chunk_bytes;
+__device__ __forceinline__ uint32_t slot_of(uint32_t b, uint32_t nslots, uint32_t inv, uint32_t &phase) {
+    const uint32_t cycle = __umulhi(b, inv);     // b / nslots (b < 2^29)
+    phase = cycle & 1;
+    return b - cycle * nslots;
+}
+
+// Batch b's rows into its ring slot (one thread). Rows past the range read as
+// zero and cost no traffic; the transaction counts whole boxes.
+__device__ __forceinline__ void issue_batch(const Ptq1Params &p, const Cta &c, uint8_t *smem, uint32_t b) {
+    const uint32_t br = p.nsets * p.u;
+    uint32_t phase;
+    const uint32_t slot = slot_of(b, p.nslots, p.nslots_inv, phase);
     const uint32_t bar = smem_u32(smem + p.off_bar) + 8 * slot;
-    mbar_arrive_expect_tx(bar, T::chunk_bytes);
-    const int y0 = (int)(tile * T::rows), z = (int)blockIdx.x;
+    mbar_arrive_expect_tx(bar, br * (24 * p.wg * p.nbx + 2 * c.hbytes));
+    const uint32_t dst = smem_u32(smem + p.off_ring) + slot * p.slot_bytes;
+    const bool last = c.unit == p.units - 1;
+    const int y = (int)(b * br), z = last ? 0 : (int)c.unit;
+    for (uint32_t bx = 0; bx < p.nbx; ++bx)
+        tma_load_3d(dst + bx * p.bstride, last ? &p.bmap_last : &p.bmap_main, (int)(3 * (c.g0 + bx * p.wg)), y, z, bar);
+    tma_load_3d(dst + p.slot_high, last ? &p.hmap_last : &p.hmap_main, (int)(c.h0 / 4), y, z, bar);
+    tma_load_3d(dst + p.slot_scale, last ? &p.smap_last : &p.smap_main, (int)(c.h0 / 4), y, z, bar);
+}
+
+// Block b of x (and its signs) as one warp holds it: v[8 i + e] = element
+// 1024 b + 256 i + 8 lane + e; zero past k.
+template <int kXType>
+__device__ __forceinline__ void load_block1(const void *x, uint32_t k, uint32_t b, int lane, float (&v)[32]) {
 #pragma unroll
-    for (int bx = 0; bx < 3; ++bx) {
-        const int x = (int)(ch * 384 + 128 * bx);
-        if (last_cta) tma_load_2d(dst + bx * T::base_box, &p.bmap_last, x, y0, bar);
-        else tma_load_3d(dst + bx * T::base_box, &p.bmap_main, x, y0, z, bar);
-    }
-    const int xh = (int)(ch * 32);
-    if (last_cta) {
-        tma_load_2d(dst + 3 * T::base_box, &p.hmap_last, xh, y0, bar);
-        tma_load_2d(dst + 3 * T::base_box + 32 * T::rows, &p.smap_last, xh, y0, bar);
-    } else {
-        tma_load_3d(dst + 3 * T::base_box, &p.hmap_main, xh, y0, z, bar);
-        tma_load_3d(dst + 3 * T::base_box + 32 * T::rows, &p.smap_main, xh, y0, z, bar);
+    for (int i = 0; i < 4; ++i) {
+        float u[8];
+        const uint64_t idx = (uint64_t)b * 1024 + 256 * i + 8 * lane;
+        if (idx + 8 <= k) {
+            load8(x, idx, kXType, u);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) u[e] = idx + e < k ? load1(x, idx + e, kXType) : 0.f;
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[8 * i + e] = u[e];
     }
 }
 
-// Rotates block b with the pair and writes the operand words and group entries
-// {2^-E (with the transform's 1/32), sum of the group's x16 (int bits)} of its
-// eight groups into act and, when act_remote is non-zero (the cluster address
-// of the same table in the other CTA of the cluster), into that table too.
-__device__ __forceinline__ void rotate_pack_ptq1(bool rotate, float (&v)[16], const float (&d)[16], uint32_t b,
-                                                 uint32_t groups, uint8_t *act, uint32_t act_remote, float *scr,
-                                                 int t, uint32_t bar) {
-    const int lane = t & 31;
-    uint32_t qb[16];
-    const int E = rotate_quant2(rotate, v, d, scr, t, bar, qb);
-    const float f = ldexpf(1.f, -E - (rotate ? 5 : 0));
-    // x16 in natural order (int16) in the scratch: elements 512 i + 8 t .. + 7
-    int16_t *qs = reinterpret_cast<int16_t *>(scr);
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const uint32_t *q = qb + 8 * i;
-        uint4 w;
-        w.x = __byte_perm(q[0], q[1], 0x5410);
-        w.y = __byte_perm(q[2], q[3], 0x5410);
-        w.z = __byte_perm(q[4], q[5], 0x5410);
-        w.w = __byte_perm(q[6], q[7], 0x5410);
-        *reinterpret_cast<uint4 *>(qs + 512 * i + 8 * t) = w;
-        // the group's sum of x16 (group 4 i + t / 16 of the block): the 16 lanes of each half-warp
-        const int sum = (int)(q[0] + q[1] + q[2] + q[3] + q[4] + q[5] + q[6] + q[7] - 8u * 0x4B400000u);
-        const int s_lo = __reduce_add_sync(0xffffffffu, lane < 16 ? sum : 0);
-        const int s_hi = __reduce_add_sync(0xffffffffu, lane < 16 ? 0 : sum);
-        const uint32_t G = b * 8 + 4 * i + (t >> 4);
-        if ((lane & 15) == 0 && G < groups) {
-            const int sg = lane < 16 ? s_lo : s_hi;
-            reinterpret_cast<float2 *>(act + (uint64_t)groups * kActGroupBytes)[G] = make_float2(f, __int_as_float(sg));
-            if (act_remote) st_cluster_v2(act_remote + groups * kActGroupBytes + 8 * G, __float_as_uint(f), (uint32_t)sg);
-        }
-    }
-    named_barrier(bar, 64);
-    // operand words: the block's 8 groups have 208 code bytes (192 base, 16 high);
-    // thread t takes bytes t, t + 64, t + 128 and t + 192
-    uint32_t *aw = reinterpret_cast<uint32_t *>(act);
+__device__ __forceinline__ void load_signs1(const uint16_t *s, uint32_t b, int lane, float (&d)[32]) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const uint32_t u = t + 64 * i;
+        float u[8];
+        load_signs8(s, (uint64_t)b * 1024 + 256 * i + 8 * lane, u);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) d[8 * i + e] = u[e];
+    }
+}
+
+// Butterflies over the five register index bits of 32 values: bits 1-4 as
+// paired fp32 adds and subtracts (each element rounded exactly as by a scalar
+// add), bit 0 within the pairs.
+__device__ __forceinline__ void butterfly32(float (&v)[32]) {
+    uint64_t w[16];
+#pragma unroll
+    for (int m = 0; m < 16; ++m) w[m] = f2pack(v[2 * m], v[2 * m + 1]);
+#pragma unroll
+    for (int bit = 0; bit < 4; ++bit)
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+            if (m & (1 << bit)) continue;
+            uint64_t sum, dif;
+            asm("add.rn.f32x2 %0, %1, %2;" : "=l"(sum) : "l"(w[m]), "l"(w[m | (1 << bit)]));
+            asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(dif) : "l"(w[m]), "l"(w[m | (1 << bit)]));
+            w[m] = sum;
+            w[m | (1 << bit)] = dif;
+        }
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+        float a, c;
+        f2unpack(w[m], a, c);
+        v[2 * m] = a + c;
+        v[2 * m + 1] = a - c;
+    }
+}
+
+// Rotates block b with one warp (x in v as load_block1 leaves it; signs in d
+// unless rotate is false), rounds it to x16 = rint(v * 2^E) with E chosen so
+// that max |x16| < 2^14 (v = H (D x) = 32 xr, or x unrotated), and writes the
+// operand words and group entries {2^-E (with the transform's 1/32), sum of
+// the group's x16 (int bits)} of those of its eight groups that lie in
+// [g0, g0 + ng) (local index G - g0). The element bits held in registers are
+// first {0,1,2,8,9} (lane = bits 3-7), then, after a transpose through the
+// scratch, bits 3-7 (lane = {0,1,2,8,9}); the rounded values go back through
+// the scratch as int16 in natural order (element e at e + 16 (e >> 8)).
+__device__ __forceinline__ void rotate_pack(bool rotate, float (&v)[32], const float (&d)[32], uint32_t b,
+                                            uint32_t g0, uint32_t ng, uint8_t *act, float *scr, int lane) {
+    if (rotate) {
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+            uint64_t r;
+            asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2pack(v[2 * m], v[2 * m + 1])),
+                "l"(f2pack(d[2 * m], d[2 * m + 1])));
+            f2unpack(r, v[2 * m], v[2 * m + 1]);
+        }
+        butterfly32(v);      // element bits 0, 1, 2, 8, 9
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+            *reinterpret_cast<float4 *>(scr + 264 * i + 8 * lane + 4 * c) =
+                make_float4(v[8 * i + 4 * c], v[8 * i + 4 * c + 1], v[8 * i + 4 * c + 2], v[8 * i + 4 * c + 3]);
+    __syncwarp();
+    // lane = element bits (0, 1, 2, 8, 9), register j = bits 3-7: e = (lane & 7) + 8 j + 256 (lane >> 3)
+    const int base = (lane & 7) + 264 * (lane >> 3);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = scr[base + 8 * j];
+    if (rotate) butterfly32(v);      // element bits 3-7
+    // block maximum: a tree in registers, then the warp (a non-negative float's
+    // bits order as its value: one warp-wide integer max)
+    float m[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) m[j] = fmaxf(fabsf(v[j]), fabsf(v[j + 16]));
+#pragma unroll
+    for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+        for (int j = 0; j < w; ++j) m[j] = fmaxf(m[j], m[j + w]);
+    const float mx = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(m[0])));
+    int E = 0;
+    if (mx > 0.f) E = 13 - ilogbf(mx);     // max |x16| < 2^14
+    E = max(-100, min(100, E));
+    const float up = ldexpf(1.f, E);
+    const float f = ldexpf(1.f, -E - (rotate ? 5 : 0));
+    __syncwarp();        // every lane has read its transposed values
+    // x16 = rint(v * 2^E): adding 1.5 * 2^23 rounds to nearest (ties to even) and
+    // leaves x16 in the low 16 bits; group (element bits 7-9) sums: bit 7 = j >> 4,
+    // bits 8-9 = lane >> 3
+    int16_t *qs = reinterpret_cast<int16_t *>(scr);
+    const int qbase = (lane & 7) + 272 * (lane >> 3);
+    int gsum[2] = {0, 0};
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        const int q = __float_as_int(fmaf(v[j], up, 12582912.0f)) - 0x4B400000;
+        gsum[j >> 4] += q;
+        qs[qbase + 8 * j] = (int16_t)q;
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int sh = 1; sh < 8; sh <<= 1) gsum[h] += __shfl_xor_sync(0xffffffffu, gsum[h], sh);
+    float2 *gs = reinterpret_cast<float2 *>(act + ng * kActGroupBytes);
+    if ((lane & 7) == 0) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint32_t L = b * 8 + 2 * (lane >> 3) + h - g0;     // wraps past ng when below g0
+            if (L < ng) gs[L] = make_float2(f, __int_as_float(gsum[h]));
+        }
+    }
+    __syncwarp();
+    // operand words: the block's 8 groups have 208 code bytes (192 base, 16 high);
+    // lane l takes bytes l, l + 32, ..; group gl's elements start at 128 gl + 16 (gl >> 1)
+    uint32_t *aw = reinterpret_cast<uint32_t *>(act);
+#pragma unroll
+    for (int i = 0; i < 7; ++i) {
+        const uint32_t u = lane + 32 * i;
         if (u >= 208) break;
-        const uint32_t gl = u < 192 ? u / 24 : (u - 192) >> 1, G = b * 8 + gl;
-        if (G >= groups) continue;
-        uint32_t *dst = aw + (uint64_t)G * kActStride;
+        const uint32_t gl = u < 192 ? u / 24 : (u - 192) >> 1, L = b * 8 + gl - g0;
+        if (L >= ng) continue;
+        uint32_t *dst = aw + L * kActStride;
+        const int16_t *grp = qs + 128 * gl + 16 * (gl >> 1);
         if (u < 192) {
             const uint32_t j = u % 24;
-            const int16_t *e = qs + 128 * gl + 5 * j;
+            const int16_t *e = grp + 5 * j;
             dst[2 * j] = (uint32_t)(uint16_t)e[0] | ((uint32_t)(uint16_t)e[1] << 16);
             dst[2 * j + 1] = (uint32_t)(uint16_t)e[2] | ((uint32_t)(uint16_t)e[3] << 16);
             reinterpret_cast<int16_t *>(dst + 48 + 2 * (j >> 2) + ((j >> 1) & 1))[j & 1] = e[4];
         } else {
             const uint32_t hh = (u - 192) & 1;
-            const int16_t *e = qs + 128 * gl + 120 + 4 * hh;
+            const int16_t *e = grp + 120 + 4 * hh;
             dst[60 + 2 * hh] = (uint32_t)(uint16_t)e[0] | ((uint32_t)(uint16_t)e[1] << 16);
             dst[61 + 2 * hh] = (uint32_t)(uint16_t)e[2] | ((uint32_t)(uint16_t)e[3] << 16);
         }
     }
-    named_barrier(bar, 64);
-    if (act_remote) {
-        // the block's groups as they now stand in this table, to the other CTA of the cluster
-        const uint32_t g0 = b * 8, ng = g0 + 8 <= groups ? 8 : (g0 < groups ? groups - g0 : 0);
-        const uint32_t n16 = ng * kActGroupBytes / 16;
-        const uint4 *src = reinterpret_cast<const uint4 *>(act + (uint64_t)g0 * kActGroupBytes);
-        for (uint32_t c = t; c < n16; c += 64) st_cluster_v4(act_remote + g0 * kActGroupBytes + 16 * c, src[c]);
-    }
-    named_barrier(bar, 64);      // the scratch may be reused
+    __syncwarp();        // the scratch may be reused
 }
 
-// sum_j t_j x16_j over kNq base words (four code bytes each) and kNh high
-// bytes of one group (a whole group: 6 and 2; half a group: 3 and 1), from the
-// operand words av (in registers, in the order of the group's 64 words: the
-// pairs of base byte j at 2 j, the fifth-weight pairs of word q at kT4 + 2 q,
-// the pairs of high byte h at kHi + 2 h) and the lane's copies of the digit
-// table: entry B of this lane at lut + (B << 7 | lane4), lane4 = 4 * lane.
-template <int kNq, int kNh, int kT4, int kHi, int kN>
-__device__ __forceinline__ int group_dot(const uint32_t (&bw)[kNq], uint32_t hb, uint32_t lut, uint32_t lane4,
-                                         const uint32_t (&av)[kN]) {
+// Lane's copy of the table entry of byte c of w: lut + (B_c << 8 | lane4).
+__device__ __forceinline__ uint32_t lut_entry(const uint8_t *lut, uint32_t w, uint32_t lane4, uint32_t c) {
+    return *reinterpret_cast<const uint32_t *>(lut + __byte_perm(w, lane4, 0x5504u | (c << 4)));
+}
+
+// sum_j t_j x16_j over the group's six base words (four code bytes each) and
+// two high bytes, from the operand words av (the pairs of base byte j at 2 j,
+// the fifth-weight pairs of word q at 48 + 2 q, the pairs of high byte h at
+// 60 + 2 h).
+__device__ __forceinline__ int group_dot(const uint32_t (&bw)[6], uint32_t hb, const uint8_t *lut, uint32_t lane4,
+                                         const uint32_t (&av)[kActWords]) {
     int acc[4] = {0, 0, 0, 0}, acc4 = 0;
 #pragma unroll
-    for (int q = 0; q < kNq; ++q) {
+    for (int q = 0; q < 6; ++q) {
         uint32_t W[4];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const int sh = 8 * c - 7;
-            const uint32_t off = ((sh >= 0 ? bw[q] >> sh : bw[q] << (-sh)) & 0x7F80u) | lane4;
-            W[c] = lds32(lut + off);
-        }
+        for (int c = 0; c < 4; ++c) W[c] = lut_entry(lut, bw[q], lane4, c);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
             const uint32_t m = W[c] & 0x03030303u;
@@ -244,299 +340,212 @@ __device__ __forceinline__ int group_dot(const uint32_t (&bw)[kNq], uint32_t hb,
         // byte 0 of each entry holds 4 * t4 in bits 2-3: gather the four
         const uint32_t g = __byte_perm(__byte_perm(W[0], W[1], 0x0040u), __byte_perm(W[2], W[3], 0x0040u), 0x5410u) &
                            0x0C0C0C0Cu;
-        acc4 = dp2a_lo(av[kT4 + 2 * q], g, acc4);
-        acc4 = dp2a_hi(av[kT4 + 2 * q + 1], g, acc4);
+        acc4 = dp2a_lo(av[48 + 2 * q], g, acc4);
+        acc4 = dp2a_hi(av[49 + 2 * q], g, acc4);
     }
 #pragma unroll
-    for (int hh = 0; hh < kNh; ++hh) {
-        const int sh = 8 * hh - 7;
-        const uint32_t off = ((sh >= 0 ? hb >> sh : hb << (-sh)) & 0x7F80u) | lane4;
-        const uint32_t m = lds32(lut + off) & 0x03030303u;
-        acc[hh] = dp2a_lo(av[kHi + 2 * hh], m, acc[hh]);
-        acc[hh] = dp2a_hi(av[kHi + 2 * hh + 1], m, acc[hh]);
+    for (int h = 0; h < 2; ++h) {
+        const uint32_t m = lut_entry(lut, hb, lane4, h) & 0x03030303u;
+        acc[h] = dp2a_lo(av[60 + 2 * h], m, acc[h]);
+        acc[h] = dp2a_hi(av[61 + 2 * h], m, acc[h]);
     }
     return acc[0] + acc[1] + acc[2] + acc[3] + (acc4 >> 2);
 }
 
-template <int kN>
-__device__ __forceinline__ void load_words(const uint32_t *src, uint32_t (&av)[kN]) {
-    const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
-#pragma unroll
-    for (int i = 0; i < kN / 4; ++i) {
-        const uint4 a = s4[i];
-        av[4 * i] = a.x;
-        av[4 * i + 1] = a.y;
-        av[4 * i + 2] = a.z;
-        av[4 * i + 3] = a.w;
-    }
-}
-
-template <int kRL, int kXType>
+template <int kXType>
 __global__ void __launch_bounds__(kThreads, 1) gemv_ptq1_int_kernel(const __grid_constant__ Ptq1Params p) {
-    using TL = Tile<kRL>;
     extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const CtaRows cr = cta_rows<kRL>(p);
-    const bool last_cta = blockIdx.x == p.grid_rows - 1;
-    const uint32_t nitems = cr.ntile * p.nch;
+    const uint32_t csize = cluster_nctarank(), crank = csize == 2 ? cluster_ctarank() : 0u;
+    const Cta c = cta_share(p, csize, crank);
     const uint32_t bar0 = smem_u32(smem + p.off_bar);
-    const uint32_t rem_bar = bar0 + 8 * kMaxSlots;
-    uint32_t *cnt = reinterpret_cast<uint32_t *>(smem + p.off_cnt);
-    uint32_t *issued = cnt + kMaxSlots, *failed = cnt + kMaxSlots + 1;
-    const uint32_t lut_s = smem_u32(smem), lane4 = 4u * (uint32_t)lane;
-    uint8_t *rem_s = smem + p.off_rem;
-    uint8_t *act_s = smem + p.off_act;
-    const uint32_t ring_to = p.nslots < nitems ? p.nslots : nitems;
-    const uint32_t pre = p.pre_issue < ring_to ? p.pre_issue : ring_to;
-    // rotation tasks = 1024-blocks; in a cluster of two CTAs each takes every
-    // other block (local task i is block 2 i + rank) and writes both tables
-    const uint32_t csize = cluster_nctarank(), crank = cluster_ctarank();
-    const uint32_t ntask = csize == 2 ? (p.nblk + 1 - crank) / 2 : p.nblk;
-    auto task_of = [&](uint32_t i) { return csize == 2 ? 2 * i + crank : i; };
-    const uint32_t npr = ntask < p.nrot ? ntask : p.nrot;
-    const uint32_t pr = (uint32_t)warp >> 1;
-    const int t = tid & 63;
-    const bool rotating = pr < npr;
-    const uint32_t nwait = 32 * (2 * npr + 1);
-    const uint32_t act_remote0 = csize == 2 ? mapa_shared(smem_u32(act_s), crank ^ 1u) : 0u;
+    const uint32_t empty0 = bar0 + 8 * kMaxSlots;
+    uint32_t *failed = reinterpret_cast<uint32_t *>(smem + p.off_bar + 16 * kMaxSlots);
+    uint32_t *lastb = failed + 1;               // per slot: the last batch issued into it
+    uint8_t *act = smem + p.off_part;           // operand words, later the partial sums
+    const uint32_t nact = p.nsets * c.ng;        // threads with a group
+    const uint32_t nmw = (nact + 31) / 32;       // warps with work
+    const uint32_t ring_to = min(p.nslots, c.nbatch);
+    const uint32_t pre = min(p.pre_issue, ring_to);
 
-    if (tid == kProducer * 32) {
-        prefetch_tmap(last_cta ? &p.bmap_last : &p.bmap_main);
-        prefetch_tmap(last_cta ? &p.hmap_last : &p.hmap_main);
-        prefetch_tmap(last_cta ? &p.smap_last : &p.smap_main);
+    if (csize == 2) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+    if (tid == 0) {
         for (uint32_t s = 0; s < p.nslots; ++s) {
             mbar_init(bar0 + 8 * s, 1);
-            cnt[s] = 0;
+            mbar_init(empty0 + 8 * s, nmw);
+            lastb[s] = s;
         }
-        mbar_init(rem_bar, 1);
         *failed = 0;
         fence_mbar_init();
-        // weights are read-only parameters: the first chunks and the remainder rows before the dependency wait
-        for (uint32_t i = 0; i < pre; ++i) issue_chunk<kRL>(p, smem, i, last_cta);
-        *issued = pre;
-        if (cr.rem) {
-            const uint32_t rb_bytes = (uint32_t)(p.base_row + p.high_row + p.scale_row);
-            mbar_arrive_expect_tx(rem_bar, cr.rem * rb_bytes);
-            for (uint32_t rr = 0; rr < cr.rem; ++rr) {
-                const uint64_t r = cr.begin + (uint64_t)cr.ntile * TL::rows + rr;
-                const uint32_t dd = smem_u32(rem_s) + rr * rb_bytes;
-                bulk_g2s(dd, p.base + r * p.base_row, (uint32_t)p.base_row, rem_bar);
-                bulk_g2s(dd + (uint32_t)p.base_row, p.high + r * p.high_row, (uint32_t)p.high_row, rem_bar);
-                bulk_g2s(dd + (uint32_t)(p.base_row + p.high_row), p.scale + r * p.scale_row, (uint32_t)p.scale_row,
-                         rem_bar);
-            }
-        }
+        const bool last = c.unit == p.units - 1;
+        prefetch_tmap(last ? &p.bmap_last : &p.bmap_main);
+        prefetch_tmap(last ? &p.hmap_last : &p.hmap_main);
+        prefetch_tmap(last ? &p.smap_last : &p.smap_main);
+        // weights are read-only parameters: the first batches before the dependency wait
+        for (uint32_t b = 0; b < pre; ++b) issue_batch(p, c, smem, b);
     }
-    float v[16], d[16];
-    if (rotating) {
-        // the first rotation of a rotating pair
-        const uint32_t b = task_of(pr);
-        float *scr = reinterpret_cast<float *>(smem + pr * kRotScratchBytes);
-        if (p.signs) load_signs2(p.signs, b, t, d);     // read-only
-        pdl_launch_dependents();
-        pdl_wait();          // x may come from the preceding kernel
-        load_block2<kXType>(p.x, p.k, b, t, v);
-        // x has arrived once its first and last values can be stored; then the
-        // producer may queue the rest of the ring behind it
-        *reinterpret_cast<volatile float *>(scr + 1080 + (t >> 5)) = v[0] + v[15];
-        named_barrier_arrive(kBarX, nwait);
-        rotate_pack_ptq1(p.signs != nullptr, v, d, b, p.groups, act_s, act_remote0, scr, t, kBarPair0 + pr);
-    } else {
-        pdl_launch_dependents();
-        pdl_wait();
-        if (warp == kProducer) {
-            // the rest of the ring, once x has arrived in every rotating warp
-            named_barrier(kBarX, nwait);
-            if (lane == 0) {
-                for (uint32_t i = pre; i < ring_to; ++i) issue_chunk<kRL>(p, smem, i, last_cta);
-                *issued = ring_to;
-            }
-            __syncwarp();
-        }
-    }
+
+    // rotation: warp w takes blocks first + w, first + w + 16, ...
+    const uint32_t b_first = c.g0 / 8;
+    const uint32_t nblk = c.ng ? (c.g0 + c.ng - 1) / 8 - b_first + 1 : 0u;
+    float v[32], d[32];
+    if ((uint32_t)warp < nblk && p.signs) load_signs1(p.signs, b_first + warp, lane, d);      // read-only
+    pdl_launch_dependents();
+    pdl_wait();          // x may come from the preceding kernel; y may still be read by it
+    if (tid == 0)
+        for (uint32_t b = pre; b < ring_to; ++b) issue_batch(p, c, smem, b);
 #pragma unroll 1
-    for (uint32_t i = pr + npr; rotating && i < ntask; i += npr) {     // more blocks than rotating pairs
-        const uint32_t b = task_of(i);
-        if (p.signs) load_signs2(p.signs, b, t, d);
-        load_block2<kXType>(p.x, p.k, b, t, v);
-        rotate_pack_ptq1(p.signs != nullptr, v, d, b, p.groups, act_s, act_remote0,
-                         reinterpret_cast<float *>(smem + pr * kRotScratchBytes), t, kBarPair0 + pr);
+    for (uint32_t task = warp; task < nblk; task += kWarps) {
+        const uint32_t b = b_first + task;
+        if (task != (uint32_t)warp && p.signs) load_signs1(p.signs, b, lane, d);
+        load_block1<kXType>(p.x, p.k, b, lane, v);
+        rotate_pack(p.signs != nullptr, v, d, b, c.g0, c.ng, act, reinterpret_cast<float *>(smem + warp * kRotScratch),
+                    lane);
     }
-    // the operand words are complete in both CTAs of a cluster; the rotation
-    // scratch is free for the digit table
-    if (csize == 2) cluster_sync();
-    else __syncthreads();
+    __syncthreads();     // operand words complete; the rotation scratch is free for the table
     {
-        // digit table, replicated per bank: entry (B, l) at word 32 B + l; thread
-        // tid computes entry tid / 2 and writes 16 of its copies
-        uint32_t B = (uint32_t)tid >> 1, W = 0;
+        // digit table: entry B's 32 lane copies as 8 16-byte stores
+        for (uint32_t i = tid; i < 256 * 8; i += kThreads) {
+            uint32_t B = i >> 3, W = 0;
 #pragma unroll
-        for (int i = 0; i < 5; ++i) {
-            const uint32_t dg = B % 3;
-            B /= 3;
-            W |= i < 4 ? dg << (8 * i) : dg << 2;
+            for (int e = 0; e < 5; ++e) {
+                const uint32_t dg = B % 3;
+                B /= 3;
+                W |= e < 4 ? dg << (8 * e) : dg << 2;
+            }
+            *reinterpret_cast<uint4 *>(smem + (i >> 3) * kLutStride + 16 * (i & 7)) = make_uint4(W, W, W, W);
         }
-        uint4 *dst = reinterpret_cast<uint4 *>(smem + ((tid >> 1) * 32 + 16 * (tid & 1)) * 4);
-        const uint4 w4 = make_uint4(W, W, W, W);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) dst[c] = w4;
     }
-    __syncthreads();
+    const bool math = (uint32_t)tid < nact;
+    const uint32_t gl = math ? (uint32_t)tid % c.ng : 0u, set = math ? (uint32_t)tid / c.ng : 0u;
+    uint32_t av[kActWords];
+    float fx = 0.f;
+    int off = 0;
+    if (math) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(act + gl * kActGroupBytes);
+#pragma unroll
+        for (int i = 0; i < (int)kActWords / 4; ++i) {
+            const uint4 a = src[i];
+            av[4 * i] = a.x;
+            av[4 * i + 1] = a.y;
+            av[4 * i + 2] = a.z;
+            av[4 * i + 3] = a.w;
+        }
+        const float2 e = reinterpret_cast<const float2 *>(act + c.ng * kActGroupBytes)[gl];
+        fx = e.x;
+        off = __float_as_int(e.y);
+    }
+    __syncthreads();     // table built; the operand-word area now takes the partial sums
 
     bool ok = true;
-    const uint32_t *act_w = reinterpret_cast<const uint32_t *>(act_s);
-    const float2 *gs = reinterpret_cast<const float2 *>(act_s + (uint64_t)p.groups * kActGroupBytes);
-    float *part = reinterpret_cast<float *>(smem + p.off_part);
-    float *part_rem = part + kWarps * TL::rows;      // [kMaxRem][groups]
-
-    // remainder rows: lanes = (row, group of the chunk); warp w takes chunks w, w + 16, ...
-    if (cr.rem) {
-        ok = ok && mbar_wait(rem_bar, 0, p.err, p.wait_cycles);
-        const uint32_t rb_bytes = (uint32_t)(p.base_row + p.high_row + p.scale_row);
-        const uint32_t rr = lane >> 4;
-        for (uint32_t ch = warp; ok && ch < p.nch; ch += kWarps) {
-            const uint32_t G = ch * kChunkGroups + (lane & 15);
-            if (rr < cr.rem && G < p.groups) {
-                const uint8_t *row = rem_s + rr * rb_bytes;
-                const uint2 q0 = *reinterpret_cast<const uint2 *>(row + 24 * G);
-                const uint2 q1 = *reinterpret_cast<const uint2 *>(row + 24 * G + 8);
-                const uint2 q2 = *reinterpret_cast<const uint2 *>(row + 24 * G + 16);
-                const uint32_t bw[6] = {q0.x, q0.y, q1.x, q1.y, q2.x, q2.y};
-                const uint32_t hb = *reinterpret_cast<const uint16_t *>(row + p.base_row + 2 * G);
-                const float s = __half2float(*reinterpret_cast<const __half *>(row + p.base_row + p.high_row + 2 * G));
-                const float2 f = gs[G];
-                uint32_t av[64];
-                load_words(act_w + G * kActStride, av);
-                const int dot = group_dot<6, 2, 48, 60>(bw, hb, lut_s, lane4, av);
-                part_rem[rr * p.groups + G] = s * f.x * (float)(dot - __float_as_int(f.y));
+    const uint32_t br = p.nsets * p.u;
+    float *rs = reinterpret_cast<float *>(smem + p.off_rs);     // this CTA's row sums (split ranges)
+    // batch b, once every warp is done with it: its row sums over the CTA's groups
+    // (lanes = rows), then the slot's refill with batch b + nslots
+    auto reduce = [&](uint32_t b) {
+        uint32_t phase;
+        const uint32_t slot = slot_of(b, p.nslots, p.nslots_inv, phase);
+        const uint32_t rows_b = min(br, c.rows - b * br);
+        ok = ok && mbar_wait(empty0 + 8 * slot, phase, p.err, p.wait_cycles);
+        if (ok) {
+            const float *part = reinterpret_cast<const float *>(smem + p.off_part + slot * p.part_slot_bytes);
+            for (uint32_t rr = lane; rr < rows_b; rr += 32) {
+                float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+                uint32_t g = 0;
+                for (; g + 4 <= c.ng; g += 4) {
+                    a0 += part[g * p.part_stride + rr];
+                    a1 += part[(g + 1) * p.part_stride + rr];
+                    a2 += part[(g + 2) * p.part_stride + rr];
+                    a3 += part[(g + 3) * p.part_stride + rr];
+                }
+                for (; g < c.ng; ++g) a0 += part[g * p.part_stride + rr];
+                const float acc = (a0 + a1) + (a2 + a3);
+                const uint32_t row = b * br + rr;
+                if (csize == 2) rs[row] = acc;
+                else store1(p.y, c.r0 + row, p.y_dtype, acc);
             }
         }
-    }
-
-    // tiles: warp w takes group 16 ch + w of chunk (tile, ch), or half of group
-    // 16 ch + w % 8 when the chunk has eight groups; lane l: rows l + 32 q
-    // the 24 base bytes of group g of a chunk's row: three 8-byte words in the
-    // swizzled 128-byte columns (row % 8 pattern); g = warp for a whole group,
-    // warp % 8 for half a group
-    auto base_off = [&](uint32_t g, int i) {
-        const uint32_t o = 24 * g + 8 * i, bx = o >> 7, c16 = (o & 127) >> 4, hf = (o >> 3) & 1;
-        return bx * TL::base_box + lane * 128 + ((c16 ^ (lane & 7)) << 4) + 8 * hf;
+        __syncwarp();
+        if (lane == 0) {
+            if (!ok) {
+                *failed = 1;
+            } else if (!*(volatile uint32_t *)failed && b + p.nslots < c.nbatch) {
+                fence_proxy_async();
+                lastb[slot] = b + p.nslots;
+                issue_batch(p, c, smem, b + p.nslots);
+            }
+        }
+        __syncwarp();
     };
-    const uint32_t bo_f0 = base_off(warp, 0), bo_f1 = base_off(warp, 1), bo_f2 = base_off(warp, 2);
-    const uint32_t bo_h0 = base_off(warp & 7, 0), bo_h1 = base_off(warp & 7, 1), bo_h2 = base_off(warp & 7, 2);
+    const bool dedicated = nmw < (uint32_t)kWarps;     // warp kWarps - 1 adds the partials
+    if ((uint32_t)warp < nmw) {
+        const uint32_t lane4 = 4u * (uint32_t)lane;
+        // group gl: box gl / wg, bytes 24 (gl % wg) of each of its rows
+        const uint32_t rb_b = 24 * p.wg, o_b = (gl / p.wg) * p.bstride + 24 * (gl % p.wg);
+        const uint32_t o_h = p.slot_high + 2 * (c.g0 + gl - c.h0), o_s = p.slot_scale + 2 * (c.g0 + gl - c.h0);
 #pragma unroll 1
-    for (uint32_t tile = 0; tile < cr.ntile; ++tile) {
-        float y[kRL];
-#pragma unroll
-        for (int q = 0; q < kRL; ++q) y[q] = 0.f;
-#pragma unroll 1
-        for (uint32_t ch = 0; ch < p.nch; ++ch) {
-            const uint32_t item = tile * p.nch + ch;
-            const uint32_t cycle = __umulhi(item, p.nslots_inv);      // item / nslots (item < 2^29)
-            const uint32_t slot = item - cycle * p.nslots, phase = cycle & 1;
-            const bool half = p.groups - ch * kChunkGroups <= 8;       // a chunk of eight groups
-            const uint32_t gw = half ? (uint32_t)(warp & 7) : (uint32_t)warp, hh = half ? (uint32_t)(warp >> 3) : 0u;
-            const uint32_t G = ch * kChunkGroups + gw;
+        for (uint32_t b = 0; b < c.nbatch; ++b) {
+            uint32_t phase;
+            const uint32_t slot = slot_of(b, p.nslots, p.nslots_inv, phase);
+            const uint32_t rows_b = min(br, c.rows - b * br);
             ok = ok && mbar_wait(bar0 + 8 * slot, phase, p.err, p.wait_cycles);
-            if (ok && G < p.groups) {
-                const uint8_t *sa = smem + p.off_ring + slot * TL::chunk_bytes;
-                const float2 f = gs[G];
-                if (!half) {
-                    uint32_t av[64];
-                    load_words(act_w + G * kActStride, av);
-                    const int off = __float_as_int(f.y);
-#pragma unroll
-                    for (int q = 0; q < kRL; ++q) {
-                        const uint32_t ro = q * 32 * 128;      // row lane + 32 q of each base box
-                        const uint2 b0 = *reinterpret_cast<const uint2 *>(sa + bo_f0 + ro);
-                        const uint2 b1 = *reinterpret_cast<const uint2 *>(sa + bo_f1 + ro);
-                        const uint2 b2 = *reinterpret_cast<const uint2 *>(sa + bo_f2 + ro);
-                        const uint32_t bw[6] = {b0.x, b0.y, b1.x, b1.y, b2.x, b2.y};
-                        const uint32_t r = lane + 32 * q;
-                        const uint32_t hb = *reinterpret_cast<const uint16_t *>(sa + 3 * TL::base_box + r * 32 + 2 * gw);
-                        const float s = __half2float(
-                            *reinterpret_cast<const __half *>(sa + 3 * TL::base_box + 32 * TL::rows + r * 32 + 2 * gw));
-                        const int dot = group_dot<6, 2, 48, 60>(bw, hb, lut_s, lane4, av);
-                        y[q] = fmaf(s * f.x, (float)(dot - off), y[q]);
-                    }
-                } else {
-                    // half hh of the group: base words 3 hh .. 3 hh + 2 (bytes 12 hh .. 12 hh + 11),
-                    // high byte hh; its 32 operand words: base pairs 24 hh .., fifth-weight
-                    // pairs 48 + 6 hh .., high pairs 60 + 2 hh ..
-                    const uint32_t *src = act_w + G * kActStride;
-                    uint32_t avh[32];
-                    load_words<24>(src + 24 * hh, *reinterpret_cast<uint32_t(*)[24]>(avh));
-                    // (8-byte aligned: a group starts 16-byte aligned, word 48 + 6 hh at byte 192 + 24 hh)
-#pragma unroll
-                    for (int i = 0; i < 3; ++i) {
-                        const uint2 t4 = *reinterpret_cast<const uint2 *>(src + 48 + 6 * hh + 2 * i);
-                        avh[24 + 2 * i] = t4.x;
-                        avh[25 + 2 * i] = t4.y;
-                    }
-                    const uint2 hi = *reinterpret_cast<const uint2 *>(src + 60 + 2 * hh);
-                    avh[30] = hi.x; avh[31] = hi.y;
-                    const int off = hh ? 0 : __float_as_int(f.y);
-#pragma unroll
-                    for (int q = 0; q < kRL; ++q) {
-                        const uint32_t ro = q * 32 * 128;
-                        const uint2 b0 = *reinterpret_cast<const uint2 *>(sa + bo_h0 + ro);
-                        const uint2 b1 = *reinterpret_cast<const uint2 *>(sa + bo_h1 + ro);
-                        const uint2 b2 = *reinterpret_cast<const uint2 *>(sa + bo_h2 + ro);
-                        const uint32_t bh[3] = {hh ? b1.y : b0.x, hh ? b2.x : b0.y, hh ? b2.y : b1.x};
-                        const uint32_t r = lane + 32 * q;
-                        const uint32_t hb = *reinterpret_cast<const uint16_t *>(sa + 3 * TL::base_box + r * 32 + 2 * gw);
-                        const float s = __half2float(
-                            *reinterpret_cast<const __half *>(sa + 3 * TL::base_box + 32 * TL::rows + r * 32 + 2 * gw));
-                        const int dot = group_dot<3, 1, 24, 30>(bh, hh ? hb >> 8 : hb, lut_s, lane4, avh);
-                        y[q] = fmaf(s * f.x, (float)(dot - off), y[q]);
-                    }
+            if (ok && math) {
+                const uint8_t *sa = smem + p.off_ring + slot * p.slot_bytes;
+                float *part = reinterpret_cast<float *>(smem + p.off_part + slot * p.part_slot_bytes) + gl * p.part_stride;
+#pragma unroll 1
+                for (uint32_t i = 0; i < p.u; ++i) {
+                    const uint32_t rb = i * p.nsets + set;
+                    if (rb >= rows_b) break;
+                    const uint8_t *row = sa + rb * rb_b + o_b;
+                    const uint2 b0 = *reinterpret_cast<const uint2 *>(row);
+                    const uint2 b1 = *reinterpret_cast<const uint2 *>(row + 8);
+                    const uint2 b2 = *reinterpret_cast<const uint2 *>(row + 16);
+                    const uint32_t bw[6] = {b0.x, b0.y, b1.x, b1.y, b2.x, b2.y};
+                    const uint32_t hb = *reinterpret_cast<const uint16_t *>(sa + rb * c.hbytes + o_h);
+                    const float s = __half2float(*reinterpret_cast<const __half *>(sa + rb * c.hbytes + o_s));
+                    const int dot = group_dot(bw, hb, smem, lane4, av);
+                    part[rb] = (s * fx) * (float)(dot - off);
                 }
             }
-            // release the slot; the last of its sixteen readers refills it with the chunk nslots further on
             __syncwarp();
             if (lane == 0) {
                 if (!ok) *failed = 1;
-                __threadfence_block();
-                const uint32_t seen = atomicAdd(&cnt[slot], 1u);
-                if (seen == kWarps - 1) {
-                    cnt[slot] = 0;
-                    if (ok && !*(volatile uint32_t *)failed && item + p.nslots < nitems) {
-                        fence_proxy_async();
-                        issue_chunk<kRL>(p, smem, item + p.nslots, last_cta);
-                        atomicAdd(issued, 1u);
-                    }
-                }
+                mbar_arrive(empty0 + 8 * slot);
             }
-            __syncwarp();
+            // warps take the batches' sums in turn, one batch behind their own work
+            if (!dedicated && b >= 1 && (b - 1) % nmw == (uint32_t)warp) reduce(b - 1);
         }
-#pragma unroll
-        for (int q = 0; q < kRL; ++q) part[warp * TL::rows + 32 * q + lane] = y[q];
-        __syncthreads();
-        if (warp < kRL) {
-            const uint32_t rl = warp * 32 + lane;
-            float acc = 0.f;
-#pragma unroll
-            for (int w = 0; w < kWarps; ++w) acc += part[w * TL::rows + rl];
-            const uint32_t row = tile * TL::rows + rl;
-            if (row < cr.rows - cr.rem) store1(p.y, cr.begin + row, p.y_dtype, acc);
-        }
-        __syncthreads();
+        if (!dedicated && c.nbatch >= 1 && (c.nbatch - 1) % nmw == (uint32_t)warp) reduce(c.nbatch - 1);
+    } else if (dedicated && warp == kWarps - 1) {
+#pragma unroll 1
+        for (uint32_t b = 0; b < c.nbatch; ++b) reduce(b);
     }
-    if (cr.rem) {
-        __syncthreads();       // part_rem complete (also when the CTA has no tile)
-        if (warp == 0 && lane < cr.rem) {
-            float acc = 0.f;
-            for (uint32_t G = 0; G < p.groups; ++G) acc += part_rem[lane * p.groups + G];
-            store1(p.y, cr.begin + (uint64_t)cr.ntile * TL::rows + lane, p.y_dtype, acc);
+    __syncthreads();     // every row sum is in place; failures are recorded
+
+    if (csize == 2) {
+        // the other rank's share of the rows this rank finishes arrives in its
+        // second row-sum array (rows_per_cta floats further on)
+        asm volatile("barrier.cluster.wait.aligned;" ::: "memory");     // both CTAs are running
+        const uint32_t half = (c.rows + 1) / 2;
+        if (warp == 0) {
+            const uint32_t lo = crank ? 0u : half, hi = crank ? half : c.rows;     // rows the peer finishes
+            const uint32_t peer = mapa_shared(smem_u32(rs + p.rows_per_cta), crank ^ 1u);
+            for (uint32_t rr = lo + lane; rr < hi; rr += 32) st_cluster_u32(peer + 4 * rr, __float_as_uint(rs[rr]));
+        }
+        cluster_sync();
+        if (warp == 0) {
+            const uint32_t lo = crank ? half : 0u, hi = crank ? c.rows : half;
+            for (uint32_t rr = lo + lane; rr < hi; rr += 32) {
+                const float mine = rs[rr], other = rs[p.rows_per_cta + rr];
+                store1(p.y, c.r0 + rr, p.y_dtype, crank ? other + mine : mine + other);     // rank 0's share first
+            }
         }
     }
-    // after a timed-out wait: let the copies still in flight land (at most one
-    // per slot, the last one issued into it) before the CTA's memory is freed
+    // after a timed-out wait: let the copies still in flight land (the last one
+    // issued into each slot) before the CTA's memory is freed
     if (tid == 0 && *(volatile uint32_t *)failed) {
-        const uint32_t n_issued = *(volatile uint32_t *)issued;
-        for (uint32_t i = n_issued > p.nslots ? n_issued - p.nslots : 0; i < n_issued; ++i)
-            mbar_wait(bar0 + 8 * (i % p.nslots), (i / p.nslots) & 1, p.err, 200000000ll);
-        if (cr.rem) mbar_wait(rem_bar, 0, p.err, 200000000ll);
+        for (uint32_t s = 0; s < ring_to; ++s)
+            mbar_wait(bar0 + 8 * s, (lastb[s] / p.nslots) & 1, p.err, 200000000ll);
     }
 }
 
@@ -545,61 +554,88 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ptq1_int_kernel(const __grid
 bool gemv_ptq1_int_plan(const ninfer_row_split_geometry &g, uint64_t M, bool rotate, int sms, int smem_limit,
                         Ptq1Plan *plan) {
     *plan = Ptq1Plan{};
-    if (M != 1) return false;
+    if (M != 1 || sms < 2) return false;
     if (rotate && g.k % 1024) return false;
-    // high and scale rows must be whole 16-byte units (8 groups) for the boxes and bulk copies
+    // high and scale rows are whole 16-byte units (8 groups), as every copied segment is
     if (g.groups_per_row % 8 || g.base_row_bytes % 16 || g.high_row_bytes % 16 || g.scale_row_bytes % 16) return false;
-    if (g.k > (1u << 24) || g.n > (1ull << 31)) return false;
-    const uint32_t groups = (uint32_t)g.groups_per_row;
+    if (g.base_offset % 16 || g.high_offset % 16 || g.scale_offset % 16) return false;
+    if (g.k > (1u << 24) || g.n > (1ull << 31) || g.n == 0) return false;
+    const uint32_t G = (uint32_t)g.groups_per_row;
     const uint32_t nblk = (uint32_t)((g.k + 1023) / 1024);
-    const uint32_t nch = (groups + kChunkGroups - 1) / kChunkGroups;
-    // one CTA per SM with ~n / SMs rows each; four rows per lane when a CTA has
-    // 256 rows or more (the operand words of a group then serve four rows)
-    const uint64_t grid0 = std::max<uint64_t>(1, std::min<uint64_t>((uint64_t)sms, g.n / 32));
-    const uint64_t R = (g.n + grid0 - 1) / grid0;
-    const uint64_t grid_rows = (g.n + R - 1) / R;
-    const int rl = R >= 256 ? 4 : 1;
-    if ((uint64_t)nch * ((R + 32 * rl - 1) / (32 * rl)) >= (1ull << 29)) return false;
-    // more blocks than rotating pairs: CTA pairs form clusters that share the rotations
-    const bool cluster = grid_rows >= 2 && nblk > kMaxPairs;
-    const uint64_t grid = cluster ? (grid_rows + 1) / 2 * 2 : grid_rows;
-    const uint32_t ntask = cluster ? (nblk + 1) / 2 : nblk;
-    const uint32_t nrot = std::min<uint32_t>(ntask, kMaxPairs);
-    const uint32_t chunk = rl == 4 ? Tile<4>::chunk_bytes : Tile<1>::chunk_bytes;
-    const uint32_t act_bytes = ((groups * (kActGroupBytes + 8) + 15) / 16) * 16;
-    const uint32_t rem_bytes = rl == 1 ? (uint32_t)(kMaxRem * (g.base_row_bytes + g.high_row_bytes + g.scale_row_bytes)) : 0u;
-    const uint32_t part_bytes = (kWarps * 32 * rl + (rl == 1 ? kMaxRem * groups : 0)) * 4;
-    const uint32_t bar_bytes = (kMaxSlots + 2) * 8;
-    const uint32_t cnt_bytes = (kMaxSlots + 4) * 4;
-    const uint32_t fixed = kLutBytes + act_bytes + ((rem_bytes + 15) / 16) * 16 + ((part_bytes + 15) / 16) * 16 +
-                           bar_bytes + cnt_bytes;
-    if ((int64_t)fixed + 2 * (int64_t)chunk > smem_limit) return false;
-    const uint32_t nslots = std::min<uint32_t>(kMaxSlots, (uint32_t)((smem_limit - (int)fixed) / (int)chunk));
+    // split k over a CTA pair when one CTA would rotate in more than one round
+    // (or has more groups than math threads); the split is even (16-byte base rows)
+    bool cluster = nblk > (uint32_t)kWarps || G > (uint32_t)kThreads;
+    uint32_t split = cluster ? (G / 2) & ~1u : G;
+    uint64_t units = (uint64_t)(cluster ? sms / 2 : sms);
+    uint64_t R = (g.n + units - 1) / units;
+    if (cluster && R > kMaxClusterRows) {
+        if (G > (uint32_t)kThreads) return false;
+        cluster = false;
+        split = G;
+        units = (uint64_t)sms;
+        R = (g.n + units - 1) / units;
+    }
+    const uint32_t ng0 = split, ng1 = cluster ? G - split : 0u;
+    const uint32_t ng_max = std::max(ng0, ng1);
+    if (ng_max == 0 || ng_max > (uint32_t)kThreads) return false;
+    const uint64_t used = (g.n + R - 1) / R;
+    // high bytes and scales of a CTA's groups rounded out to 8 groups (the halves
+    // of a split have the same number of groups, and so the same rounded width)
+    auto hseg = [&](uint32_t g0, uint32_t ng) { return 2 * (((g0 + ng + 7) & ~7u) - (g0 & ~7u)); };
+    const uint32_t hb_max = std::max(hseg(0, ng0), cluster ? hseg(split, ng1) : 0u);
+    const uint32_t nsets = (uint32_t)kThreads / ng_max;
+    const uint32_t u = nsets >= 32 ? 1 : 2;
+    const uint32_t br = nsets * u;
+    const uint64_t nbatch = (R + br - 1) / br;
+    // base boxes of wg groups (3 wg <= 255 elements; even, so that every box starts 16-byte aligned)
+    const uint32_t nbx = (ng_max + 83) / 84;
+    const uint32_t wg = ((ng_max + nbx - 1) / nbx + 1) & ~1u;
+    if (nbatch >= (1ull << 29) || hb_max / 8 > 256 || br > 256) return false;
+    // a slot: the batch's base boxes, high bytes and scales, each box 128-byte aligned
+    auto a128 = [](uint32_t b) { return (b + 127) / 128 * 128; };
+    const uint32_t bstride = a128(br * 24 * wg);
+    const uint32_t slot_high = nbx * bstride, slot_scale = slot_high + a128(br * hb_max);
+    const uint32_t slot = slot_scale + a128(br * hb_max);
+    const uint32_t part_stride = br | 1u;      // odd: the writers' lanes hit distinct banks
+    const uint32_t part_slot = (ng_max * part_stride * 4 + 15) / 16 * 16;
+    const uint32_t act = (ng_max * (kActGroupBytes + 8) + 15) / 16 * 16;
+    const uint32_t rs_bytes = cluster ? (uint32_t)((2 * R * 4 + 15) / 16 * 16) : 0u;
+    const uint32_t bar_bytes = kBarBytes;
+    const int64_t avail = (int64_t)smem_limit - kRegion0 - rs_bytes - bar_bytes;
+    uint32_t nslots = (uint32_t)std::min<uint64_t>(kMaxSlots, nbatch);
+    while (nslots > 0 && (int64_t)nslots * slot + std::max<int64_t>(act, (int64_t)nslots * part_slot) > avail)
+        --nslots;
+    if (nslots == 0 || (nslots < 2 && nbatch > 1) || slot >= (1u << 20)) return false;
     plan->ok = true;
-    plan->rl = rl;
     plan->cluster = cluster;
-    plan->grid = (uint32_t)grid;
-    plan->grid_rows = (uint32_t)grid_rows;
+    plan->grid = (uint32_t)(cluster ? 2 * used : used);
+    plan->units = (uint32_t)used;
     plan->rows_per_cta = (uint32_t)R;
-    plan->nch = nch;
+    plan->ng = ng_max;
+    plan->hbytes = hb_max;
+    plan->wg = wg;
+    plan->nbx = nbx;
+    plan->bstride = bstride;
+    plan->split = split;
+    plan->nsets = nsets;
+    plan->u = u;
     plan->nslots = nslots;
-    plan->pre_issue = std::min<uint32_t>(1, nslots);
-    plan->nrot = nrot;
-    uint32_t off = kLutBytes;     // the table (and, before it, the rotation scratch) starts the shared memory
+    plan->pre_issue = 1;
+    plan->slot_bytes = slot;
+    plan->slot_high = slot_high;
+    plan->slot_scale = slot_scale;
+    plan->part_stride = part_stride;
+    plan->part_slot_bytes = part_slot;
+    uint32_t off = kRegion0;      // the table (and, before it, the rotation scratch) starts the shared memory
     plan->off_ring = off;
-    off += nslots * chunk;
-    plan->off_act = off;
-    off += act_bytes;
-    plan->off_rem = off;
-    off += ((rem_bytes + 15) / 16) * 16;
+    off += nslots * slot;
     plan->off_part = off;
-    off += ((part_bytes + 15) / 16) * 16;
+    off += std::max(act, nslots * part_slot);
+    plan->off_rs = off;
+    off += rs_bytes;
     plan->off_bar = off;
     off += bar_bytes;
-    plan->off_cnt = off;
-    off += cnt_bytes;
     plan->smem = off;
-    plan->act_bytes = act_bytes;
     plan->workspace = 0;
     return true;
 }
@@ -610,65 +646,64 @@ int gemv_ptq1_int_launch(const Ptq1Plan &plan, const uint8_t *payload, const nin
     (void)workspace;
     Ptq1Params p;
     std::memset(&p, 0, sizeof p);
-    p.base = payload + g.base_offset;
-    p.high = payload + g.high_offset;
-    p.scale = payload + g.scale_offset;
-    p.base_row = g.base_row_bytes;
-    p.high_row = g.high_row_bytes;
-    p.scale_row = g.scale_row_bytes;
-    p.x = x;
-    p.signs = signs;
-    p.act_bytes = plan.act_bytes;
-    p.y = y;
-    p.n = g.n;
-    p.k = (uint32_t)g.k;
-    p.groups = (uint32_t)g.groups_per_row;
-    p.nblk = (uint32_t)((g.k + 1023) / 1024);
-    p.nch = plan.nch;
-    p.rows_per_cta = plan.rows_per_cta;
-    p.grid_rows = plan.grid_rows;
-    p.x_dtype = x_dtype;
-    p.y_dtype = y_dtype;
-    p.nslots = plan.nslots;
-    p.nslots_inv = (uint32_t)((1ull << 32) / plan.nslots + 1);
-    p.pre_issue = plan.pre_issue;
-    p.nrot = plan.nrot;
-    p.off_ring = plan.off_ring;
-    p.off_act = plan.off_act;
-    p.off_rem = plan.off_rem;
-    p.off_part = plan.off_part;
-    p.off_bar = plan.off_bar;
-    p.off_cnt = plan.off_cnt;
-    p.wait_cycles = wait_limit_cycles();
-    int st = device_error_word(&p.err);
-    if (st) return st;
-    const uint32_t box_rows = 32u * (uint32_t)plan.rl;
-    const uint64_t R = plan.rows_per_cta, G = plan.grid_rows, last_rows = g.n - (G - 1) * R;
-    if (G > 1) {
-        st = encode_row_tiles(&p.bmap_main, p.base, g.base_row_bytes, R, G - 1, 128, box_rows, true);
-        if (!st) st = encode_row_tiles(&p.hmap_main, p.high, g.high_row_bytes, R, G - 1, 32, box_rows, false);
-        if (!st) st = encode_row_tiles(&p.smap_main, p.scale, g.scale_row_bytes, R, G - 1, 32, box_rows, false);
+    const uint8_t *base = payload + g.base_offset, *high = payload + g.high_offset, *scale = payload + g.scale_offset;
+    if (!aligned(base, 16) || !aligned(high, 16) || !aligned(scale, 16))
+        return fail(NINFER_ERR_ALIGNMENT, "ptq1 gemv: planes must start 16-byte aligned");
+    const uint64_t G = g.groups_per_row, R = plan.rows_per_cta, U = plan.units, last_rows = g.n - (U - 1) * R;
+    const uint32_t br = plan.nsets * plan.u;
+    const uint32_t bbox[3] = {3 * plan.wg, br, 1}, hbox[3] = {plan.hbytes / 8, br, 1};
+    int st = NINFER_OK;
+    if (U > 1) {
+        st = encode_3d_u64(&p.bmap_main, base, {3 * G, R, U - 1}, {g.base_row_bytes, R * g.base_row_bytes}, bbox);
+        if (!st) st = encode_3d_u64(&p.hmap_main, high, {G / 4, R, U - 1}, {g.high_row_bytes, R * g.high_row_bytes}, hbox);
+        if (!st)
+            st = encode_3d_u64(&p.smap_main, scale, {G / 4, R, U - 1}, {g.scale_row_bytes, R * g.scale_row_bytes}, hbox);
         if (st) return st;
     }
-    const uint64_t lr = (G - 1) * R;
-    st = encode_rows(&p.bmap_last, p.base + lr * g.base_row_bytes, g.base_row_bytes, last_rows, 128, box_rows, true);
+    const uint64_t lr = (U - 1) * R;
+    st = encode_3d_u64(&p.bmap_last, base + lr * g.base_row_bytes, {3 * G, last_rows, 1},
+                       {g.base_row_bytes, last_rows * g.base_row_bytes}, bbox);
     if (!st)
-        st = encode_rows(&p.hmap_last, p.high + lr * g.high_row_bytes, g.high_row_bytes, last_rows, 32, box_rows,
-                         false);
+        st = encode_3d_u64(&p.hmap_last, high + lr * g.high_row_bytes, {G / 4, last_rows, 1},
+                           {g.high_row_bytes, last_rows * g.high_row_bytes}, hbox);
     if (!st)
-        st = encode_rows(&p.smap_last, p.scale + lr * g.scale_row_bytes, g.scale_row_bytes, last_rows, 32, box_rows,
-                         false);
+        st = encode_3d_u64(&p.smap_last, scale + lr * g.scale_row_bytes, {G / 4, last_rows, 1},
+                           {g.scale_row_bytes, last_rows * g.scale_row_bytes}, hbox);
     if (st) return st;
-    void (*kernel)(Ptq1Params) = nullptr;
-    if (plan.rl == 4) {
-        kernel = x_dtype == NINFER_F32 ? gemv_ptq1_int_kernel<4, NINFER_F32>
-                 : x_dtype == NINFER_BF16 ? gemv_ptq1_int_kernel<4, NINFER_BF16>
-                                          : gemv_ptq1_int_kernel<4, NINFER_F16>;
-    } else {
-        kernel = x_dtype == NINFER_F32 ? gemv_ptq1_int_kernel<1, NINFER_F32>
-                 : x_dtype == NINFER_BF16 ? gemv_ptq1_int_kernel<1, NINFER_BF16>
-                                          : gemv_ptq1_int_kernel<1, NINFER_F16>;
-    }
+    p.x = x;
+    p.signs = signs;
+    p.y = y;
+    p.n = g.n;
+    p.units = plan.units;
+    p.k = (uint32_t)g.k;
+    p.groups = (uint32_t)g.groups_per_row;
+    p.split = plan.split;
+    p.rows_per_cta = plan.rows_per_cta;
+    p.nsets = plan.nsets;
+    p.u = plan.u;
+    p.wg = plan.wg;
+    p.nbx = plan.nbx;
+    p.bstride = plan.bstride;
+    p.nslots = plan.nslots;
+    p.nslots_inv = (uint32_t)((1ull << 32) / plan.nslots + 1);
+    p.pre_issue = pdl ? plan.pre_issue : 0u;
+    p.slot_bytes = plan.slot_bytes;
+    p.slot_high = plan.slot_high;
+    p.slot_scale = plan.slot_scale;
+    p.part_stride = plan.part_stride;
+    p.part_slot_bytes = plan.part_slot_bytes;
+    p.off_ring = plan.off_ring;
+    p.off_part = plan.off_part;
+    p.off_rs = plan.off_rs;
+    p.off_bar = plan.off_bar;
+    p.x_dtype = x_dtype;
+    p.y_dtype = y_dtype;
+    p.wait_cycles = wait_limit_cycles();
+    st = device_error_word(&p.err);
+    if (st) return st;
+    void (*kernel)(Ptq1Params) = x_dtype == NINFER_F32    ? gemv_ptq1_int_kernel<NINFER_F32>
+                                 : x_dtype == NINFER_BF16 ? gemv_ptq1_int_kernel<NINFER_BF16>
+                                                          : gemv_ptq1_int_kernel<NINFER_F16>;
     st = set_smem_attribute((const void *)kernel, (int)plan.smem);
     if (st) return st;
     cudaLaunchConfig_t cfg = {};

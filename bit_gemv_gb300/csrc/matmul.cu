@@ -77,7 +77,7 @@ int plan_matmul(int fmt, const ninfer_row_split_geometry &g, uint64_t M, bool ro
         mp->workspace = mp->gmma.workspace;     // the activation fragments
         return NINFER_OK;
     }
-    if (fmt == NINFER_PTQ1_0_G128 && M >= 2 && gemv_ptq1_mma_plan(g, M, rotate, d.sms, d.smem_optin, &mp->gpm)) {
+    if (fmt == NINFER_PTQ1_0_G128 && gemv_ptq1_mma_plan(g, M, rotate, d.sms, d.smem_optin, &mp->gpm)) {
         mp->path = Path::kMmaPtq1;
         mp->workspace = mp->gpm.workspace;      // per-block partial sums
         return NINFER_OK;
