@@ -74,10 +74,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// The same test, but the thread may stay suspended in the barrier for up to
+// `ns` nanoseconds while the phase is incomplete (instead of spinning, which
+// takes issue slots from the warps that share its scheduler).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Waits for the phase with the given parity to complete; gives up after about
 // `cycles` SM clocks (~2 s), sets kErrBarrierTimeout in *err and returns false.
 // cycles <= 0 gives up at once, without looking at the barrier (the failure
-// path's test hook).
+// path's test hook). While waiting the thread sleeps in the barrier for up to
+// 100 us at a time.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t *err,
                                           long long cycles = 4000000000ll) {
     if (cycles <= 0) {
@@ -86,7 +100,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_
     }
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity)) {
+    while (!mbar_try_wait_sleep(bar, parity, 100000u)) {
         if (clock64() - t0 > cycles) {
             atomicOr(err, kErrBarrierTimeout);
             return false;

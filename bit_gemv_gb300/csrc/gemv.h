@@ -69,8 +69,8 @@ int gemv_pq2_int_launch(const IntPlan &plan, const uint8_t *payload, const ninfe
 // M = 1 integer kernel (PTQ1_0_G128), rotation fused in.
 struct Ptq1Plan {
     bool ok;
-    bool cluster;            // CTA pairs split the groups of one row range (grid even)
-    uint32_t grid, units, rows_per_cta, split, ng, hbytes, wg, nbx, bstride, nsets, u, nslots, pre_issue;
+    uint32_t cluster;        // CTAs of a cluster, which split the groups of one row range (1: none)
+    uint32_t grid, units, rows_per_cta, ng, hbytes, wg, nbx, bstride, nsets, u, nslots, pre_issue;
     uint32_t slot_bytes, slot_high, slot_scale, part_stride, part_slot_bytes;
     uint32_t off_ring, off_part, off_rs, off_bar, smem;
     uint64_t workspace;

@@ -9,16 +9,16 @@
 // byte j of a group holds weights 5j .. 5j+4 as (byte / 3^i) % 3, high byte h
 // holds weights 120 + 4h .. 123 + 4h; one binary16 scale per group.
 //
-// Work split: a CTA owns a contiguous range of rows. When its sixteen warps
-// could not rotate all 1024-blocks of k in one round, two CTAs of a cluster
-// share a row range and split the groups in halves: each rotates and reads only
-// its half, and the two partial row sums meet through distributed shared memory
-// at the end (rank 0 finishes the first half of the rows, rank 1 the second).
+// Work split: a CTA owns a contiguous range of rows. When its eight warp pairs
+// could not rotate all 1024-blocks of k in one round, two or four CTAs of a
+// cluster share a row range and split its groups: each rotates and reads only
+// its share, and the partial row sums meet through distributed shared memory at
+// the end (rank r finishes the r-th part of the rows, adding the ranks' sums in
+// rank order).
 //
-// Activation: each warp rotates one of the CTA's blocks in registers (element
-// bits {0,1,2,8,9} in the registers, then, after a transpose through the
-// warp's scratch, bits 3-7), rounds it to 16-bit fixed point (x16 =
-// rint(xr * 2^E'), max |x16| < 2^14) and packs, per group, 64 operand words: for base byte
+// Activation: a warp pair rotates each of the CTA's blocks and rounds it to
+// 16-bit fixed point (rot2.cuh: x16 = rint(xr * 2^E'), max |x16| < 2^14), then
+// packs, per group, 64 operand words: for base byte
 // j (< 24), (x16[5j], x16[5j+1]) and (x16[5j+2], x16[5j+3]); for the four bytes
 // 4q .. 4q+3, the pairs of their fifth weights (x16[5(4q+2c)+4],
 // x16[5(4q+2c+1)+4]); for high byte h, its two pairs; and one group entry
@@ -52,6 +52,7 @@
 // the end); all exact in int32. Per group:
 //   y += scale * 2^-E * (sum t x16 - sum x16)                    (value = t - 1)
 #include <cstring>
+#include <mutex>
 
 #include <cuda.h>
 #include <cuda_fp16.h>
@@ -78,11 +79,12 @@ static_assert(kActStride >= kActWords && kActStride % 8 == 4, "operand words: an
 constexpr uint32_t kActGroupBytes = kActStride * 4;
 constexpr uint32_t kLutStride = 256;        // entry B at B * 256: 32 lane copies, then unused
 constexpr uint32_t kLutBytes = 256 * kLutStride;
-// a warp's rotation scratch: 1024 fp32 values, element e at e + 8 (e >> 8)
-constexpr uint32_t kRotScratch = 4 * 264 * 4;
-// the table, and before it the warps' rotation scratch, start the shared memory
-constexpr uint32_t kRegion0 = (kWarps * kRotScratch > kLutBytes ? kWarps * kRotScratch : kLutBytes);
+constexpr uint32_t kPairs = kWarps / 2;     // rotating warp pairs; named barriers 1 .. 8
+constexpr uint32_t kBarPair0 = 1;
+// the table, and before it the pairs' rotation scratch, start the shared memory
+constexpr uint32_t kRegion0 = (kPairs * kRotScratchBytes > kLutBytes ? kPairs * kRotScratchBytes : kLutBytes);
 static_assert(kRegion0 % 128 == 0, "ring slots 128-byte aligned");
+static_assert(kBarPair0 + kPairs <= 16, "named barriers");
 constexpr uint32_t kMaxClusterRows = 4096;  // rows of a split range (their partial sums stay in shared memory)
 // after the full and empty barriers of the slots: the failure flag, then per slot
 // the last batch issued into it
@@ -98,8 +100,9 @@ struct Ptq1Params {
     void *y;
     uint64_t n;
     uint32_t units;                 // row ranges (CTAs, or CTA pairs when clustered)
-    uint32_t k, groups, split;      // split: groups of cluster rank 0 (all groups without a cluster)
-    uint32_t rows_per_cta;          // rows of a CTA (of a CTA pair when clustered)
+    uint32_t k, groups;
+    uint32_t rows_per_cta;          // rows of a CTA (of a cluster when clustered)
+    uint32_t hbytes;                // high bytes (and scales) per row in a slot: the same for every rank
     uint32_t nsets, u;              // row sets and rows per set of a batch
     uint32_t wg, nbx, bstride;      // groups per base box, base boxes per batch, their distance in a slot
     uint32_t nslots, nslots_inv, pre_issue;
@@ -112,7 +115,8 @@ struct Ptq1Params {
 };
 
 // This CTA's share: row range unit (rows [r0, r0 + rows)), groups [g0, g0 + ng),
-// high bytes and scales of groups [h0, h0 + hbytes / 2).
+// high bytes and scales of groups [h0, h0 + hbytes / 2) (a slot holds the plan's
+// width from h0, which covers them).
 struct Cta {
     uint64_t r0;
     uint32_t unit, rows, g0, ng, h0, hbytes, nbatch;
@@ -124,8 +128,10 @@ __device__ __forceinline__ Cta cta_share(const Ptq1Params &p, uint32_t csize, ui
     c.r0 = (uint64_t)c.unit * p.rows_per_cta;
     const uint64_t left = c.r0 < p.n ? p.n - c.r0 : 0;
     c.rows = left < p.rows_per_cta ? (uint32_t)left : p.rows_per_cta;
-    c.g0 = crank ? p.split : 0u;
-    c.ng = csize == 2 ? (crank ? p.groups - p.split : p.split) : p.groups;
+    // rank r of C: groups [s_r, s_{r+1}), s_r = floor(r G / C) rounded down to even
+    auto split = [&](uint32_t r) { return r >= csize ? p.groups : ((r * p.groups) / csize) & ~1u; };
+    c.g0 = split(crank);
+    c.ng = split(crank + 1) - c.g0;
     c.h0 = c.g0 & ~7u;
     c.hbytes = 2 * (((c.g0 + c.ng + 7) & ~7u) - c.h0);
     const uint32_t br = p.nsets * p.u;
@@ -146,7 +152,7 @@ __device__ __forceinline__ void issue_batch(const Ptq1Params &p, const Cta &c, u
     uint32_t phase;
     const uint32_t slot = slot_of(b, p.nslots, p.nslots_inv, phase);
     const uint32_t bar = smem_u32(smem + p.off_bar) + 8 * slot;
-    mbar_arrive_expect_tx(bar, br * (24 * p.wg * p.nbx + 2 * c.hbytes));
+    mbar_arrive_expect_tx(bar, br * (24 * p.wg * p.nbx + 2 * p.hbytes));
     const uint32_t dst = smem_u32(smem + p.off_ring) + slot * p.slot_bytes;
     const bool last = c.unit == p.units - 1;
     const int y = (int)(b * br), z = last ? 0 : (int)c.unit;
@@ -156,161 +162,59 @@ __device__ __forceinline__ void issue_batch(const Ptq1Params &p, const Cta &c, u
     tma_load_3d(dst + p.slot_scale, last ? &p.smap_last : &p.smap_main, (int)(c.h0 / 4), y, z, bar);
 }
 
-// Block b of x (and its signs) as one warp holds it: v[8 i + e] = element
-// 1024 b + 256 i + 8 lane + e; zero past k.
-template <int kXType>
-__device__ __forceinline__ void load_block1(const void *x, uint32_t k, uint32_t b, int lane, float (&v)[32]) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        float u[8];
-        const uint64_t idx = (uint64_t)b * 1024 + 256 * i + 8 * lane;
-        if (idx + 8 <= k) {
-            load8(x, idx, kXType, u);
-        } else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) u[e] = idx + e < k ? load1(x, idx + e, kXType) : 0.f;
-        }
-#pragma unroll
-        for (int e = 0; e < 8; ++e) v[8 * i + e] = u[e];
-    }
-}
-
-__device__ __forceinline__ void load_signs1(const uint16_t *s, uint32_t b, int lane, float (&d)[32]) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        float u[8];
-        load_signs8(s, (uint64_t)b * 1024 + 256 * i + 8 * lane, u);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) d[8 * i + e] = u[e];
-    }
-}
-
-// Butterflies over the five register index bits of 32 values: bits 1-4 as
-// paired fp32 adds and subtracts (each element rounded exactly as by a scalar
-// add), bit 0 within the pairs.
-__device__ __forceinline__ void butterfly32(float (&v)[32]) {
-    uint64_t w[16];
-#pragma unroll
-    for (int m = 0; m < 16; ++m) w[m] = f2pack(v[2 * m], v[2 * m + 1]);
-#pragma unroll
-    for (int bit = 0; bit < 4; ++bit)
-#pragma unroll
-        for (int m = 0; m < 16; ++m) {
-            if (m & (1 << bit)) continue;
-            uint64_t sum, dif;
-            asm("add.rn.f32x2 %0, %1, %2;" : "=l"(sum) : "l"(w[m]), "l"(w[m | (1 << bit)]));
-            asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(dif) : "l"(w[m]), "l"(w[m | (1 << bit)]));
-            w[m] = sum;
-            w[m | (1 << bit)] = dif;
-        }
-#pragma unroll
-    for (int m = 0; m < 16; ++m) {
-        float a, c;
-        f2unpack(w[m], a, c);
-        v[2 * m] = a + c;
-        v[2 * m + 1] = a - c;
-    }
-}
-
-// Rotates block b with one warp (x in v as load_block1 leaves it; signs in d
-// unless rotate is false), rounds it to x16 = rint(v * 2^E) with E chosen so
-// that max |x16| < 2^14 (v = H (D x) = 32 xr, or x unrotated), and writes the
-// operand words and group entries {2^-E (with the transform's 1/32), sum of
-// the group's x16 (int bits)} of those of its eight groups that lie in
-// [g0, g0 + ng) (local index G - g0). The element bits held in registers are
-// first {0,1,2,8,9} (lane = bits 3-7), then, after a transpose through the
-// scratch, bits 3-7 (lane = {0,1,2,8,9}); the rounded values go back through
-// the scratch as int16 in natural order (element e at e + 16 (e >> 8)).
-__device__ __forceinline__ void rotate_pack(bool rotate, float (&v)[32], const float (&d)[32], uint32_t b,
-                                            uint32_t g0, uint32_t ng, uint8_t *act, float *scr, int lane) {
-    if (rotate) {
-#pragma unroll
-        for (int m = 0; m < 16; ++m) {
-            uint64_t r;
-            asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2pack(v[2 * m], v[2 * m + 1])),
-                "l"(f2pack(d[2 * m], d[2 * m + 1])));
-            f2unpack(r, v[2 * m], v[2 * m + 1]);
-        }
-        butterfly32(v);      // element bits 0, 1, 2, 8, 9
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int c = 0; c < 2; ++c)
-            *reinterpret_cast<float4 *>(scr + 264 * i + 8 * lane + 4 * c) =
-                make_float4(v[8 * i + 4 * c], v[8 * i + 4 * c + 1], v[8 * i + 4 * c + 2], v[8 * i + 4 * c + 3]);
-    __syncwarp();
-    // lane = element bits (0, 1, 2, 8, 9), register j = bits 3-7: e = (lane & 7) + 8 j + 256 (lane >> 3)
-    const int base = (lane & 7) + 264 * (lane >> 3);
-#pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] = scr[base + 8 * j];
-    if (rotate) butterfly32(v);      // element bits 3-7
-    // block maximum: a tree in registers, then the warp (a non-negative float's
-    // bits order as its value: one warp-wide integer max)
-    float m[16];
-#pragma unroll
-    for (int j = 0; j < 16; ++j) m[j] = fmaxf(fabsf(v[j]), fabsf(v[j + 16]));
-#pragma unroll
-    for (int w = 8; w > 0; w >>= 1)
-#pragma unroll
-        for (int j = 0; j < w; ++j) m[j] = fmaxf(m[j], m[j + w]);
-    const float mx = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(m[0])));
-    int E = 0;
-    if (mx > 0.f) E = 13 - ilogbf(mx);     // max |x16| < 2^14
-    E = max(-100, min(100, E));
-    const float up = ldexpf(1.f, E);
+// Rotates block b with the pair and writes the operand words and group entries
+// {2^-E (with the transform's 1/32), sum of the group's x16 (int bits)} of those
+// of its eight groups that lie in [g0, g0 + ng) (local index G - g0).
+__device__ __forceinline__ void rotate_pack(bool rotate, float (&v)[16], const float (&d)[16], uint32_t b,
+                                            uint32_t g0, uint32_t ng, uint8_t *act, float *scr, int t, uint32_t bar) {
+    const int lane = t & 31;
+    uint32_t qb[16];
+    const int E = rotate_quant2(rotate, v, d, scr, t, bar, qb);
     const float f = ldexpf(1.f, -E - (rotate ? 5 : 0));
-    __syncwarp();        // every lane has read its transposed values
-    // x16 = rint(v * 2^E): adding 1.5 * 2^23 rounds to nearest (ties to even) and
-    // leaves x16 in the low 16 bits; group (element bits 7-9) sums: bit 7 = j >> 4,
-    // bits 8-9 = lane >> 3
+    // x16 in natural order (int16) in the scratch: elements 512 i + 8 t .. + 7
     int16_t *qs = reinterpret_cast<int16_t *>(scr);
-    const int qbase = (lane & 7) + 272 * (lane >> 3);
-    int gsum[2] = {0, 0};
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-        const int q = __float_as_int(fmaf(v[j], up, 12582912.0f)) - 0x4B400000;
-        gsum[j >> 4] += q;
-        qs[qbase + 8 * j] = (int16_t)q;
-    }
-#pragma unroll
-    for (int h = 0; h < 2; ++h)
-#pragma unroll
-        for (int sh = 1; sh < 8; sh <<= 1) gsum[h] += __shfl_xor_sync(0xffffffffu, gsum[h], sh);
     float2 *gs = reinterpret_cast<float2 *>(act + ng * kActGroupBytes);
-    if ((lane & 7) == 0) {
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const uint32_t L = b * 8 + 2 * (lane >> 3) + h - g0;     // wraps past ng when below g0
-            if (L < ng) gs[L] = make_float2(f, __int_as_float(gsum[h]));
-        }
+    for (int i = 0; i < 2; ++i) {
+        const uint32_t *q = qb + 8 * i;
+        uint4 w;
+        w.x = __byte_perm(q[0], q[1], 0x5410);
+        w.y = __byte_perm(q[2], q[3], 0x5410);
+        w.z = __byte_perm(q[4], q[5], 0x5410);
+        w.w = __byte_perm(q[6], q[7], 0x5410);
+        *reinterpret_cast<uint4 *>(qs + 512 * i + 8 * t) = w;
+        // the group's sum of x16 (group 4 i + t / 16 of the block): the 16 lanes of each half-warp
+        const int sum = (int)(q[0] + q[1] + q[2] + q[3] + q[4] + q[5] + q[6] + q[7] - 8u * 0x4B400000u);
+        const int s_lo = __reduce_add_sync(0xffffffffu, lane < 16 ? sum : 0);
+        const int s_hi = __reduce_add_sync(0xffffffffu, lane < 16 ? 0 : sum);
+        const uint32_t L = b * 8 + 4 * i + (t >> 4) - g0;     // wraps past ng when below g0
+        if ((lane & 15) == 0 && L < ng) gs[L] = make_float2(f, __int_as_float(lane < 16 ? s_lo : s_hi));
     }
-    __syncwarp();
+    named_barrier(bar, 64);
     // operand words: the block's 8 groups have 208 code bytes (192 base, 16 high);
-    // lane l takes bytes l, l + 32, ..; group gl's elements start at 128 gl + 16 (gl >> 1)
+    // thread t takes bytes t, t + 64, t + 128 and t + 192
     uint32_t *aw = reinterpret_cast<uint32_t *>(act);
 #pragma unroll
-    for (int i = 0; i < 7; ++i) {
-        const uint32_t u = lane + 32 * i;
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t u = t + 64 * i;
         if (u >= 208) break;
         const uint32_t gl = u < 192 ? u / 24 : (u - 192) >> 1, L = b * 8 + gl - g0;
         if (L >= ng) continue;
         uint32_t *dst = aw + L * kActStride;
-        const int16_t *grp = qs + 128 * gl + 16 * (gl >> 1);
         if (u < 192) {
             const uint32_t j = u % 24;
-            const int16_t *e = grp + 5 * j;
+            const int16_t *e = qs + 128 * gl + 5 * j;
             dst[2 * j] = (uint32_t)(uint16_t)e[0] | ((uint32_t)(uint16_t)e[1] << 16);
             dst[2 * j + 1] = (uint32_t)(uint16_t)e[2] | ((uint32_t)(uint16_t)e[3] << 16);
             reinterpret_cast<int16_t *>(dst + 48 + 2 * (j >> 2) + ((j >> 1) & 1))[j & 1] = e[4];
         } else {
             const uint32_t hh = (u - 192) & 1;
-            const int16_t *e = grp + 120 + 4 * hh;
+            const int16_t *e = qs + 128 * gl + 120 + 4 * hh;
             dst[60 + 2 * hh] = (uint32_t)(uint16_t)e[0] | ((uint32_t)(uint16_t)e[1] << 16);
             dst[61 + 2 * hh] = (uint32_t)(uint16_t)e[2] | ((uint32_t)(uint16_t)e[3] << 16);
         }
     }
-    __syncwarp();        // the scratch may be reused
+    named_barrier(bar, 64);      // the scratch may be reused
 }
 
 // Lane's copy of the table entry of byte c of w: lut + (B_c << 8 | lane4).
@@ -356,7 +260,7 @@ template <int kXType>
 __global__ void __launch_bounds__(kThreads, 1) gemv_ptq1_int_kernel(const __grid_constant__ Ptq1Params p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const uint32_t csize = cluster_nctarank(), crank = csize == 2 ? cluster_ctarank() : 0u;
+    const uint32_t csize = cluster_nctarank(), crank = csize > 1 ? cluster_ctarank() : 0u;
     const Cta c = cta_share(p, csize, crank);
     const uint32_t bar0 = smem_u32(smem + p.off_bar);
     const uint32_t empty0 = bar0 + 8 * kMaxSlots;
@@ -385,22 +289,24 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ptq1_int_kernel(const __grid
         for (uint32_t b = 0; b < pre; ++b) issue_batch(p, c, smem, b);
     }
 
-    // rotation: warp w takes blocks first + w, first + w + 16, ...
+    // rotation: pair pr takes blocks first + pr, first + pr + 8, ...
     const uint32_t b_first = c.g0 / 8;
     const uint32_t nblk = c.ng ? (c.g0 + c.ng - 1) / 8 - b_first + 1 : 0u;
-    float v[32], d[32];
-    if ((uint32_t)warp < nblk && p.signs) load_signs1(p.signs, b_first + warp, lane, d);      // read-only
+    const uint32_t pr = (uint32_t)warp >> 1;
+    const int t = tid & 63;
+    float v[16], d[16];
+    if (pr < nblk && p.signs) load_signs2(p.signs, b_first + pr, t, d);      // read-only
     pdl_launch_dependents();
     pdl_wait();          // x may come from the preceding kernel; y may still be read by it
     if (tid == 0)
         for (uint32_t b = pre; b < ring_to; ++b) issue_batch(p, c, smem, b);
 #pragma unroll 1
-    for (uint32_t task = warp; task < nblk; task += kWarps) {
+    for (uint32_t task = pr; task < nblk; task += kPairs) {
         const uint32_t b = b_first + task;
-        if (task != (uint32_t)warp && p.signs) load_signs1(p.signs, b, lane, d);
-        load_block1<kXType>(p.x, p.k, b, lane, v);
-        rotate_pack(p.signs != nullptr, v, d, b, c.g0, c.ng, act, reinterpret_cast<float *>(smem + warp * kRotScratch),
-                    lane);
+        if (task != pr && p.signs) load_signs2(p.signs, b, t, d);
+        load_block2<kXType>(p.x, p.k, b, t, v);
+        rotate_pack(p.signs != nullptr, v, d, b, c.g0, c.ng, act, reinterpret_cast<float *>(smem + pr * kRotScratchBytes),
+                    t, kBarPair0 + pr);
     }
     __syncthreads();     // operand words complete; the rotation scratch is free for the table
     {
@@ -461,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ptq1_int_kernel(const __grid
                 for (; g < c.ng; ++g) a0 += part[g * p.part_stride + rr];
                 const float acc = (a0 + a1) + (a2 + a3);
                 const uint32_t row = b * br + rr;
-                if (csize == 2) rs[row] = acc;
+                if (csize > 1) rs[row] = acc;
                 else store1(p.y, c.r0 + row, p.y_dtype, acc);
             }
         }
@@ -501,8 +407,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ptq1_int_kernel(const __grid
                     const uint2 b1 = *reinterpret_cast<const uint2 *>(row + 8);
                     const uint2 b2 = *reinterpret_cast<const uint2 *>(row + 16);
                     const uint32_t bw[6] = {b0.x, b0.y, b1.x, b1.y, b2.x, b2.y};
-                    const uint32_t hb = *reinterpret_cast<const uint16_t *>(sa + rb * c.hbytes + o_h);
-                    const float s = __half2float(*reinterpret_cast<const __half *>(sa + rb * c.hbytes + o_s));
+                    const uint32_t hb = *reinterpret_cast<const uint16_t *>(sa + rb * p.hbytes + o_h);
+                    const float s = __half2float(*reinterpret_cast<const __half *>(sa + rb * p.hbytes + o_s));
                     const int dot = group_dot(bw, hb, smem, lane4, av);
                     part[rb] = (s * fx) * (float)(dot - off);
                 }
@@ -522,22 +428,27 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ptq1_int_kernel(const __grid
     }
     __syncthreads();     // every row sum is in place; failures are recorded
 
-    if (csize == 2) {
-        // the other rank's share of the rows this rank finishes arrives in its
-        // second row-sum array (rows_per_cta floats further on)
-        asm volatile("barrier.cluster.wait.aligned;" ::: "memory");     // both CTAs are running
-        const uint32_t half = (c.rows + 1) / 2;
+    if (csize > 1) {
+        // rows split in csize parts of rq rows; rank q finishes part q: every rank
+        // stores its sums for part q in rank q's inbox (row sums rows_per_cta
+        // floats on: csize arrays of rq floats, one per source rank)
+        asm volatile("barrier.cluster.wait.aligned;" ::: "memory");     // every CTA of the cluster is running
+        const uint32_t rq = (c.rows + csize - 1) / csize;
+        float *inbox = rs + p.rows_per_cta;
         if (warp == 0) {
-            const uint32_t lo = crank ? 0u : half, hi = crank ? half : c.rows;     // rows the peer finishes
-            const uint32_t peer = mapa_shared(smem_u32(rs + p.rows_per_cta), crank ^ 1u);
-            for (uint32_t rr = lo + lane; rr < hi; rr += 32) st_cluster_u32(peer + 4 * rr, __float_as_uint(rs[rr]));
+            for (uint32_t q = 0; q < csize; ++q) {
+                const uint32_t peer = mapa_shared(smem_u32(inbox + crank * rq), q);
+                const uint32_t lo = q * rq, hi = min(c.rows, lo + rq);
+                for (uint32_t rr = lo + lane; rr < hi; rr += 32) st_cluster_u32(peer + 4 * (rr - lo), __float_as_uint(rs[rr]));
+            }
         }
         cluster_sync();
         if (warp == 0) {
-            const uint32_t lo = crank ? half : 0u, hi = crank ? c.rows : half;
+            const uint32_t lo = crank * rq, hi = min(c.rows, lo + rq);
             for (uint32_t rr = lo + lane; rr < hi; rr += 32) {
-                const float mine = rs[rr], other = rs[p.rows_per_cta + rr];
-                store1(p.y, c.r0 + rr, p.y_dtype, crank ? other + mine : mine + other);     // rank 0's share first
+                float acc = 0.f;
+                for (uint32_t s2 = 0; s2 < csize; ++s2) acc += inbox[s2 * rq + (rr - lo)];      // rank order
+                store1(p.y, c.r0 + rr, p.y_dtype, acc);
             }
         }
     }
@@ -547,6 +458,40 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ptq1_int_kernel(const __grid
         for (uint32_t s = 0; s < ring_to; ++s)
             mbar_wait(bar0 + 8 * s, (lastb[s] / p.nslots) & 1, p.err, 200000000ll);
     }
+}
+
+// Clusters of C CTAs (one per SM) that can be resident at once, from the
+// occupancy calculator, once per device and C; sms / C if it cannot tell.
+uint32_t max_clusters(uint32_t C, int smem_limit, int sms) {
+    static std::mutex mu;
+    static int cache[64][5];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return (uint32_t)sms / C;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[dev][C] > 0) return (uint32_t)cache[dev][C];
+    int n = 0;
+    const void *kernel = (const void *)gemv_ptq1_int_kernel<NINFER_BF16>;
+    if (set_smem_attribute(kernel, smem_limit) == NINFER_OK) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(C * ((uint32_t)sms / C));
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = (size_t)smem_limit;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = C;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&n, (void (*)(Ptq1Params))gemv_ptq1_int_kernel<NINFER_BF16>, &cfg) !=
+            cudaSuccess)
+            n = 0;
+        (void)cudaGetLastError();
+    }
+    if (n <= 0) n = sms / (int)C;
+    n = std::min(n, sms / (int)C);
+    cache[dev][C] = n;
+    return (uint32_t)n;
 }
 
 }  // namespace
@@ -561,28 +506,43 @@ bool gemv_ptq1_int_plan(const ninfer_row_split_geometry &g, uint64_t M, bool rot
     if (g.base_offset % 16 || g.high_offset % 16 || g.scale_offset % 16) return false;
     if (g.k > (1u << 24) || g.n > (1ull << 31) || g.n == 0) return false;
     const uint32_t G = (uint32_t)g.groups_per_row;
-    const uint32_t nblk = (uint32_t)((g.k + 1023) / 1024);
-    // split k over a CTA pair when one CTA would rotate in more than one round
-    // (or has more groups than math threads); the split is even (16-byte base rows)
-    bool cluster = nblk > (uint32_t)kWarps || G > (uint32_t)kThreads;
-    uint32_t split = cluster ? (G / 2) & ~1u : G;
-    uint64_t units = (uint64_t)(cluster ? sms / 2 : sms);
+    // the ranks' groups and the blocks they span, for a cluster of C CTAs
+    auto split = [&](uint32_t C, uint32_t r) { return r >= C ? G : ((r * G) / C) & ~1u; };
+    auto max_blocks = [&](uint32_t C) {
+        uint32_t m = 0;
+        for (uint32_t r = 0; r < C; ++r) {
+            const uint32_t a = split(C, r), b = split(C, r + 1);
+            if (b > a) m = std::max(m, (b - 1) / 8 - a / 8 + 1);
+        }
+        return m;
+    };
+    auto max_groups = [&](uint32_t C) {
+        uint32_t m = 0;
+        for (uint32_t r = 0; r < C; ++r) m = std::max(m, split(C, r + 1) - split(C, r));
+        return m;
+    };
+    // the smallest cluster whose CTAs rotate their blocks in one round (pairs)
+    uint32_t C = 1;
+    while (C < 4 && (max_blocks(C) > kPairs || max_groups(C) > (uint32_t)kThreads)) C *= 2;
+    uint64_t units = C == 1 ? (uint64_t)sms : (uint64_t)max_clusters(C, smem_limit, sms);
     uint64_t R = (g.n + units - 1) / units;
-    if (cluster && R > kMaxClusterRows) {
-        if (G > (uint32_t)kThreads) return false;
-        cluster = false;
-        split = G;
+    if (C > 1 && R > kMaxClusterRows) {
+        if (max_groups(1) > (uint32_t)kThreads) return false;
+        C = 1;
         units = (uint64_t)sms;
         R = (g.n + units - 1) / units;
     }
-    const uint32_t ng0 = split, ng1 = cluster ? G - split : 0u;
-    const uint32_t ng_max = std::max(ng0, ng1);
+    const bool cluster = C > 1;
+    const uint32_t ng_max = max_groups(C);
     if (ng_max == 0 || ng_max > (uint32_t)kThreads) return false;
     const uint64_t used = (g.n + R - 1) / R;
-    // high bytes and scales of a CTA's groups rounded out to 8 groups (the halves
-    // of a split have the same number of groups, and so the same rounded width)
-    auto hseg = [&](uint32_t g0, uint32_t ng) { return 2 * (((g0 + ng + 7) & ~7u) - (g0 & ~7u)); };
-    const uint32_t hb_max = std::max(hseg(0, ng0), cluster ? hseg(split, ng1) : 0u);
+    // high bytes and scales of a CTA's groups rounded out to 8 groups; a slot holds
+    // the widest rank's
+    uint32_t hb_max = 0;
+    for (uint32_t r = 0; r < C; ++r) {
+        const uint32_t a = split(C, r), b = split(C, r + 1);
+        hb_max = std::max(hb_max, 2 * (((b + 7) & ~7u) - (a & ~7u)));
+    }
     const uint32_t nsets = (uint32_t)kThreads / ng_max;
     const uint32_t u = nsets >= 32 ? 1 : 2;
     const uint32_t br = nsets * u;
@@ -599,7 +559,8 @@ bool gemv_ptq1_int_plan(const ninfer_row_split_geometry &g, uint64_t M, bool rot
     const uint32_t part_stride = br | 1u;      // odd: the writers' lanes hit distinct banks
     const uint32_t part_slot = (ng_max * part_stride * 4 + 15) / 16 * 16;
     const uint32_t act = (ng_max * (kActGroupBytes + 8) + 15) / 16 * 16;
-    const uint32_t rs_bytes = cluster ? (uint32_t)((2 * R * 4 + 15) / 16 * 16) : 0u;
+    // row sums, then the inbox of C parts of ceil(R / C) rows
+    const uint32_t rs_bytes = cluster ? (uint32_t)(((R + C * ((R + C - 1) / C)) * 4 + 15) / 16 * 16) : 0u;
     const uint32_t bar_bytes = kBarBytes;
     const int64_t avail = (int64_t)smem_limit - kRegion0 - rs_bytes - bar_bytes;
     uint32_t nslots = (uint32_t)std::min<uint64_t>(kMaxSlots, nbatch);
@@ -607,8 +568,8 @@ bool gemv_ptq1_int_plan(const ninfer_row_split_geometry &g, uint64_t M, bool rot
         --nslots;
     if (nslots == 0 || (nslots < 2 && nbatch > 1) || slot >= (1u << 20)) return false;
     plan->ok = true;
-    plan->cluster = cluster;
-    plan->grid = (uint32_t)(cluster ? 2 * used : used);
+    plan->cluster = C;
+    plan->grid = (uint32_t)(C * used);
     plan->units = (uint32_t)used;
     plan->rows_per_cta = (uint32_t)R;
     plan->ng = ng_max;
@@ -616,7 +577,6 @@ bool gemv_ptq1_int_plan(const ninfer_row_split_geometry &g, uint64_t M, bool rot
     plan->wg = wg;
     plan->nbx = nbx;
     plan->bstride = bstride;
-    plan->split = split;
     plan->nsets = nsets;
     plan->u = u;
     plan->nslots = nslots;
@@ -677,7 +637,7 @@ int gemv_ptq1_int_launch(const Ptq1Plan &plan, const uint8_t *payload, const nin
     p.units = plan.units;
     p.k = (uint32_t)g.k;
     p.groups = (uint32_t)g.groups_per_row;
-    p.split = plan.split;
+    p.hbytes = plan.hbytes;
     p.rows_per_cta = plan.rows_per_cta;
     p.nsets = plan.nsets;
     p.u = plan.u;
@@ -715,11 +675,11 @@ int gemv_ptq1_int_launch(const Ptq1Plan &plan, const uint8_t *payload, const nin
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
     attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = plan.cluster ? 2 : 1;
+    attr[1].val.clusterDim.x = plan.cluster;
     attr[1].val.clusterDim.y = 1;
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = plan.cluster ? 2 : 1;     // no cluster attribute at all unless CTA pairs are wanted
+    cfg.numAttrs = plan.cluster > 1 ? 2 : 1;     // no cluster attribute at all unless clusters are wanted
     cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, p);
     if (e != cudaSuccess) return fail(NINFER_ERR_CUDA, "ptq1 gemv launch: %s", cudaGetErrorString(e));
     return NINFER_OK;

@@ -110,8 +110,8 @@ def test_matmul_ptq1_block_split(n, k, M):
                                         (150, 34816, True), (90, 33700, False), (70, 20400, False)])
 def test_matmul_ptq1_m1_wide_k(n, k, rotate):
     """PTQ1_0 at M = 1 with 16 to 34 1024-blocks (rotated, and raw with a
-    ragged last block): past sixteen blocks CTA pairs split the groups, each
-    CTA rotating only the blocks of its half, and add their row sums through
+    ragged last block): clusters of two or four CTAs split the groups, each CTA
+    rotating only the blocks of its share, and add their row sums through
     distributed shared memory."""
     c = synth.make_case("down", n=n, k=k, M=1, seed=n + k)
     y = run_matmul("PTQ1_0_G128", c, rotate=rotate)
@@ -119,20 +119,20 @@ def test_matmul_ptq1_m1_wide_k(n, k, rotate):
     check_decode(y, ref)
 
 
-@pytest.mark.parametrize("n,k", [(200, 16384), (200, 17408), (200, 18432), (90, 19456), (20000, 17408),
+@pytest.mark.parametrize("n,k", [(200, 8192), (200, 9216), (200, 16384), (200, 17408), (90, 19456), (20000, 17408),
                                  (3, 73728), (700, 69632), (64, 147456)])
 def test_matmul_ptq1_m1_group_split(n, k):
-    """PTQ1_0 at M = 1 around the group split: sixteen blocks (one CTA rotates
-    them in one round), seventeen and nineteen (a CTA pair, 68 and 76 groups
-    each, so the high-byte and scale segments of the halves are rounded out to
-    whole 16-byte units and overlap), eighteen (72 each, no overlap), a ring
-    refilled many times per CTA pair (n = 20000), 272 and 288 groups per CTA
-    (one row set), and 1152 groups, more than a CTA pair takes, which the
-    block-split kernel serves instead."""
+    """PTQ1_0 at M = 1 around the group split: eight blocks (one CTA's eight
+    warp pairs rotate them in one round), nine and sixteen (a cluster of two
+    CTAs, each rotating and reading its half), seventeen and nineteen (four
+    CTAs with 34 and 38 groups each, so that the high-byte and scale segments of
+    neighbouring ranks are rounded out to whole 16-byte units and overlap), a
+    ring refilled many times per cluster (n = 20000), and 144 to 288 groups per
+    CTA (several rotation rounds, one to three row sets)."""
     c = synth.make_case("down", n=n, k=k, M=1, seed=n + 3 * k)
     y = run_matmul("PTQ1_0_G128", c)
     if n > 1000:
-        rows = np.unique(np.concatenate([np.arange(0, n, 97), [n - 1], np.arange(250, 280)]))
+        rows = np.unique(np.concatenate([np.arange(0, n, 97), [n - 1], np.arange(250, 300)]))
     else:
         rows = np.arange(n)
     ref = oracle_matmul_rows("PTQ1_0_G128", c, rows)
