@@ -94,7 +94,8 @@ def sources_sha256(files) -> str:
 
 _COMMON = ["bit_gemv_gb300/csrc/gemv_common.cu", "bit_gemv_gb300/csrc/async.cuh",
            "bit_gemv_gb300/csrc/device.cuh", "bit_gemv_gb300/csrc/gemv.h"]
-GEMV_SOURCES = ["bit_gemv_gb300/csrc/gemv_pq2_int.cu", "bit_gemv_gb300/csrc/act16.cuh"] + _COMMON
+GEMV_SOURCES = ["bit_gemv_gb300/csrc/gemv_pq2_int.cu", "bit_gemv_gb300/csrc/act16.cuh",
+                "bit_gemv_gb300/csrc/rot2.cuh"] + _COMMON
 KERNEL_TAG = "gemv"
 
 
@@ -111,7 +112,8 @@ def dominant_kernel(w):
     if w.fmt == "PQ2_0_G128":
         return "gemm_tc", ["bit_gemv_gb300/csrc/gemm_tc.cu"] + _COMMON
     if w.M == 1:
-        return "gemv_ptq1", ["bit_gemv_gb300/csrc/gemv_ptq1_int.cu", "bit_gemv_gb300/csrc/act16.cuh"] + _COMMON
+        return "gemv_ptq1", ["bit_gemv_gb300/csrc/gemv_ptq1_int.cu", "bit_gemv_gb300/csrc/act16.cuh",
+                             "bit_gemv_gb300/csrc/rot2.cuh"] + _COMMON
     if w.M <= 8:
         return "gemv_ptq1_mma", ["bit_gemv_gb300/csrc/gemv_ptq1_mma.cu", "bit_gemv_gb300/csrc/act16.cuh"] + _COMMON
     return "gemm_tc", ["bit_gemv_gb300/csrc/gemm_tc.cu", "bit_gemv_gb300/csrc/transcode.cu"] + _COMMON
