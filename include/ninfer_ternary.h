@@ -239,7 +239,10 @@ int ninfer_ternary_matmul_workspace(int fmt, uint64_t n, uint64_t k, uint64_t M,
  * Arithmetic: transform in fp32. M = 1 (both formats): the rotated
  * activations are rounded to 16-bit fixed point per 1024-block (|x16| < 2^14,
  * relative error <= 2^-14 of the block maximum); code x activation products
- * accumulate exactly in int32 per 128-weight group, then scale in fp32.
+ * accumulate exactly in int32 per 128-weight group, then scale in fp32
+ * (PTQ1_0 shapes the M = 1 kernel cannot split among at most four CTAs of a
+ * cluster -- more than 2048 groups per row, or more than 512 with over about
+ * 147,000 rows -- take the 2 <= M <= 8 path below).
  * 2 <= M <= 8 (both formats): binary16 activations scaled per 1024-block
  * (relative error <= 2^-11 per element), exact binary16 codes, products on the
  * tensor cores (mma.sync) with fp32 accumulation. M > 8 (prefill, both
@@ -318,8 +321,8 @@ int ninfer_device_errors(uint32_t *out, int clear);
 
 /*
  * ninfer_set_wait_limit -- bound, in SM clock cycles, of each wait of the
- * PQ2_0_G128 M = 1 decode kernel (ninfer_ternary_matmul and the one-kernel
- * ninfer_ternary_gate_up) for its weight copies, for calls launched after
+ * M = 1 decode kernels of both formats (ninfer_ternary_matmul and the
+ * one-kernel ninfer_ternary_gate_up) for their weight copies, for calls launched after
  * this one; the default is 4e9 (about two seconds). No counterpart on the
  * source pages: a diagnostic hook that lets a test drive the failure path
  * described under ninfer_device_errors without breaking anything. cycles == 0

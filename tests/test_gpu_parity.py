@@ -195,6 +195,29 @@ def test_matmul_bf16_output():
     assert oracle.max_rel_error(y, ref) <= 4e-3       # bf16 output rounding
 
 
+@pytest.mark.parametrize("fmt", ["PQ2_0_G128", "PTQ1_0_G128"])
+@pytest.mark.parametrize("n,k", [(300, 5120), (200, 17408)])
+@pytest.mark.parametrize("x_dtype,y_dtype", [(torch.float32, torch.float32), (torch.float16, torch.float32),
+                                             (torch.float16, torch.bfloat16), (torch.float32, torch.bfloat16)])
+def test_matmul_m1_activation_and_output_dtypes(fmt, n, k, x_dtype, y_dtype):
+    """The M = 1 kernels for every activation dtype (each is a separate
+    instance) and bf16 outputs, also through the exchange of the clustered
+    PTQ1_0 path (k = 17408: clusters of four CTAs). The oracle takes the
+    activation as the kernel sees it (rounded to the input dtype)."""
+    c = synth.make_case("gateup", n=n, k=k, M=1, seed=n + k + 7)
+    xd = torch.from_numpy(c.x.astype(np.float32)).to(DEV).to(x_dtype)
+    payload = dev_u8(nt.ninfer_ternary_pack(fmt, c.values, c.scales))
+    y = nt.ninfer_ternary_matmul(fmt, payload, n, k, xd, dev_signs(c.signs), y_dtype=y_dtype)
+    torch.cuda.synchronize()
+    xs = xd.float().cpu().numpy().astype(np.float64)
+    ref = oracle.ternary_matmul(fmt, oracle.pack_planes(fmt, c.values, c.scales), n, k, xs, signs_values(c))
+    got = y.float().cpu().numpy().astype(np.float64)
+    if y_dtype == torch.float32:
+        check_decode(got, ref)
+    else:
+        assert oracle.max_rel_error(got, ref) <= 4e-3      # bf16 output rounding
+
+
 @pytest.mark.slow
 def test_matmul_gateup_full():
     c = synth.make_case("gateup")
@@ -378,28 +401,32 @@ def test_no_device_errors_after_suite():
     assert nt.ninfer_device_errors(clear=True) == 0
 
 
-@pytest.mark.parametrize("n,k", [(600, 5120), (3000, 16384)])
-def test_bounded_wait_failure_path(n, k):
+@pytest.mark.parametrize("fmt,n,k", [("PQ2_0_G128", 600, 5120), ("PQ2_0_G128", 3000, 16384),
+                                     ("PTQ1_0_G128", 600, 5120), ("PTQ1_0_G128", 20000, 17408)])
+def test_bounded_wait_failure_path(fmt, n, k):
     """A weight-ring wait that gives up: with the bound set to 0 every wait of
-    the PQ2_0 M = 1 kernel gives up at its first check, although the copies
-    land normally. The call still returns OK and sets bit 0 of the device error
-    word (the call's output is not meaningful); the CTAs let their issued
-    copies land before exiting, so the context stays usable: the next call
-    with the default bound matches the oracle and leaves the word clear. The
-    second shape refills the ring (more chunks per CTA than slots)."""
+    the M = 1 kernels gives up at its first check, although the copies land
+    normally. The call still returns OK and sets bit 0 of the device error word
+    (the call's output is not meaningful); the CTAs let their issued copies
+    land before exiting, so the context stays usable: the next call with the
+    default bound matches the oracle and leaves the word clear. The second and
+    fourth shapes have more ring items per CTA than slots; the fourth runs the
+    PTQ1_0 kernel in clusters of four CTAs, whose barriers every thread still
+    reaches. Output rows are sampled for the large shape."""
     c = synth.make_case("gateup", n=n, k=k, M=1, seed=n + k)
-    payload = dev_u8(nt.ninfer_ternary_pack("PQ2_0_G128", c.values, c.scales))
+    payload = dev_u8(nt.ninfer_ternary_pack(fmt, c.values, c.scales))
     torch.cuda.synchronize()
     assert nt.ninfer_device_errors(clear=True) == 0
     try:
         nt.ninfer_set_wait_limit(0)
-        nt.ninfer_ternary_matmul("PQ2_0_G128", payload, n, k, dev_x(c), dev_signs(c.signs))
+        nt.ninfer_ternary_matmul(fmt, payload, n, k, dev_x(c), dev_signs(c.signs))
         torch.cuda.synchronize()
     finally:
         nt.ninfer_set_wait_limit(nt.WAIT_LIMIT_DEFAULT)
     assert nt.ninfer_device_errors(clear=True) & 1
-    y = run_matmul("PQ2_0_G128", c, payload_dev=payload)
-    check_decode(y, oracle_matmul_rows("PQ2_0_G128", c, np.arange(n)))
+    y = run_matmul(fmt, c, payload_dev=payload)
+    rows = np.arange(n) if n <= 3000 else np.unique(np.concatenate([np.arange(0, n, 53), [n - 1]]))
+    check_decode(y[:, rows], oracle_matmul_rows(fmt, c, rows))
     assert nt.ninfer_device_errors(clear=True) == 0
 
 
