@@ -429,27 +429,30 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ptq1_int_kernel(const __grid
     __syncthreads();     // every row sum is in place; failures are recorded
 
     if (csize > 1) {
-        // rows split in csize parts of rq rows; rank q finishes part q: every rank
-        // stores its sums for part q in rank q's inbox (row sums rows_per_cta
-        // floats on: csize arrays of rq floats, one per source rank)
+        // rows split in csize parts of rq rows (a multiple of 4); rank q finishes
+        // part q: warp q stores this rank's sums for part q, four rows per store,
+        // in rank q's inbox (rows_per_cta rounded up to 4 floats after the row
+        // sums: csize arrays of rq floats, one per source rank)
         asm volatile("barrier.cluster.wait.aligned;" ::: "memory");     // every CTA of the cluster is running
-        const uint32_t rq = (c.rows + csize - 1) / csize;
-        float *inbox = rs + p.rows_per_cta;
-        if (warp == 0) {
-            for (uint32_t q = 0; q < csize; ++q) {
-                const uint32_t peer = mapa_shared(smem_u32(inbox + crank * rq), q);
-                const uint32_t lo = q * rq, hi = min(c.rows, lo + rq);
-                for (uint32_t rr = lo + lane; rr < hi; rr += 32) st_cluster_u32(peer + 4 * (rr - lo), __float_as_uint(rs[rr]));
+        const uint32_t rq = ((c.rows + csize - 1) / csize + 3) & ~3u;
+        float *inbox = rs + ((p.rows_per_cta + 3) & ~3u);
+        if ((uint32_t)warp < csize) {
+            const uint32_t q = warp;
+            const uint32_t peer = mapa_shared(smem_u32(inbox + crank * rq), q);
+            const uint32_t lo = q * rq, hi = min(c.rows, lo + rq);
+            for (uint32_t r4 = lo + 4 * lane; r4 < hi; r4 += 128) {
+                // rows past hi (at most 3, within the rounding) are sent but never read
+                const float4 v = *reinterpret_cast<const float4 *>(rs + r4);
+                st_cluster_v4(peer + 4 * (r4 - lo), make_uint4(__float_as_uint(v.x), __float_as_uint(v.y),
+                                                              __float_as_uint(v.z), __float_as_uint(v.w)));
             }
         }
         cluster_sync();
-        if (warp == 0) {
-            const uint32_t lo = crank * rq, hi = min(c.rows, lo + rq);
-            for (uint32_t rr = lo + lane; rr < hi; rr += 32) {
-                float acc = 0.f;
-                for (uint32_t s2 = 0; s2 < csize; ++s2) acc += inbox[s2 * rq + (rr - lo)];      // rank order
-                store1(p.y, c.r0 + rr, p.y_dtype, acc);
-            }
+        const uint32_t lo = crank * rq, hi = min(c.rows, lo + rq);
+        for (uint32_t rr = lo + tid; rr < hi; rr += kThreads) {
+            float acc = 0.f;
+            for (uint32_t s2 = 0; s2 < csize; ++s2) acc += inbox[s2 * rq + (rr - lo)];      // rank order
+            store1(p.y, c.r0 + rr, p.y_dtype, acc);
         }
     }
     // after a timed-out wait: let the copies still in flight land (the last one
@@ -559,8 +562,10 @@ bool gemv_ptq1_int_plan(const ninfer_row_split_geometry &g, uint64_t M, bool rot
     const uint32_t part_stride = br | 1u;      // odd: the writers' lanes hit distinct banks
     const uint32_t part_slot = (ng_max * part_stride * 4 + 15) / 16 * 16;
     const uint32_t act = (ng_max * (kActGroupBytes + 8) + 15) / 16 * 16;
-    // row sums, then the inbox of C parts of ceil(R / C) rows
-    const uint32_t rs_bytes = cluster ? (uint32_t)(((R + C * ((R + C - 1) / C)) * 4 + 15) / 16 * 16) : 0u;
+    // row sums (a whole number of 4-row vectors past R), then the inbox: C parts of
+    // ceil(R / C) rows rounded up to a multiple of 4
+    const uint64_t rq = ((R + C - 1) / C + 3) & ~3ull;
+    const uint32_t rs_bytes = cluster ? (uint32_t)((((R + 3) & ~3ull) + C * rq) * 4) : 0u;
     const uint32_t bar_bytes = kBarBytes;
     const int64_t avail = (int64_t)smem_limit - kRegion0 - rs_bytes - bar_bytes;
     uint32_t nslots = (uint32_t)std::min<uint64_t>(kMaxSlots, nbatch);
