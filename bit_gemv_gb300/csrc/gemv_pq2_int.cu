@@ -36,8 +36,8 @@
 // odd number of chunks per tile the last one is shared by all sixteen warps,
 // half a group each. One chunk is requested before the programmatic-
 // dependent-launch wait (weights and signs are read-only), the rest of the
-// ring after the rotating warps have requested x, by a warp that does not
-// rotate; the last reader of a chunk refills its slot with the chunk nslots
+// ring after x has arrived in the rotating warps (in a cluster, at once), by a
+// warp that does not rotate; the last reader of a chunk refills its slot with the chunk nslots
 // further on.
 #include <cstring>
 
@@ -185,6 +185,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_pq2_int_kernel(const __grid_
     const int t = tid & 63;
     const bool rotating = pr < npr;
     const uint32_t nwait = 32 * (2 * npr + 1);
+    // the rest of the ring is requested once x has arrived, except in a cluster
+    // (two CTAs sharing the rotations), where requesting it at once measured faster
+    const bool ring_after_x = csize == 1;
 
     if (tid == producer * 32) {
         prefetch_tmap(last_cta ? &p.wmap_last : &p.wmap_main);
@@ -219,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_pq2_int_kernel(const __grid_
         // pair's maximum slot, written again later); then the producer may
         // queue the rest of the ring behind it
         *reinterpret_cast<volatile float *>(scr + 1080 + (t >> 5)) = v[0] + v[15];
-        named_barrier_arrive(kBarX, nwait);
+        if (ring_after_x) named_barrier_arrive(kBarX, nwait);
         rotate_pack2(p.signs != nullptr, v, d, b, p.groups, act_s + (task / p.nblk) * p.act_bytes,
                      act_remote0 ? act_remote0 + (task / p.nblk) * p.act_bytes : 0u, scr, t, kBarPair0 + pr);
     } else {
@@ -228,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_pq2_int_kernel(const __grid_
         if (warp == producer) {
             // the rest of the ring is requested once x has arrived in every rotating
             // warp, so that x does not queue behind it
-            named_barrier(kBarX, nwait);
+            if (ring_after_x) named_barrier(kBarX, nwait);
             if (lane == 0) {
                 for (uint32_t i = pre; i < ring_to; ++i) issue_chunk<kMats>(p, smem, i, last_cta);
                 *issued = ring_to;
