@@ -1,5 +1,6 @@
 // Inline-PTX wrappers for mbarriers, bulk and tensor-map async copies (TMA
-// engine), programmatic dependent launch and shared-memory loads on sm_103a,
+// engine), programmatic dependent launch, named barriers and thread-block clusters
+// (ranks, distributed shared-memory stores, the cluster barrier) on sm_103a,
 // plus the bits of the library's device error word. Every wait is bounded: a wait that runs out
 // records an error code and returns false instead of spinning forever.
 #pragma once
@@ -149,46 +150,12 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint4 v) {
                  : "memory");
 }
 
-__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t a) {
-    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(a) : "memory");
-}
-
 __device__ __forceinline__ void st_cluster_v2(uint32_t addr, uint32_t a, uint32_t b) {
     asm volatile("st.shared::cluster.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
 }
 
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ uint2 lds64(uint32_t addr) {
-    uint2 v;
-    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
-    return v;
-}
-
-__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
-    uint32_t v;
-    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
-    return v;
-}
-
-__device__ __forceinline__ uint32_t lds16(uint32_t addr) {
-    unsigned short v;
-    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
-    return v;
-}
-
-__device__ __forceinline__ uint4 lds128u(uint32_t addr) {
-    uint4 v;
-    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
-    return v;
-}
-
-__device__ __forceinline__ float4 lds128f(uint32_t addr) {
-    float4 v;
-    asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
-    return v;
 }
 
 }  // namespace ninfer

@@ -18,7 +18,6 @@ namespace ninfer {
 // Warp-owned 1024-element block: lane l holds v[8*i + e] = element
 // 256*i + 8*l + e (i < 4, e < 8). Index bits 0-2 and 8-9 live in the lane's
 // registers, bits 3-7 in the lane id.
-__device__ __forceinline__ int wht_index(int lane, int r) { return ((r >> 3) << 8) | (lane << 3) | (r & 7); }
 
 __device__ __forceinline__ void wht1024_warp(float (&v)[32], int lane) {
 #pragma unroll
