@@ -43,13 +43,15 @@
 // requests already in flight have landed.
 //
 // Arithmetic: a 256-entry table maps a code byte to its digits as bytes
-// (t0 | t1 << 8 | t2 << 16 | t3 << 24, with t4 in bits 2-3 of byte 0), entry B
-// at B * 256 and held once per lane (lane l's copy at + 4 l, bank l), so that a
-// byte permute of the code word and 4 l forms a lane's address in one
-// instruction. Per base byte dp2a multiplies (t0, t1) and (t2, t3) by their
-// activation pairs; the t4 fields of four consecutive bytes are gathered into
-// one word by byte permutes and multiplied by their pairs (times 4, removed at
-// the end); all exact in int32. Per group:
+// (t0 | t1 << 8 | t2 << 16 | t3 << 24) with t4 in bits 2-3 of byte 0, and in
+// its second half the same with t4 in bits 2-3 of byte 1; entry B at B * 256,
+// each half held once per lane (lane l's copy at + 4 l, bank l), so that a
+// byte permute of the code word and 4 l (or 4 l + 128) forms a lane's address
+// in one instruction. Per base byte dp2a multiplies (t0, t1) and (t2, t3) by
+// their activation pairs; bytes 0 and 2 of a code word look up the first half,
+// bytes 1 and 3 the second, so that two or-and operations and one byte permute
+// gather the t4 fields of the word's four bytes, multiplied by their pairs
+// (times 4, removed at the end); all exact in int32. Per group:
 //   y += scale * 2^-E * (sum t x16 - sum x16)                    (value = t - 1)
 #include <cstring>
 #include <mutex>
@@ -77,7 +79,7 @@ constexpr uint32_t kActWords = 64;
 constexpr uint32_t kActStride = 68;
 static_assert(kActStride >= kActWords && kActStride % 8 == 4, "operand words: an odd number of 16-byte units");
 constexpr uint32_t kActGroupBytes = kActStride * 4;
-constexpr uint32_t kLutStride = 256;        // entry B at B * 256: 32 lane copies, then unused
+constexpr uint32_t kLutStride = 256;        // entry B at B * 256: 32 lane copies of each half
 constexpr uint32_t kLutBytes = 256 * kLutStride;
 constexpr uint32_t kPairs = kWarps / 2;     // rotating warp pairs; named barriers 1 .. 8
 constexpr uint32_t kBarPair0 = 1;
@@ -217,7 +219,8 @@ __device__ __forceinline__ void rotate_pack(bool rotate, float (&v)[16], const f
     named_barrier(bar, 64);      // the scratch may be reused
 }
 
-// Lane's copy of the table entry of byte c of w: lut + (B_c << 8 | lane4).
+// Lane's copy of the table entry of byte c of w: lut + (B_c << 8 | lane4), lane4
+// = 4 lane (first half) or 4 lane + 128 (second half).
 __device__ __forceinline__ uint32_t lut_entry(const uint8_t *lut, uint32_t w, uint32_t lane4, uint32_t c) {
     return *reinterpret_cast<const uint32_t *>(lut + __byte_perm(w, lane4, 0x5504u | (c << 4)));
 }
@@ -229,11 +232,12 @@ __device__ __forceinline__ uint32_t lut_entry(const uint8_t *lut, uint32_t w, ui
 __device__ __forceinline__ int group_dot(const uint32_t (&bw)[6], uint32_t hb, const uint8_t *lut, uint32_t lane4,
                                          const uint32_t (&av)[kActWords]) {
     int acc[4] = {0, 0, 0, 0}, acc4 = 0;
+    const uint32_t lane4b = lane4 | 128u;
 #pragma unroll
     for (int q = 0; q < 6; ++q) {
         uint32_t W[4];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) W[c] = lut_entry(lut, bw[q], lane4, c);
+        for (int c = 0; c < 4; ++c) W[c] = lut_entry(lut, bw[q], (c & 1) ? lane4b : lane4, c);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
             const uint32_t m = W[c] & 0x03030303u;
@@ -241,9 +245,9 @@ __device__ __forceinline__ int group_dot(const uint32_t (&bw)[6], uint32_t hb, c
             acc[c] = dp2a_lo(av[2 * j], m, acc[c]);
             acc[c] = dp2a_hi(av[2 * j + 1], m, acc[c]);
         }
-        // byte 0 of each entry holds 4 * t4 in bits 2-3: gather the four
-        const uint32_t g = __byte_perm(__byte_perm(W[0], W[1], 0x0040u), __byte_perm(W[2], W[3], 0x0040u), 0x5410u) &
-                           0x0C0C0C0Cu;
+        // 4 * t4 sits in bits 2-3 of byte 0 (bytes 0, 2) or byte 1 (bytes 1, 3):
+        // gather the four into bytes 0-3
+        const uint32_t g = __byte_perm((W[0] | W[1]) & 0x0C0Cu, (W[2] | W[3]) & 0x0C0Cu, 0x5410u);
         acc4 = dp2a_lo(av[48 + 2 * q], g, acc4);
         acc4 = dp2a_hi(av[49 + 2 * q], g, acc4);
     }
@@ -310,17 +314,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ptq1_int_kernel(const __grid
     }
     __syncthreads();     // operand words complete; the rotation scratch is free for the table
     {
-        // digit table: entry B's 32 lane copies as 8 16-byte stores
-        for (uint32_t i = tid; i < 256 * 8; i += kThreads) {
-            uint32_t B = i >> 3, W = 0;
+        // digit table: thread t builds half t % 2 of entry t / 2 (512 threads, 512
+        // halves) as eight 16-byte stores of 4 lane copies each, in an order
+        // staggered by lane so that a warp's stores spread over all banks
+        static_assert(kThreads == 512, "one table half per thread");
+        uint32_t B = (uint32_t)tid >> 1, W = 0;
+        const uint32_t half = (uint32_t)tid & 1;
 #pragma unroll
-            for (int e = 0; e < 5; ++e) {
-                const uint32_t dg = B % 3;
-                B /= 3;
-                W |= e < 4 ? dg << (8 * e) : dg << 2;
-            }
-            *reinterpret_cast<uint4 *>(smem + (i >> 3) * kLutStride + 16 * (i & 7)) = make_uint4(W, W, W, W);
+        for (int e = 0; e < 5; ++e) {
+            const uint32_t dg = B % 3;
+            B /= 3;
+            W |= e < 4 ? dg << (8 * e) : dg << (2 + 8 * half);
         }
+        uint8_t *ent = smem + ((uint32_t)tid >> 1) * kLutStride + 128 * half;
+#pragma unroll
+        for (int k2 = 0; k2 < 8; ++k2) *reinterpret_cast<uint4 *>(ent + 16 * ((k2 + lane) & 7)) = make_uint4(W, W, W, W);
     }
     const bool math = (uint32_t)tid < nact;
     const uint32_t gl = math ? (uint32_t)tid % c.ng : 0u, set = math ? (uint32_t)tid / c.ng : 0u;
