@@ -267,6 +267,9 @@ def _capture(stream, fn, count, offset=0):
     return g
 
 
+HOLD_CYCLES = 300_000      # about 0.15 ms at 2 GHz: longer than the submission of the graphs
+
+
 def _timed_graphs(stream, graphs, warm_replays, world, dev):
     """Replay graphs (each a list replayed in order) after warm-up replays of the
     first; CUDA events on the launching stream, barrier + synchronize on both
@@ -283,6 +286,12 @@ def _timed_graphs(stream, graphs, warm_replays, world, dev):
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
+        # a short spin kernel holds the idle stream while the host records the start
+        # event and submits the graphs, so that the timed region begins with the
+        # first step on the device instead of waiting for the host's submission
+        # (the blocking-kernel technique of NVIDIA's nvbench); it runs before the
+        # start event and is not part of any step
+        torch.cuda._sleep(HOLD_CYCLES)
         e0.record(stream)
         for gr in graphs:
             gr.replay()
