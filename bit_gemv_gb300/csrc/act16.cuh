@@ -1,15 +1,14 @@
-// Activation preparation shared by the integer decode kernels (M = 1): the
-// forward signed block Walsh-Hadamard transform ("artifact-container.md" §8
-// hadamard_signs; TensorSharp article §4.2: per 1024-block H (D * x) / 32),
-// then 16-bit fixed point per block, x16 = rint(xr * 2^E) with E chosen so that
-// max |x16| < 2^14.
+// Activation helpers shared by the decode kernels: the dp2a wrappers of the
+// M = 1 integer kernels, and for the M <= 8 tensor-core kernels the loads of a
+// 1024-block of x and its signs and the forward signed block Walsh-Hadamard
+// transform ("artifact-container.md" §8 hadamard_signs; TensorSharp article
+// §4.2: per 1024-block H (D * x) / 32).
 //
-// Two warps (64 threads) per 1024-block, 16 elements per thread, in three
-// register passes over index bits 0-3, 4-7 and 8-9 with transposes through a
-// padded float tile between them (element e at e + e/16, conflict-free for the
-// first two layouts). The quantised values are left in the same scratch as
-// int16 in natural order; a layout-specific packer turns them into the dp2a
-// operand words of its kernel.
+// rotate16: two warps (64 threads) per 1024-block, 16 elements per thread, in
+// three register passes over index bits 0-3, 4-7 and 8-9 with transposes
+// through a padded float tile between them (element e at e + e/16,
+// conflict-free for the first two layouts). Each kernel then converts the
+// rotated values into its own operand layout.
 #pragma once
 
 #include <cstdint>
@@ -128,26 +127,6 @@ __device__ __forceinline__ float rotate16(bool rotate, int t, float (&v)[16], co
     if (lane == 0) pmax[t >> 5] = mx;
     named_barrier(bar, 64);      // also: every thread has read its tile values
     return fmaxf(pmax[0], pmax[1]);
-}
-
-// Rotates and quantises block b (x in v, signs in d). On return the block's
-// x16 values sit in the tile as int16 in natural order, visible to the whole
-// pair, and *E_out is the block's exponent. t = thread of the pair (0..63),
-// bar = the pair's named barrier.
-__device__ __forceinline__ const int16_t *rotate_quantize16(bool rotate, int t, float (&v)[16], const float (&d)[16],
-                                                           float *tile, uint32_t bar, int *E_out) {
-    const float mx = rotate16(rotate, t, v, d, tile, bar);
-    int E = 0;
-    if (mx > 0.f) E = 13 - ilogbf(mx);     // max |x16| < 2^14
-    E = max(-100, min(100, E));
-    const float up = ldexpf(1.f, E);
-    int16_t *qs = reinterpret_cast<int16_t *>(tile);
-#pragma unroll
-    for (int r = 0; r < 16; ++r)           // adding 1.5 * 2^23 rounds to nearest, ties to even
-        qs[256 * (r >> 2) + 4 * t + (r & 3)] = (int16_t)(__float_as_int(fmaf(v[r], up, 12582912.0f)) - 0x4B400000);
-    named_barrier(bar, 64);
-    *E_out = E;
-    return qs;
 }
 
 }  // namespace ninfer

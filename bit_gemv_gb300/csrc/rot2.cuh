@@ -57,7 +57,7 @@ __device__ __forceinline__ void f2unpack(uint64_t r, float &a, float &b) {
 // Butterflies over the four register index bits of 16 values: bits 1-3 as
 // paired fp32 adds and subtracts (each element rounded exactly as by a scalar
 // add), bit 0 within the pairs.
-__device__ __forceinline__ void butterfly16(float (&v)[16]) {
+__device__ __forceinline__ void butterfly16_f32x2(float (&v)[16]) {
     uint64_t w[8];
 #pragma unroll
     for (int m = 0; m < 8; ++m) w[m] = f2pack(v[2 * m], v[2 * m + 1]);
@@ -105,7 +105,7 @@ __device__ __forceinline__ int rotate_quant2(bool rotate, float (&v)[16], const 
                 "l"(f2pack(d[2 * m], d[2 * m + 1])));
             f2unpack(r, v[2 * m], v[2 * m + 1]);
         }
-        butterfly16(v);      // element bits 0, 1, 2, 9
+        butterfly16_f32x2(v);      // element bits 0, 1, 2, 9
     }
     const int aA = 8 * t + 8 * (t >> 4);
     const int aB = (lane & 7) + 136 * (lane >> 3) + 544 * wh;
@@ -119,7 +119,7 @@ __device__ __forceinline__ int rotate_quant2(bool rotate, float (&v)[16], const 
 #pragma unroll
     for (int j = 0; j < 16; ++j) v[j] = scr[aB + 8 * j];
     if (rotate) {
-        butterfly16(v);      // element bits 3-6
+        butterfly16_f32x2(v);      // element bits 3-6
         // element bits 7 and 8 (lane bits 3 and 4): the lane whose bit is set keeps
         // partner - own, the other own + partner (fmaf(+-1, own, partner): one rounding)
 #pragma unroll
