@@ -506,3 +506,101 @@ def test_gate_up_full_sampled():
                                 oracle.pack_planes("PQ2_0_G128", vu[rows], su[rows]), rows.size, k, c.x,
                                 signs_values(c), synth.bf16_bits_to_f32(du).astype(np.float64))
     assert oracle.max_rel_error(y.cpu().numpy()[:, rows].astype(np.float64), ref) <= TOL_DECODE
+
+
+# ------------------------------------------ chained calls in a CUDA graph ---
+def _graph(fn):
+    """fn() captured in a CUDA graph on a side stream (as bench.py captures its
+    back-to-back calls; each call is launched with programmatic dependent launch
+    on the one before)."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            fn()
+    torch.cuda.current_stream().wait_stream(s)
+    return g
+
+
+def test_ffn_chain_graph_replay():
+    """The FFN at full size, chained as a decoder runs it: the fused gate/up
+    pair with SwiGLU (PQ2_0, 17408 x 5120) writes h in bf16, and the down
+    projection (PTQ1_0, 5120 x 17408) reads h as its x. Three tokens run
+    eagerly into separate buffers and are checked against the oracle (sampled
+    gate/up rows; every down row from the oracle applied to the h the GPU
+    produced). The same three chains, captured back to back in one CUDA graph
+    with a single shared h buffer (each call waits for the one before it to
+    finish reading and writing h), must reproduce the eager outputs bit for
+    bit: every kernel adds in a fixed order."""
+    cg = synth.make_case("gateup")
+    cd = synth.make_case("down")
+    n, k = cg.values.shape                      # 17408 x 5120
+    nd, kd = cd.values.shape                    # 5120 x 17408
+    assert kd == n and nd == k
+    vu, su, du = _up_inputs(11, n, k)
+    pay_g = dev_u8(nt.ninfer_ternary_pack("PQ2_0_G128", cg.values, cg.scales))
+    pay_u = dev_u8(nt.ninfer_ternary_pack("PQ2_0_G128", vu, su))
+    pay_d = dev_u8(nt.ninfer_ternary_pack("PTQ1_0_G128", cd.values, cd.scales))
+    sg, su_d, sd = dev_signs(cg.signs), dev_signs(du), dev_signs(cd.signs)
+    T = 3
+    xv, xraw = synth.activations(np.random.default_rng(21), T, k, "bf16")
+    xs = [torch.from_numpy(np.ascontiguousarray(xraw[t:t + 1]).view(np.int16)).to(DEV).view(torch.bfloat16)
+          for t in range(T)]
+
+    def chain(h_bufs, y_bufs):
+        for t in range(T):
+            nt.ninfer_ternary_gate_up("PQ2_0_G128", pay_g, pay_u, n, k, xs[t], sg, su_d, y=h_bufs[t])
+            nt.ninfer_ternary_matmul("PTQ1_0_G128", pay_d, nd, kd, h_bufs[t], sd, y=y_bufs[t])
+
+    h_e = [torch.empty((1, n), dtype=torch.bfloat16, device=DEV) for _ in range(T)]
+    y_e = [torch.empty((1, nd), dtype=torch.float32, device=DEV) for _ in range(T)]
+    chain(h_e, y_e)
+    torch.cuda.synchronize()
+    h_np = np.concatenate([h.float().cpu().numpy() for h in h_e]).astype(np.float64)
+    y_np = np.concatenate([y.cpu().numpy() for y in y_e]).astype(np.float64)
+
+    rows = np.unique(np.concatenate([[0, n - 1], np.random.default_rng(6).integers(0, n, 1500)]))
+    ref_h = oracle.gate_up_swiglu("PQ2_0_G128", oracle.pack_planes("PQ2_0_G128", cg.values[rows], cg.scales[rows]),
+                                  oracle.pack_planes("PQ2_0_G128", vu[rows], su[rows]), rows.size, k, xv,
+                                  signs_values(cg), synth.bf16_bits_to_f32(du).astype(np.float64))
+    # h is stored in bf16: compare within bf16 rounding on top of the decode bound
+    assert oracle.max_rel_error(h_np[:, rows], ref_h) <= TOL_DECODE + 2.0 ** -8
+    ref_y = oracle.ternary_matmul("PTQ1_0_G128", oracle.pack_planes("PTQ1_0_G128", cd.values, cd.scales), nd, kd,
+                                  h_np, signs_values(cd))
+    check_decode(y_np, ref_y)
+
+    h_shared = torch.empty((1, n), dtype=torch.bfloat16, device=DEV)
+    y_g = [torch.full((1, nd), float("nan"), dtype=torch.float32, device=DEV) for _ in range(T)]
+    g = _graph(lambda: chain([h_shared] * T, y_g))
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    for t in range(T):
+        assert torch.equal(y_g[t], y_e[t]), t
+    assert torch.equal(h_shared, h_e[T - 1])
+    assert nt.ninfer_device_errors() == 0
+
+
+def test_gateup_graph_replay_rotating_pool():
+    """The gate/up projection (PQ2_0 17408 x 5120, M = 1) as bench.py times it:
+    back-to-back calls in a CUDA graph over a rotating pool of payload copies.
+    Every call's output equals the eager call's bit for bit, and the eager
+    output matches the oracle on sampled rows."""
+    c = synth.make_case("gateup")
+    n, k = c.values.shape
+    host = nt.ninfer_ternary_pack("PQ2_0_G128", c.values, c.scales)
+    pool = [dev_u8(host) for _ in range(2)]
+    x, s = dev_x(c), dev_signs(c.signs)
+    y_ref = nt.ninfer_ternary_matmul("PQ2_0_G128", pool[0], n, k, x, s)
+    torch.cuda.synchronize()
+    rows = np.unique(np.concatenate([[0, n - 1], np.random.default_rng(8).integers(0, n, 1500)]))
+    check_decode(y_ref.cpu().numpy()[:, rows].astype(np.float64), oracle_matmul_rows("PQ2_0_G128", c, rows))
+    K = 6
+    ys = [torch.full((1, n), float("nan"), dtype=torch.float32, device=DEV) for _ in range(K)]
+    g = _graph(lambda: [nt.ninfer_ternary_matmul("PQ2_0_G128", pool[i % 2], n, k, x, s, y=ys[i]) for i in range(K)])
+    g.replay()
+    torch.cuda.synchronize()
+    for i in range(K):
+        assert torch.equal(ys[i], y_ref), i
+    assert nt.ninfer_device_errors() == 0
