@@ -645,3 +645,74 @@ def test_m8_graph_replay_shared_workspace(fmt, wl):
     for t in range(T):
         assert torch.equal(y_g[t], y_e[t]), t
     assert nt.ninfer_device_errors() == 0
+
+
+@pytest.mark.parametrize("fmt", ["PQ2_0_G128", "PTQ1_0_G128"])
+def test_prefill_graph_replay_shared_workspace(fmt):
+    """Prefill (M = 300 on a 1100 x 2048 matrix), two calls back to back through
+    one shared workspace (the rotated binary16 activations; for PTQ1_0 also the
+    planes rewritten as PQ2_0), eager and in a CUDA graph: the graph's outputs
+    equal the eager ones bit for bit, and the eager ones match the oracle on
+    every output."""
+    M, T = 300, 2
+    c = synth.make_case("prefill", n=1100, k=2048, M=M, seed=12)
+    n, k = c.values.shape
+    pay = dev_u8(nt.ninfer_ternary_pack(fmt, c.values, c.scales))
+    s = dev_signs(c.signs)
+    xv, xraw = synth.activations(np.random.default_rng(41), T * M, k, "bf16")
+    xs = [torch.from_numpy(np.ascontiguousarray(xraw[M * t:M * (t + 1)]).view(np.int16)).to(DEV).view(torch.bfloat16)
+          for t in range(T)]
+    need = nt.ninfer_ternary_matmul_workspace(fmt, n, k, M, True)
+    assert need > 0
+    ws = torch.empty(need, dtype=torch.uint8, device=DEV)
+
+    def calls(ys):
+        for t in range(T):
+            nt.ninfer_ternary_matmul(fmt, pay, n, k, xs[t], s, y=ys[t], workspace=ws)
+
+    y_e = [torch.empty((M, n), dtype=torch.float32, device=DEV) for _ in range(T)]
+    calls(y_e)
+    torch.cuda.synchronize()
+    ref = oracle.ternary_matmul(fmt, oracle.pack_planes(fmt, c.values, c.scales), n, k, xv, signs_values(c))
+    check_prefill(np.concatenate([y.cpu().numpy() for y in y_e]).astype(np.float64), ref)
+    y_g = [torch.full((M, n), float("nan"), dtype=torch.float32, device=DEV) for _ in range(T)]
+    g = _graph(lambda: calls(y_g))
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    for t in range(T):
+        assert torch.equal(y_g[t], y_e[t]), t
+    assert nt.ninfer_device_errors() == 0
+
+
+@pytest.mark.parametrize("fmt", ["PQ2_0_G128", "PTQ1_0_G128"])
+def test_embed_graph_replay(fmt):
+    """Three embedding gathers (16 ids each, repeats included) back to back,
+    eager and in a CUDA graph: equal bit for bit; the eager rows match the
+    oracle."""
+    c = synth.make_case("gateup", n=2000, k=5120, M=1, seed=23)
+    n, k = c.values.shape
+    pay = dev_u8(nt.ninfer_ternary_pack(fmt, c.values, c.scales))
+    s = dev_signs(c.signs)
+    T = 3
+    ids_np = np.random.default_rng(24).integers(0, n, (T, 16)).astype(np.int32)
+    ids_np[1, 3] = ids_np[1, 4]
+    ids = [torch.from_numpy(ids_np[t].copy()).to(DEV) for t in range(T)]
+
+    def calls(outs):
+        for t in range(T):
+            nt.ninfer_ternary_embed(fmt, pay, n, k, ids[t], s, out=outs[t])
+
+    o_e = [torch.empty((16, k), dtype=torch.float32, device=DEV) for _ in range(T)]
+    calls(o_e)
+    torch.cuda.synchronize()
+    ref = oracle.embed_rows(fmt, oracle.pack_planes(fmt, c.values, c.scales), n, k, ids_np.reshape(-1), signs_values(c))
+    check_decode(np.concatenate([o.cpu().numpy() for o in o_e]).astype(np.float64), ref)
+    o_g = [torch.full((16, k), float("nan"), dtype=torch.float32, device=DEV) for _ in range(T)]
+    g = _graph(lambda: calls(o_g))
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    for t in range(T):
+        assert torch.equal(o_g[t], o_e[t]), t
+    assert nt.ninfer_device_errors() == 0
