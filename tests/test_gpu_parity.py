@@ -716,3 +716,26 @@ def test_embed_graph_replay(fmt):
     for t in range(T):
         assert torch.equal(o_g[t], o_e[t]), t
     assert nt.ninfer_device_errors() == 0
+
+
+def _sweep_shapes():
+    """24 seeded decode shapes per format: n in [1, 1500], k a multiple of 1024
+    up to 12288 (the rotated path), M in {1, 2, ..., 8}; they cover single CTAs,
+    ragged last CTAs, clusters of two and four and both M = 1 kernels' fallbacks."""
+    rng = np.random.default_rng(2026)
+    out = []
+    for fmt in ("PQ2_0_G128", "PTQ1_0_G128"):
+        for i in range(24):
+            n = int(rng.integers(1, 1501))
+            k = 1024 * int(rng.integers(1, 13))
+            M = 1 if i % 2 == 0 else int(rng.integers(2, 9))
+            out.append((fmt, n, k, M))
+    return out
+
+
+@pytest.mark.parametrize("fmt,n,k,M", _sweep_shapes())
+def test_matmul_decode_shape_sweep(fmt, n, k, M):
+    c = synth.make_case("gateup", n=n, k=k, M=M, seed=1000 + n + k + M)
+    y = run_matmul(fmt, c)
+    ref = oracle_matmul_rows(fmt, c, np.arange(n))
+    check_decode(y, ref)
