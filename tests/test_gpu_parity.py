@@ -739,3 +739,19 @@ def test_matmul_decode_shape_sweep(fmt, n, k, M):
     y = run_matmul(fmt, c)
     ref = oracle_matmul_rows(fmt, c, np.arange(n))
     check_decode(y, ref)
+
+
+def _prefill_sweep_shapes():
+    """8 seeded prefill shapes per format: M in [9, 700] (ragged 192-token
+    tiles), n in [1, 1500] (ragged 128-row tiles), k a multiple of 1024 up to 4096."""
+    rng = np.random.default_rng(2027)
+    return [(fmt, int(rng.integers(1, 1501)), 1024 * int(rng.integers(1, 5)), int(rng.integers(9, 701)))
+            for fmt in ("PQ2_0_G128", "PTQ1_0_G128") for _ in range(8)]
+
+
+@pytest.mark.parametrize("fmt,n,k,M", _prefill_sweep_shapes())
+def test_matmul_prefill_shape_sweep(fmt, n, k, M):
+    c = synth.make_case("prefill", n=n, k=k, M=M, seed=2000 + n + k + M)
+    y = run_matmul(fmt, c)
+    ref = oracle_matmul_rows(fmt, c, np.arange(n))
+    check_prefill(y, ref)
