@@ -260,7 +260,9 @@ __device__ __forceinline__ int group_dot(const uint32_t (&bw)[6], uint32_t hb, c
     return acc[0] + acc[1] + acc[2] + acc[3] + (acc4 >> 2);
 }
 
-template <int kXType>
+// kU: rows per row set of a batch (p.u), 1 or 2, fixed per instance so that the
+// row loop unrolls
+template <int kXType, int kU>
 __global__ void __launch_bounds__(kThreads, 1) gemv_ptq1_int_kernel(const __grid_constant__ Ptq1Params p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -406,8 +408,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_ptq1_int_kernel(const __grid
             if (ok && math) {
                 const uint8_t *sa = smem + p.off_ring + slot * p.slot_bytes;
                 float *part = reinterpret_cast<float *>(smem + p.off_part + slot * p.part_slot_bytes) + gl * p.part_stride;
-#pragma unroll 1
-                for (uint32_t i = 0; i < p.u; ++i) {
+#pragma unroll
+                for (uint32_t i = 0; i < (uint32_t)kU; ++i) {
                     const uint32_t rb = i * p.nsets + set;
                     if (rb >= rows_b) break;
                     const uint8_t *row = sa + rb * rb_b + o_b;
@@ -481,7 +483,7 @@ uint32_t max_clusters(uint32_t C, int smem_limit, int sms) {
     std::lock_guard<std::mutex> lock(mu);
     if (cache[dev][C] > 0) return (uint32_t)cache[dev][C];
     int n = 0;
-    const void *kernel = (const void *)gemv_ptq1_int_kernel<NINFER_BF16>;
+    const void *kernel = (const void *)gemv_ptq1_int_kernel<NINFER_BF16, 2>;
     if (set_smem_attribute(kernel, smem_limit) == NINFER_OK) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(C * ((uint32_t)sms / C));
@@ -494,7 +496,7 @@ uint32_t max_clusters(uint32_t C, int smem_limit, int sms) {
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        if (cudaOccupancyMaxActiveClusters(&n, (void (*)(Ptq1Params))gemv_ptq1_int_kernel<NINFER_BF16>, &cfg) !=
+        if (cudaOccupancyMaxActiveClusters(&n, (void (*)(Ptq1Params))gemv_ptq1_int_kernel<NINFER_BF16, 2>, &cfg) !=
             cudaSuccess)
             n = 0;
         (void)cudaGetLastError();
@@ -674,9 +676,13 @@ int gemv_ptq1_int_launch(const Ptq1Plan &plan, const uint8_t *payload, const nin
     p.wait_cycles = wait_limit_cycles();
     st = device_error_word(&p.err);
     if (st) return st;
-    void (*kernel)(Ptq1Params) = x_dtype == NINFER_F32    ? gemv_ptq1_int_kernel<NINFER_F32>
-                                 : x_dtype == NINFER_BF16 ? gemv_ptq1_int_kernel<NINFER_BF16>
-                                                          : gemv_ptq1_int_kernel<NINFER_F16>;
+    void (*kernel)(Ptq1Params) =
+        plan.u == 1 ? (x_dtype == NINFER_F32    ? gemv_ptq1_int_kernel<NINFER_F32, 1>
+                       : x_dtype == NINFER_BF16 ? gemv_ptq1_int_kernel<NINFER_BF16, 1>
+                                                : gemv_ptq1_int_kernel<NINFER_F16, 1>)
+                    : (x_dtype == NINFER_F32    ? gemv_ptq1_int_kernel<NINFER_F32, 2>
+                       : x_dtype == NINFER_BF16 ? gemv_ptq1_int_kernel<NINFER_BF16, 2>
+                                                : gemv_ptq1_int_kernel<NINFER_F16, 2>);
     st = set_smem_attribute((const void *)kernel, (int)plan.smem);
     if (st) return st;
     cudaLaunchConfig_t cfg = {};
